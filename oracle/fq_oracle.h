@@ -1,0 +1,117 @@
+/* Oracle for the Qwen3 single-token decode step -- TEST INFRASTRUCTURE ONLY.
+ *
+ * A plain, slow CPU implementation in f64 of what the fucina Qwen3 pages define:
+ *   - "The qwen3 descriptor runner" (block style .fused: fused norm+QKV, half-rope
+ *     QK-norm, grouped causal attention over the KvCache, dense / softmax-top-k MoE FFN);
+ *   - "14. Model families", section 14.1 (forwardStep / forwardLastLogits contract) and
+ *     section 14.2 "Qwen3 -- dense and MoE" (Config, validation, forwardStepBatch,
+ *     routerTopK with normalize_selected, tied embeddings).
+ * Storage formats (ggml Q8_0 / Q4_K blocks, fp16 / bf16 / f32) are emulated exactly;
+ * all arithmetic on values is f64.
+ *
+ * Only the tests, the package's smoke check and the benchmark's CPU-baseline leg may
+ * load this library.  It shares no code with the CUDA path.
+ */
+#ifndef FQ_ORACLE_H
+#define FQ_ORACLE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum { OR_Q8_0 = 0, OR_Q4_K = 1, OR_F32 = 2 };
+
+typedef struct or_dims {
+    int vocab, hidden, ffn, layers, n_q, n_kv, head_dim;
+    double eps, theta;
+    int n_exp, n_used, moe_ffn, norm_topk;
+    int wtype;    /* OR_Q8_0 or OR_Q4_K: every linear except the f32 router */
+    int kv_bf16;  /* 1: cache stores bf16 values, 0: f32 values */
+} or_dims;
+
+typedef struct or_model or_model;
+typedef struct or_cache or_cache;
+
+/* threads used for independent output rows (OpenMP); returns the count in effect */
+int or_set_threads(int n);
+
+/* ---- storage codecs ---- */
+double   or_fp16_to_f64(uint16_t h);
+uint16_t or_f64_to_fp16(double v);
+double   or_bf16_to_f64(uint16_t h);
+uint16_t or_f64_to_bf16(double v);
+float    or_f64_to_f32(double v);
+void or_dequant_q8_0(const uint8_t* blocks, size_t n, float* out);
+void or_quant_q8_0(const float* x, size_t n, uint8_t* blocks);
+void or_q4k_scale_min(const uint8_t* s12, int j, int* sc, int* mn);
+void or_q4k_pack_scale_min(const int* sc, const int* mn, uint8_t* s12);
+void or_dequant_q4_k(const uint8_t* blocks, size_t n, float* out);
+void or_quant_q4_k(const float* x, size_t n, uint8_t* blocks);
+
+/* ---- building blocks ---- */
+void or_rmsnorm(const double* x, int n, const float* g, double eps, double* y);
+void or_rope(double* v, int d, int pos, double theta);
+void or_attention(const double* q, const float* K, const float* V, int T, int d, size_t row_stride,
+                  double* o);
+double or_silu(double z);
+void or_router(const double* logits, int n_exp, int k, int norm, int* idx, double* w);
+/* y[r] = sum_c W[r,c] x[c] over a packed [rows, cols] matrix (wtype OR_Q8_0/OR_Q4_K/OR_F32) */
+void or_gemv(int wtype, const void* W, int rows, int cols, const double* x, double* y);
+
+/* ---- model ---- */
+int  or_validate(const or_dims* d);   /* 0 ok, 1 invalid config (section 14.2 validation) */
+or_model* or_model_new(const or_dims* d);
+void or_model_free(or_model* m);
+void or_model_set_global(or_model* m, const void* tok_embd, const float* output_norm, const void* output);
+void or_model_set_layer(or_model* m, int layer, const float* attn_norm, const void* wq, const void* wk,
+                        const void* wv, const float* q_norm, const float* k_norm, const void* wo,
+                        const float* ffn_norm, const void* w_gate, const void* w_up, const void* w_down,
+                        const float* router, const void* gate_exps, const void* up_exps,
+                        const void* down_exps);
+
+or_cache* or_cache_new(const or_model* m, int capacity);
+void or_cache_free(or_cache* c);
+int  or_cache_len(const or_cache* c);
+/* write n prior positions of one layer (values in the cache dtype, given as f32; bf16
+ * caches round them again, which is the identity for bf16 inputs) and set len = pos0+n
+ * once every layer holds them; returns 0 or an error code */
+int  or_cache_write(or_cache* c, int layer, int pos0, int n, const float* k, const float* v);
+int  or_cache_set_len(or_cache* c, int len);
+/* read back [n][n_kv][head_dim] of one layer */
+int  or_cache_read(const or_cache* c, int layer, int pos0, int n, float* k, float* v);
+
+/* status codes mirror the C ABI's contract errors */
+enum { OR_OK = 0, OR_INVALID_CONFIG = 1, OR_INVALID_SEQUENCE_LENGTH = 2, OR_KV_CACHE_OVERFLOW = 3,
+       OR_MISMATCHED_KV_CACHES = 4, OR_INVALID_ARGUMENT = 5 };
+
+/* One decoder layer for one token at absolute position pos (== cache len for this layer),
+ * residual stream x (length hidden) updated in place.  Appends k/v at pos for this layer.
+ * route_idx / route_w (may be NULL) receive the MoE selection. */
+int or_layer_step(const or_model* m, int layer, or_cache* c, int pos, double* x, int* route_idx,
+                  double* route_w);
+
+/* forwardStep with one token at pos0 == cache len: embedding, all layers, output norm and
+ * LM head into logits (vocab, may be NULL to skip the head).  layer_out (may be NULL)
+ * receives the residual stream after every layer, [layers][hidden]; route (may be NULL)
+ * the MoE indices [layers][n_used] and weights. Advances len by one. */
+int or_decode_step(const or_model* m, or_cache* c, int token, int pos0, double* logits,
+                   double* layer_out, int* route_idx, double* route_w);
+
+/* forwardStepBatch: one token per stream, stream s against caches[s]; logits [n][vocab].
+ * Validates the caches first (distinct, same model); all advance by one. */
+int or_decode_step_batch(const or_model* m, or_cache* const* caches, int n, const int* tokens,
+                         double* logits);
+
+/* forwardLastLogits: cacheless causal forward over tokens[0..n), last row's logits */
+int or_forward_last_logits(const or_model* m, const int* tokens, int n, double* logits);
+
+/* index of the largest value, ties to the lowest index */
+int or_argmax(const double* v, int n);
+
+#ifdef __cplusplus
+}
+#endif
+#endif
