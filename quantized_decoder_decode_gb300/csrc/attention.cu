@@ -1,0 +1,308 @@
+// Grouped causal attention of one new query row per sequence against its KvCache, as a
+// split-K flash-decode (sm_103a CUDA cores).
+//
+// The fucina runner page lists, for the .fused block style, half-rope QK-norm and grouped
+// causal attention over the shared KvCache; section 14.1 fixes that a step appends the
+// new K/V at pos == len.  One CTA owns (sequence b, kv head g, chunk s of positions); the
+// G = n_q / n_kv query heads of the group share every K/V row it streams.  Fused here:
+//   * per-head RMSNorm of q and k with the learned gains, then rotate-half RoPE at the
+//     absolute position (cos/sin table), q pre-scaled by log2(e)/sqrt(128);
+//   * the CTA whose chunk holds the new position rounds k and v to the cache dtype,
+//     writes them at pos and uses the rounded values itself;
+//   * scores with one lane per position (16-byte loads along the row), online softmax
+//     in base 2 per 32-position tile, V accumulation with lanes over dimensions;
+//   * partial (m, l, o) per chunk; the last CTA of a (sequence, kv head) to finish
+//     (atomic ticket, no waiting) merges the chunks and writes the head outputs.
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace fq {
+
+namespace {
+
+constexpr int ATT_THREADS = 128;
+constexpr int ATT_WARPS = 4;
+constexpr float LOG2E = 1.4426950408889634f;
+
+template <int KVT> struct KvType;
+template <> struct KvType<0> { using T = float; };
+template <> struct KvType<1> { using T = uint16_t; };
+
+// normalise + rope one head held as 4 dims per lane (dims 4l..4l+3) by one warp
+FQ_DEV void norm_rope_head(float v[4], const float* gain, const float2* rope_row, float eps, int lane) {
+    float ss = v[0] * v[0] + v[1] * v[1] + v[2] * v[2] + v[3] * v[3];
+    ss = warp_sum(ss);
+    float inv = rsqrtf(ss / (float)HEAD_DIM + eps);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) v[j] = v[j] * inv * gain[4 * lane + j];
+    // rotate-half pairing (i, i + 64): lane l < 16 holds i = 4l+j, lane l + 16 holds i + 64
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        float partner = __shfl_xor_sync(0xFFFFFFFFu, v[j], 16);
+        int i = (4 * lane + j) & 63;
+        float2 cs = rope_row[i];
+        v[j] = lane < 16 ? v[j] * cs.x - partner * cs.y : partner * cs.y + v[j] * cs.x;
+    }
+}
+
+template <int KVT>
+FQ_DEV void to_cache(float f, typename KvType<KVT>::T* dst, float& rounded) {
+    if constexpr (KVT == 1) {
+        __nv_bfloat16 h = __float2bfloat16_rn(f);
+        *dst = __bfloat16_as_ushort(h);
+        rounded = __bfloat162float(h);
+    } else {
+        *dst = f;
+        rounded = f;
+    }
+}
+
+template <int KVT, int G>
+__global__ void __launch_bounds__(ATT_THREADS) attn_kernel(const AttnArgs a) {
+    using T = typename KvType<KVT>::T;
+    const int s = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const SeqState ss = a.st->seq[b];
+    const int pos = ss.pos, T_len = pos + 1;
+    const int n_act = (T_len + a.chunk - 1) / a.chunk;
+    const int t0 = s * a.chunk, t1 = min(T_len, t0 + a.chunk);
+    const size_t head_off = ((size_t)a.layer * a.Hkv + g) * (size_t)ss.cap * HEAD_DIM;
+    const T* Kc = reinterpret_cast<const T*>(ss.k) + head_off;
+    const T* Vc = reinterpret_cast<const T*>(ss.v) + head_off;
+
+    // cached rows [t0, min(t1, pos)) were written by earlier steps: warm L2 before waiting
+    if (s < n_act) {
+        int tc = min(t1, pos);
+        if (tc > t0) {
+            size_t rb = HEAD_DIM * sizeof(T);
+            prefetch_l2_range(Kc + (size_t)t0 * HEAD_DIM, (size_t)(tc - t0) * rb, tid, ATT_THREADS);
+            prefetch_l2_range(Vc + (size_t)t0 * HEAD_DIM, (size_t)(tc - t0) * rb, tid, ATT_THREADS);
+        }
+    }
+    pdl_trigger();
+    pdl_wait();
+    if (s >= n_act) return;
+
+    __shared__ __align__(16) float qs[G][HEAD_DIM];
+    __shared__ __align__(16) float kn[HEAD_DIM], vn[HEAD_DIM];
+    __shared__ float ps[ATT_WARPS][G][32];
+    __shared__ float mw[ATT_WARPS][G], lw[ATT_WARPS][G];
+    __shared__ __align__(16) float ow[ATT_WARPS][G][HEAD_DIM];
+    __shared__ int is_last;
+
+    const float* qkv = a.qkv + (size_t)b * a.qkv_stride;
+    const float2* rope_row = a.rope + (size_t)pos * (HEAD_DIM / 2);
+    const float qscale = LOG2E * rsqrtf((float)HEAD_DIM);
+
+    // ---- q heads of the group: RMSNorm, rope, scale
+    for (int hh = warp; hh < G; hh += ATT_WARPS) {
+        int h = g * G + hh;
+        float4 raw = *reinterpret_cast<const float4*>(qkv + (size_t)h * HEAD_DIM + 4 * lane);
+        float v[4] = {raw.x, raw.y, raw.z, raw.w};
+        norm_rope_head(v, a.q_norm, rope_row, a.eps, lane);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) qs[hh][4 * lane + j] = v[j] * qscale;
+    }
+    // ---- the chunk holding the new position appends k, v (rounded as stored)
+    const bool owns_new = (s == n_act - 1);
+    if (owns_new && warp < 2) {
+        T* dst = const_cast<T*>(warp == 0 ? Kc : Vc) + (size_t)pos * HEAD_DIM;
+        const float* src = qkv + (size_t)a.Hq * HEAD_DIM + (size_t)(warp == 0 ? 0 : a.Hkv) * HEAD_DIM +
+                           (size_t)g * HEAD_DIM;
+        float4 raw = *reinterpret_cast<const float4*>(src + 4 * lane);
+        float v[4] = {raw.x, raw.y, raw.z, raw.w};
+        if (warp == 0) norm_rope_head(v, a.k_norm, rope_row, a.eps, lane);
+        float* keep = warp == 0 ? kn : vn;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) to_cache<KVT>(v[j], dst + 4 * lane + j, keep[4 * lane + j]);
+    }
+    __syncthreads();
+
+    // ---- tiles of 32 positions, interleaved over warps
+    float m_run[G], l_run[G], acc[G][4];
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+        m_run[h] = -INFINITY;
+        l_run[h] = 0.f;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[h][j] = 0.f;
+    }
+    for (int tb = t0 + warp * 32; tb < t1; tb += ATT_WARPS * 32) {
+        const int t = tb + lane;
+        const bool valid = t < t1;
+        float sc[G];
+#pragma unroll
+        for (int h = 0; h < G; ++h) sc[h] = 0.f;
+        if (valid) {
+            if (t == pos) {
+#pragma unroll 4
+                for (int d = 0; d < HEAD_DIM; d += 4) {
+                    float4 k4 = *reinterpret_cast<const float4*>(kn + d);
+#pragma unroll
+                    for (int h = 0; h < G; ++h) {
+                        float4 q4 = *reinterpret_cast<const float4*>(&qs[h][d]);
+                        sc[h] += q4.x * k4.x + q4.y * k4.y + q4.z * k4.z + q4.w * k4.w;
+                    }
+                }
+            } else {
+                const T* krow = Kc + (size_t)t * HEAD_DIM;
+                if constexpr (KVT == 1) {
+#pragma unroll 4
+                    for (int c = 0; c < HEAD_DIM / 8; ++c) {
+                        uint4 w = ld_stream16(krow + 8 * c);
+                        float k8[8] = {bf_lo(w.x), bf_hi(w.x), bf_lo(w.y), bf_hi(w.y),
+                                       bf_lo(w.z), bf_hi(w.z), bf_lo(w.w), bf_hi(w.w)};
+#pragma unroll
+                        for (int h = 0; h < G; ++h) {
+                            float4 qa = *reinterpret_cast<const float4*>(&qs[h][8 * c]);
+                            float4 qb = *reinterpret_cast<const float4*>(&qs[h][8 * c + 4]);
+                            sc[h] += qa.x * k8[0] + qa.y * k8[1] + qa.z * k8[2] + qa.w * k8[3] + qb.x * k8[4] +
+                                     qb.y * k8[5] + qb.z * k8[6] + qb.w * k8[7];
+                        }
+                    }
+                } else {
+#pragma unroll 4
+                    for (int c = 0; c < HEAD_DIM / 4; ++c) {
+                        uint4 w = ld_stream16(krow + 4 * c);
+#pragma unroll
+                        for (int h = 0; h < G; ++h) {
+                            float4 q4 = *reinterpret_cast<const float4*>(&qs[h][4 * c]);
+                            sc[h] += q4.x * __uint_as_float(w.x) + q4.y * __uint_as_float(w.y) +
+                                     q4.z * __uint_as_float(w.z) + q4.w * __uint_as_float(w.w);
+                        }
+                    }
+                }
+            }
+        }
+        // online softmax over the tile (base 2; q carries log2(e)/sqrt(D))
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+            float mt = warp_max(valid ? sc[h] : -INFINITY);
+            float mnew = fmaxf(m_run[h], mt);
+            float corr = exp2f(m_run[h] - mnew);
+            float p = valid ? exp2f(sc[h] - mnew) : 0.f;
+            l_run[h] = l_run[h] * corr + warp_sum(p);
+            m_run[h] = mnew;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) acc[h][j] *= corr;
+            ps[warp][h][lane] = p;
+        }
+        __syncwarp();
+        const int nvalid = min(32, t1 - tb);
+        for (int i = 0; i < nvalid; ++i) {
+            const int ti = tb + i;
+            float v4[4];
+            if (ti == pos) {
+                float4 x = *reinterpret_cast<const float4*>(vn + 4 * lane);
+                v4[0] = x.x; v4[1] = x.y; v4[2] = x.z; v4[3] = x.w;
+            } else if constexpr (KVT == 1) {
+                uint2 w = ld_stream8(Vc + (size_t)ti * HEAD_DIM + 4 * lane);
+                v4[0] = bf_lo(w.x); v4[1] = bf_hi(w.x); v4[2] = bf_lo(w.y); v4[3] = bf_hi(w.y);
+            } else {
+                uint4 w = ld_stream16(Vc + (size_t)ti * HEAD_DIM + 4 * lane);
+                v4[0] = __uint_as_float(w.x); v4[1] = __uint_as_float(w.y);
+                v4[2] = __uint_as_float(w.z); v4[3] = __uint_as_float(w.w);
+            }
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+                float p = ps[warp][h][i];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) acc[h][j] = fmaf(p, v4[j], acc[h][j]);
+            }
+        }
+        __syncwarp();
+    }
+
+    // ---- merge the warps of the CTA
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+        if (lane == 0) { mw[warp][h] = m_run[h]; lw[warp][h] = l_run[h]; }
+        *reinterpret_cast<float4*>(&ow[warp][h][4 * lane]) = make_float4(acc[h][0], acc[h][1], acc[h][2], acc[h][3]);
+    }
+    __syncthreads();
+    const int d = tid;   // one dimension per thread
+    float* outb = a.out + (size_t)b * a.Hq * HEAD_DIM;
+    for (int h = 0; h < G; ++h) {
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < ATT_WARPS; ++w) M = fmaxf(M, mw[w][h]);
+        float L = 0.f, O = 0.f;
+#pragma unroll
+        for (int w = 0; w < ATT_WARPS; ++w) {
+            float c = mw[w][h] == -INFINITY ? 0.f : exp2f(mw[w][h] - M);
+            L += lw[w][h] * c;
+            O += ow[w][h][d] * c;
+        }
+        const int hq = g * G + h;
+        if (n_act == 1) {
+            outb[(size_t)hq * HEAD_DIM + d] = O / L;
+        } else {
+            float* p = a.part + (((size_t)b * a.Hq + hq) * a.splits + s) * (HEAD_DIM + 2);
+            if (d == 0) { p[0] = M; p[1] = L; }
+            p[2 + d] = O;
+        }
+    }
+    if (n_act == 1) return;
+
+    // ---- last CTA of this (sequence, kv head) merges the chunks
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) {
+        uint32_t* ctr = a.counters + (size_t)b * a.Hkv + g;
+        uint32_t prev = atomicAdd(ctr, 1u);
+        is_last = (prev == (uint32_t)(n_act - 1));
+        if (is_last) *ctr = 0u;   // every chunk has arrived: re-arm for the next use
+    }
+    __syncthreads();
+    if (!is_last) return;
+    __threadfence();
+    for (int h = 0; h < G; ++h) {
+        const int hq = g * G + h;
+        const float* base = a.part + ((size_t)b * a.Hq + hq) * a.splits * (HEAD_DIM + 2);
+        float M = -INFINITY;
+        for (int c = 0; c < n_act; ++c) M = fmaxf(M, __ldcg(base + (size_t)c * (HEAD_DIM + 2)));
+        float L = 0.f, O = 0.f;
+        for (int c = 0; c < n_act; ++c) {
+            const float* p = base + (size_t)c * (HEAD_DIM + 2);
+            float w = exp2f(__ldcg(p) - M);
+            L += __ldcg(p + 1) * w;
+            O += __ldcg(p + 2 + d) * w;
+        }
+        outb[(size_t)hq * HEAD_DIM + d] = O / L;
+    }
+}
+
+template <int KVT, int G>
+void launch_t(const AttnArgs& a, cudaStream_t s, bool pdl) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(a.splits, a.Hkv, a.n);
+    cfg.blockDim = dim3(ATT_THREADS);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    cudaLaunchKernelEx(&cfg, attn_kernel<KVT, G>, a);
+}
+
+template <int KVT>
+void launch_kv(const AttnArgs& a, cudaStream_t s, bool pdl) {
+    switch (a.Hq / a.Hkv) {
+        case 1: launch_t<KVT, 1>(a, s, pdl); break;
+        case 2: launch_t<KVT, 2>(a, s, pdl); break;
+        case 4: launch_t<KVT, 4>(a, s, pdl); break;
+        case 8: launch_t<KVT, 8>(a, s, pdl); break;
+        default: break;   // rejected at descriptor validation
+    }
+}
+
+}  // namespace
+
+void launch_attention(const AttnArgs& a, cudaStream_t s, bool pdl) {
+    if (a.kv_bf16) launch_kv<1>(a, s, pdl);
+    else launch_kv<0>(a, s, pdl);
+}
+
+}  // namespace fq

@@ -1,0 +1,348 @@
+// Dequantise-in-register GEMV for the decode step (CUDA cores, sm_103a).
+//
+// y[b][r] = sum_k W[r][k] * xin[b][k] for a handful of activation rows b, where W is a
+// ggml Q8_0 or Q4_K matrix (fucina "14. Model families" 14.1: quantised weights stay
+// resident in their GGUF dtype and run their own packed kernels).  Each weight byte is
+// read once per step with 128-bit streaming loads; codes become exact floats in registers
+// (byte-permute into the mantissa of 2^23) and meet the activations, which sit in shared
+// memory, in f32 fused multiply-adds.  Warps reduce with shuffles.
+//
+// Fused around the contraction:
+//   prologue  RMSNorm of the input rows (the runner page's "fused norm+QKV projection",
+//             also used before gate_up and the LM head);
+//   epilogues plain store (QKV), residual add (O and down projections), SwiGLU over
+//             interleaved gate/up rows, and logits + argmax keys for greedy decoding.
+//
+// Q8_0 block sums use the factorisation sum_i (d q_i) x_i = d * sum_i q_i x_i.  Q4_K uses
+// (d sc) q - dmin mn per 32-element sub-block, i.e. d sc * sum q x - dmin mn * sum x, with
+// the activation sums per 16 elements computed once per CTA.
+
+#include "common.cuh"
+#include "kernels.h"
+#include "quant.cuh"
+
+namespace fq {
+
+namespace {
+
+constexpr int THREADS = 256;
+constexpr int WARPS = THREADS / 32;
+
+// Q8_0 unit: 16 consecutive codes of one row (16 bytes) sharing one fp16 scale.
+// Q4_K unit: 16 bytes of nibbles = 16 elements of sub-block 2c (low) and 16 of 2c+1 (high).
+template <int FMT> struct Unit;
+template <> struct Unit<FMT_Q8_0> { static constexpr int ELEMS = 16; };
+template <> struct Unit<FMT_Q4_K> { static constexpr int ELEMS = 32; };
+template <> struct Unit<FMT_F32> { static constexpr int ELEMS = 4; };
+
+struct Raw {
+    uint4 q;        // 16 bytes of codes (Q8_0, Q4_K) or 4 floats (F32)
+    uint4 hdr;      // Q4_K: d, dmin, 12 scale bytes
+    uint16_t sc;    // Q8_0 scale
+};
+
+template <int FMT>
+FQ_DEV Raw load_unit(const QMat& W, int row, int u) {
+    Raw r;
+    if constexpr (FMT == FMT_Q8_0) {
+        r.q = ld_stream16(W.q + (size_t)row * W.K + (size_t)u * 16);
+        r.sc = ld_stream2(W.s + (size_t)row * (W.K / 32) + (u >> 1));
+    } else if constexpr (FMT == FMT_Q4_K) {
+        const uint8_t* blk = W.q + (size_t)row * ((size_t)W.K / 256 * 144) + (size_t)(u >> 3) * 144;
+        int c = (u & 7) >> 1, h = u & 1;
+        r.q = ld_stream16(blk + 16 + 32 * c + 16 * h);
+        r.hdr = ld_stream16(blk);
+    } else {
+        r.q = ld_stream16((const float*)W.q + (size_t)row * W.K + (size_t)u * 4);
+    }
+    return r;
+}
+
+// Partial dot of one unit with activation row xs (shared memory), xsum16: per-16 sums.
+template <int FMT>
+FQ_DEV float dot_unit(const Raw& r, int u, const float* xs, const float* xsum16) {
+    if constexpr (FMT == FMT_Q8_0) {
+        const float4* xv = reinterpret_cast<const float4*>(xs + u * 16);
+        float f[16];
+        s8x4_to_f32(r.q.x, f);
+        s8x4_to_f32(r.q.y, f + 4);
+        s8x4_to_f32(r.q.z, f + 8);
+        s8x4_to_f32(r.q.w, f + 12);
+        float acc = 0.f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            float4 x = xv[i];
+            acc = fmaf(f[4 * i + 0], x.x, acc);
+            acc = fmaf(f[4 * i + 1], x.y, acc);
+            acc = fmaf(f[4 * i + 2], x.z, acc);
+            acc = fmaf(f[4 * i + 3], x.w, acc);
+        }
+        return h2f(r.sc) * acc;
+    } else if constexpr (FMT == FMT_Q4_K) {
+        int sb = u >> 3, c = (u & 7) >> 1, h = u & 1;
+        int e_lo = sb * 256 + 64 * c + 16 * h;          // first element of the low half
+        int e_hi = e_lo + 32;
+        const float4* xl = reinterpret_cast<const float4*>(xs + e_lo);
+        const float4* xh = reinterpret_cast<const float4*>(xs + e_hi);
+        uint32_t w[4] = {r.q.x, r.q.y, r.q.z, r.q.w};
+        float slo = 0.f, shi = 0.f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            float lo[4], hi[4];
+            u8x4_to_f32(w[i] & 0x0F0F0F0Fu, lo);
+            u8x4_to_f32((w[i] >> 4) & 0x0F0F0F0Fu, hi);
+            float4 a = xl[i], b = xh[i];
+            slo = fmaf(lo[0], a.x, slo); slo = fmaf(lo[1], a.y, slo);
+            slo = fmaf(lo[2], a.z, slo); slo = fmaf(lo[3], a.w, slo);
+            shi = fmaf(hi[0], b.x, shi); shi = fmaf(hi[1], b.y, shi);
+            shi = fmaf(hi[2], b.z, shi); shi = fmaf(hi[3], b.w, shi);
+        }
+        float d = h2f((unsigned short)(r.hdr.x & 0xFFFFu)), dmin = h2f((unsigned short)(r.hdr.x >> 16));
+        uint32_t sc0, mn0, sc1, mn1;
+        q4k_scale_min(r.hdr, 2 * c, sc0, mn0);
+        q4k_scale_min(r.hdr, 2 * c + 1, sc1, mn1);
+        float d1 = d * (float)sc0, m1 = dmin * (float)mn0, d2 = d * (float)sc1, m2 = dmin * (float)mn1;
+        return d1 * slo - m1 * xsum16[e_lo >> 4] + d2 * shi - m2 * xsum16[e_hi >> 4];
+    } else {
+        float4 x = reinterpret_cast<const float4*>(xs)[u];
+        return __uint_as_float(r.q.x) * x.x + __uint_as_float(r.q.y) * x.y + __uint_as_float(r.q.z) * x.z +
+               __uint_as_float(r.q.w) * x.w;
+    }
+}
+
+template <int FMT, int R, int NBG>
+__global__ void __launch_bounds__(THREADS) gemv_kernel(const GemvArgs a) {
+    extern __shared__ __align__(16) float smem[];
+    QMat W = a.W;
+    const int K = W.K;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int ksplit = a.ksplit;
+    const int rows_per_cta = (WARPS / ksplit) * R;
+    const int r0 = blockIdx.x * rows_per_cta;
+    int B = a.B;
+    const int32_t* ptok = nullptr;
+    const int32_t* pslot = nullptr;
+
+    if (a.route == nullptr) {
+        // weights do not depend on earlier kernels: start streaming them into L2 now
+        int nrows = min(rows_per_cta, W.N - r0);
+        if (nrows > 0) {
+            size_t rb = W.row_bytes();
+            prefetch_l2_range(W.q + (size_t)r0 * rb, (size_t)nrows * rb, tid, THREADS);
+            if (FMT == FMT_Q8_0 && ((size_t)r0 * (K / 32) * 2) % 16 == 0)
+                prefetch_l2_range(W.s + (size_t)r0 * (K / 32), ((size_t)nrows * (K / 32) * 2) & ~(size_t)15, tid,
+                                  THREADS);
+        }
+        pdl_trigger();
+        pdl_wait();
+    } else {
+        // the expert and its tokens come from the route the previous kernel wrote
+        pdl_trigger();
+        pdl_wait();
+        const MoeRoute* rt = a.route;
+        const int ae = blockIdx.y;
+        if (ae >= rt->n_active) return;
+        const int e = rt->expert[ae], p0 = rt->start[ae];
+        B = rt->start[ae + 1] - p0;
+        ptok = rt->pair_token + p0;
+        pslot = rt->pair_slot + p0;
+        W.N = a.rows_per_expert;
+        W.q += (size_t)e * a.rows_per_expert * W.row_bytes();
+        if (W.s) W.s += (size_t)e * a.rows_per_expert * (K / 32);
+    }
+    auto in_row = [&](int b) -> const float* {
+        size_t r = ptok ? (a.x_by_pair ? (size_t)ptok[b] * a.moe_k + pslot[b] : (size_t)ptok[b]) : (size_t)b;
+        return a.x + r * a.x_stride;
+    };
+    auto out_row = [&](int b) -> float* {
+        size_t r = ptok ? (size_t)ptok[b] * a.moe_k + pslot[b] : (size_t)b;
+        return a.y + r * a.y_stride;
+    };
+
+    float* xs = smem;                                   // [NBG][K]
+    float* xsum16 = smem + NBG * K;                     // [NBG][K/16] (Q4_K)
+    float* red = xsum16 + (FMT == FMT_Q4_K ? NBG * (K / 16) : 0);   // [WARPS][R][NBG] + 32
+    __shared__ unsigned long long best[NBG];
+
+    const int n_units = K / Unit<FMT>::ELEMS;
+    const int rg = warp / ksplit, kp = warp % ksplit;
+    const int upp = (n_units + ksplit - 1) / ksplit;
+    const int u_begin = kp * upp, u_end = min(n_units, u_begin + upp);
+    const int row_base = r0 + rg * R;
+
+    for (int b0 = 0; b0 < B; b0 += NBG) {
+        const int nb = min(NBG, B - b0);
+        // ---- prologue: input rows (RMSNorm-ed when a gain is given) into shared memory
+        for (int b = 0; b < nb; ++b) {
+            const float* xin = in_row(b0 + b);
+            float inv = 1.f;
+            if (a.norm_g) {
+                float ss = 0.f;
+                for (int k = tid * 4; k < K; k += THREADS * 4) {
+                    float4 v = *reinterpret_cast<const float4*>(xin + k);
+                    ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+                }
+                ss = block_sum(ss, red + WARPS * R * NBG);
+                inv = rsqrtf(ss / (float)K + a.eps);
+            }
+            for (int k = tid * 4; k < K; k += THREADS * 4) {
+                float4 v = *reinterpret_cast<const float4*>(xin + k);
+                if (a.norm_g) {
+                    float4 g = *reinterpret_cast<const float4*>(a.norm_g + k);
+                    v.x = v.x * inv * g.x; v.y = v.y * inv * g.y; v.z = v.z * inv * g.z; v.w = v.w * inv * g.w;
+                }
+                *reinterpret_cast<float4*>(xs + b * K + k) = v;
+                if (a.xn_out && blockIdx.x == 0)
+                    *reinterpret_cast<float4*>(a.xn_out + (size_t)(b0 + b) * a.xn_stride + k) = v;
+            }
+        }
+        if (tid < NBG) best[tid] = 0ull;
+        __syncthreads();
+        if (FMT == FMT_Q4_K) {
+            for (int i = tid; i < nb * (K / 16); i += THREADS) {
+                int b = i / (K / 16), j = i % (K / 16);
+                const float4* p = reinterpret_cast<const float4*>(xs + b * K + 16 * j);
+                float s = 0.f;
+#pragma unroll
+                for (int t = 0; t < 4; ++t) { float4 v = p[t]; s += v.x + v.y + v.z + v.w; }
+                xsum16[b * (K / 16) + j] = s;
+            }
+            __syncthreads();
+        }
+
+        // ---- main loop: R rows per warp, lanes stride over the units of this K part
+        float acc[R][NBG];
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+            for (int b = 0; b < NBG; ++b) acc[r][b] = 0.f;
+
+        bool row_ok[R];
+#pragma unroll
+        for (int r = 0; r < R; ++r) row_ok[r] = row_base + r < W.N;
+
+        for (int u = u_begin + lane; u < u_end; u += 32) {
+            Raw raw[R];
+#pragma unroll
+            for (int r = 0; r < R; ++r)
+                if (row_ok[r]) raw[r] = load_unit<FMT>(W, row_base + r, u);
+#pragma unroll
+            for (int b = 0; b < NBG; ++b) {
+                if (b < nb) {
+#pragma unroll
+                    for (int r = 0; r < R; ++r)
+                        if (row_ok[r]) acc[r][b] += dot_unit<FMT>(raw[r], u, xs + b * K, xsum16 + b * (K / 16));
+                }
+            }
+        }
+
+        // ---- reduce: lanes, then the K parts of a row group
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+            for (int b = 0; b < NBG; ++b) acc[r][b] = warp_sum(acc[r][b]);
+        if (ksplit > 1) {
+            if (lane == 0)
+#pragma unroll
+                for (int r = 0; r < R; ++r)
+#pragma unroll
+                    for (int b = 0; b < NBG; ++b) red[(warp * R + r) * NBG + b] = acc[r][b];
+            __syncthreads();
+            if (kp == 0 && lane == 0) {
+                for (int w = 1; w < ksplit; ++w)
+#pragma unroll
+                    for (int r = 0; r < R; ++r)
+#pragma unroll
+                        for (int b = 0; b < NBG; ++b) acc[r][b] += red[((warp + w) * R + r) * NBG + b];
+            }
+        }
+
+        // ---- epilogue (one lane per row group)
+        if (kp == 0 && lane == 0) {
+            for (int b = 0; b < nb; ++b) {
+                float* yrow = out_row(b0 + b);
+                if (a.epi == EPI_SWIGLU) {
+#pragma unroll
+                    for (int r = 0; r + 1 < R; r += 2)
+                        if (row_ok[r + 1]) yrow[(row_base + r) >> 1] = silu(acc[r][b]) * acc[r + 1][b];
+                } else {
+                    unsigned long long kbest = 0ull;
+#pragma unroll
+                    for (int r = 0; r < R; ++r) {
+                        if (!row_ok[r]) continue;
+                        int row = row_base + r;
+                        if (a.epi == EPI_ADD) yrow[row] += acc[r][b];
+                        else yrow[row] = acc[r][b];
+                        if (a.epi == EPI_LOGITS) {
+                            unsigned long long kk = argmax_key(acc[r][b], (uint32_t)row);
+                            kbest = kk > kbest ? kk : kbest;
+                        }
+                    }
+                    if (a.epi == EPI_LOGITS) atomicMax(&best[b], kbest);
+                }
+            }
+        }
+        if (a.epi == EPI_LOGITS) {
+            __syncthreads();
+            if (tid < nb) atomicMax(&a.st->keys[b0 + tid], best[tid]);
+        }
+        __syncthreads();
+    }
+}
+
+template <int FMT, int R, int NBG>
+void launch_t(const GemvArgs& a, cudaStream_t s, bool pdl) {
+    const int rows_per_cta = (WARPS / a.ksplit) * R;
+    const int rows = a.route ? a.rows_per_expert : a.W.N;
+    dim3 grid((rows + rows_per_cta - 1) / rows_per_cta, a.route ? a.max_experts : 1);
+    size_t smem = (size_t)NBG * a.W.K * 4 + (FMT == FMT_Q4_K ? (size_t)NBG * (a.W.K / 16) * 4 : 0) +
+                  (WARPS * R * NBG + 32) * 4;
+    auto kern = gemv_kernel<FMT, R, NBG>;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    cudaLaunchKernelEx(&cfg, kern, a);
+}
+
+template <int FMT, int R, int NBG>
+void prepare_t() {
+    cudaFuncSetAttribute(gemv_kernel<FMT, R, NBG>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+}
+
+}  // namespace
+
+void gemv_prepare() {
+    prepare_t<FMT_Q8_0, 4, 1>();
+    prepare_t<FMT_Q8_0, 4, 4>();
+    prepare_t<FMT_Q4_K, 2, 1>();
+    prepare_t<FMT_Q4_K, 2, 4>();
+    prepare_t<FMT_F32, 4, 1>();
+    prepare_t<FMT_F32, 4, 4>();
+}
+
+void launch_gemv(const GemvArgs& a, cudaStream_t s, bool pdl) {
+    const bool one = a.B == 1;
+    switch (a.W.fmt) {
+        case FMT_Q8_0:
+            if (one) launch_t<FMT_Q8_0, 4, 1>(a, s, pdl);
+            else launch_t<FMT_Q8_0, 4, 4>(a, s, pdl);
+            break;
+        case FMT_Q4_K:
+            if (one) launch_t<FMT_Q4_K, 2, 1>(a, s, pdl);
+            else launch_t<FMT_Q4_K, 2, 4>(a, s, pdl);
+            break;
+        default:
+            if (one) launch_t<FMT_F32, 4, 1>(a, s, pdl);
+            else launch_t<FMT_F32, 4, 4>(a, s, pdl);
+            break;
+    }
+}
+
+}  // namespace fq

@@ -1,0 +1,163 @@
+// Device data layouts and kernel launchers of the fq decode path.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#ifdef __CUDACC__
+#define FQ_HD __host__ __device__
+#else
+#define FQ_HD
+#endif
+
+namespace fq {
+
+constexpr int HEAD_DIM = 128;      // the only head_dim the kernels are built for
+constexpr int MAX_TOPK = 8;
+constexpr int MAX_EXPERTS = 256;
+
+enum Fmt : int { FMT_F32 = 0, FMT_BF16 = 1, FMT_Q8_0 = 8, FMT_Q4_K = 12 };
+
+// One device-resident weight matrix [N rows, K cols].
+//   Q8_0: repacked into two 16-byte-aligned planes, q int8 [N][K] and s fp16 [N][K/32]
+//         (the same bytes as the ggml blocks, split so that 16-byte loads line up);
+//   Q4_K: ggml super-blocks as stored, [N][K/256 * 144] bytes (already 16-byte aligned);
+//   F32 : plain row-major floats in q.
+struct QMat {
+    int fmt = FMT_F32;
+    int N = 0, K = 0;
+    const uint8_t* q = nullptr;
+    const uint16_t* s = nullptr;
+    FQ_HD size_t row_bytes() const {
+        return fmt == FMT_Q8_0 ? (size_t)K : fmt == FMT_Q4_K ? (size_t)K / 256 * 144 : (size_t)K * 4;
+    }
+    FQ_HD size_t bytes() const {   // algorithmic bytes of the whole matrix (ggml-equivalent size)
+        return fmt == FMT_Q8_0 ? (size_t)N * K / 32 * 34 : (size_t)N * row_bytes();
+    }
+};
+
+// Per-sequence state of one step, resident in the per-stream workspace.  Written by the
+// set-up kernel before a step (or a chain of greedy steps); read by every kernel, so a
+// captured graph is independent of the token, the positions and the cache pointers.
+struct SeqState {
+    int32_t token;        // token consumed by this step's embedding
+    int32_t pos;          // absolute position of the new token (== cache len)
+    int32_t cap;          // cache capacity
+    int32_t pad;
+    void* k;              // cache planes, [layer][kv_head][cap][head_dim]
+    void* v;
+};
+
+constexpr int MAX_SEQ = 64;
+
+struct StepState {
+    SeqState seq[MAX_SEQ];
+    unsigned long long keys[MAX_SEQ];   // argmax keys of the current step
+    int32_t step;                       // greedy step counter
+    uint32_t lm_counter;                // CTAs of the LM head that finished
+    int32_t* tokens_out;                // greedy output [n_steps][n] or null
+    float* logits;                      // [n][vocab] or null
+    int32_t greedy;                     // feed argmax back and advance positions
+    int32_t n;
+};
+
+// GEMV / small-batch GEMM on CUDA cores:  y[b][r] (op)= sum_k W[r][k] * xin[b][k]
+enum Epi : int { EPI_STORE = 0, EPI_ADD = 1, EPI_SWIGLU = 2, EPI_LOGITS = 3 };
+
+struct GemvArgs {
+    QMat W;
+    int B = 1;                    // activation rows
+    const float* x = nullptr;     // input [B][x_stride]
+    int x_stride = 0;
+    const float* norm_g = nullptr;// RMSNorm prologue gain (null: input used as is)
+    float eps = 1e-6f;
+    float* y = nullptr;           // output [B][y_stride]
+    int y_stride = 0;
+    int epi = EPI_STORE;          // SWIGLU: rows interleaved (2i gate, 2i+1 up) -> y[b][i]
+    int ksplit = 1;               // warps of a row group splitting K (1, 2, 4, 8)
+    StepState* st = nullptr;      // EPI_LOGITS: argmax keys and the greedy hand-off
+    float* xn_out = nullptr;      // optional: CTA 0 stores the normalised input [B][K]
+    int xn_stride = 0;
+    // expert mode (MoE): blockIdx.y = active expert slot of `route`; W holds every expert's
+    // rows_per_expert rows; activation rows are that expert's (token, slot) pairs
+    const struct MoeRoute* route = nullptr;
+    int moe_k = 0;
+    int rows_per_expert = 0;
+    int x_by_pair = 0;            // input row = token*moe_k + slot (else token)
+    int max_experts = 0;          // grid.y
+};
+
+void launch_gemv(const GemvArgs& a, cudaStream_t s, bool pdl);
+// one-time kernel attributes (large dynamic shared memory); call before any graph capture
+void gemv_prepare();
+
+// Attention with fused QK-norm + rope + KV append (one query row per sequence).
+struct AttnArgs {
+    const float* qkv;             // [n][(Hq + 2 Hkv) * 128] raw projections
+    int qkv_stride;
+    const float* q_norm;          // [128]
+    const float* k_norm;          // [128]
+    const float2* rope;           // [max_pos][64] (cos, sin)
+    float eps;
+    int Hq, Hkv;
+    int layer;
+    int kv_bf16;                  // 1: bf16 cache, 0: f32 cache
+    int chunk;                    // positions per CTA (multiple of 32)
+    int splits;                   // grid.x
+    const StepState* st;
+    float* part;                  // [n][Hq][splits][130] partial (m, l, o[128])
+    uint32_t* counters;           // [n][Hkv]
+    float* out;                   // [n][Hq * 128]
+    int n;
+};
+
+void launch_attention(const AttnArgs& a, cudaStream_t s, bool pdl);
+
+// Embedding rows -> x [n][H]
+void launch_embed(const QMat& emb, const StepState* st, int n, float* x, cudaStream_t s, bool pdl);
+
+// Write the step state (tokens, positions, caches) before a step or a greedy chain.
+struct SetupArgs {
+    int n;
+    int greedy;
+    int32_t* tokens_out;
+    float* logits;
+    int32_t token[MAX_SEQ];
+    int32_t pos[MAX_SEQ];
+    int32_t cap[MAX_SEQ];
+    void* k[MAX_SEQ];
+    void* v[MAX_SEQ];
+};
+void launch_setup(StepState* st, const SetupArgs& a, cudaStream_t s);
+
+// LM-head finisher: decode argmax keys, hand the token to the next step.
+void launch_lm_finish(StepState* st, int n, int vocab, cudaStream_t s, bool pdl);
+
+// MoE: router logits + softmax top-k + grouping of (token, slot) pairs by expert.
+struct MoeRoute {
+    int32_t n_active;                     // distinct experts in use
+    int32_t expert[256];                  // active expert ids, ascending
+    int32_t start[257];                   // pair ranges per active expert
+    int32_t pair_token[MAX_SEQ * 8];      // grouped pairs: token index
+    int32_t pair_slot[MAX_SEQ * 8];       //                slot j of that token
+    int32_t idx[MAX_SEQ * 8];             // [n][k] chosen experts
+    float w[MAX_SEQ * 8];                 // [n][k] weights
+};
+// softmax top-k over router logits [n][E] and the grouping of pairs by expert (one CTA)
+void launch_moe_route(const float* logits, int E, int k, int n, int norm_topk, MoeRoute* route, cudaStream_t s,
+                      bool pdl);
+// x[b] += sum_j w[b][j] * y[b*k + j]
+void launch_moe_combine(float* x, const float* y, const MoeRoute* route, int n, int k, int H, cudaStream_t s,
+                        bool pdl);
+
+// Load-time helpers
+// Source row r lands in destination row (r / group) * group_stride + (r % group) * step + off
+// (fusing q/k/v, interleaving gate/up rows, stacking experts).
+void launch_repack_q8_0(const uint8_t* ggml, int64_t rows, int64_t cols, uint8_t* q, uint16_t* sc, int64_t group,
+                        int64_t group_stride, int64_t step, int64_t off, cudaStream_t s);
+void launch_copy_rows(const uint8_t* src, int64_t rows, int64_t row_bytes, uint8_t* dst, int64_t group,
+                      int64_t group_stride, int64_t step, int64_t off, cudaStream_t s);
+void launch_rope_table(float2* tab, int max_pos, double theta, cudaStream_t s);
+void launch_dequant(const QMat& W, int64_t row0, int64_t n_rows, float* out, cudaStream_t s);
+
+}  // namespace fq

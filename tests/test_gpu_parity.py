@@ -1,0 +1,243 @@
+"""Parity of the CUDA decode path (through the C ABI) with the CPU oracle, on seeded
+synthetic Qwen3-shaped inputs small enough for the oracle to finish in seconds while still
+spanning several GEMV row tiles, several attention chunks and a ragged last tile."""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+import synth.workloads as wl
+from quantized_decoder_decode_gb300 import fq
+from tests.gpu_util import DEV, Pair, assert_layer_close, assert_logits_close, max_err, stream
+
+pytestmark = pytest.mark.gpu
+
+SMALL = wl.Dims(vocab_size=1000, hidden_size=256, intermediate_size=512, num_layers=2, num_attention_heads=4,
+                num_key_value_heads=2)
+SMALL_G4 = dataclasses.replace(SMALL, num_attention_heads=8, num_key_value_heads=2)
+SMALL_MOE = dataclasses.replace(SMALL, num_attention_heads=8, num_key_value_heads=1, num_experts=16,
+                                num_experts_used=4, moe_intermediate_size=256)
+
+
+def workload(dims, wtype="q8_0", kv="bf16", seed=21, **kw):
+    return wl.Workload("t", dims, wtype, kv, seed=seed, **kw)
+
+
+@pytest.fixture
+def pair_factory():
+    made = []
+
+    def make(*a, **k):
+        p = Pair(*a, **k)
+        made.append(p)
+        return p
+    yield make
+    for p in made:
+        p.close()
+
+
+# ---------------------------------------------------------------- dequantisation (bit-exact)
+
+@pytest.mark.parametrize("wtype,dims", [("q8_0", SMALL), ("q4_k", SMALL), ("q8_0", SMALL_MOE), ("q4_k", SMALL_MOE)])
+def test_dequant_rows_bit_exact(pair_factory, wtype, dims):
+    p = pair_factory(workload(dims, wtype), with_oracle=False)
+    d = dims
+    lw = p.W["layers"][1]
+    cases = [(fq.W_TOK_EMBD, p.W["tok_embd"], d.vocab_size, d.hidden_size, 0),
+             (fq.W_OUTPUT, p.W["output"], d.vocab_size, d.hidden_size, 0),
+             (fq.W_Q, lw["wq"], d.q_dim, d.hidden_size, 1), (fq.W_K, lw["wk"], d.kv_dim, d.hidden_size, 1),
+             (fq.W_V, lw["wv"], d.kv_dim, d.hidden_size, 1), (fq.W_O, lw["wo"], d.hidden_size, d.q_dim, 1)]
+    if d.is_moe:
+        E, Fe = d.num_experts, d.moe_intermediate_size
+        cases += [(fq.W_GATE_EXPS, lw["gate_exps"], E * Fe, d.hidden_size, 1),
+                  (fq.W_UP_EXPS, lw["up_exps"], E * Fe, d.hidden_size, 1),
+                  (fq.W_DOWN_EXPS, lw["down_exps"], E * d.hidden_size, Fe, 1)]
+    else:
+        cases += [(fq.W_GATE, lw["w_gate"], d.intermediate_size, d.hidden_size, 1),
+                  (fq.W_UP, lw["w_up"], d.intermediate_size, d.hidden_size, 1),
+                  (fq.W_DOWN, lw["w_down"], d.hidden_size, d.intermediate_size, 1)]
+    for which, host, rows, cols, layer in cases:
+        for row0, n in [(0, 3), (rows - 5, 5), (rows // 2, 17)]:
+            out = torch.empty((n, cols), dtype=torch.float32, device=DEV)
+            fq.fq_dequant_rows(p.model, layer, which, row0, n, out.data_ptr(), stream())
+            torch.cuda.synchronize()
+            ref = oracle.dequant(wtype, host[row0:row0 + n].ravel(), n * cols).reshape(n, cols)
+            assert np.array_equal(out.cpu().numpy().view(np.uint32), ref.view(np.uint32)), (which, row0)
+
+
+# ---------------------------------------------------------------- one decoder layer
+
+def test_layer_step_qwen3_0p6b_layer(pair_factory):
+    """The single 0.6B-shaped layer at its full size: T = 128 prior f32 positions."""
+    w = wl.WORKLOADS["qwen3-0.6b-layer"]
+    p = pair_factory(w, max_positions=1024)
+    kv, oc = p.new_seq(capacity=w.context + 1, ctx=w.context, seq=0)
+    x0 = wl.layer_input(w)
+    x = torch.from_numpy(x0.copy()).to(DEV)
+    fq.fq_layer_step(p.model, 0, kv, w.context, x.data_ptr(), stream())
+    torch.cuda.synchronize()
+    ref, _, _ = p.om.layer_step(0, oc, w.context, x0.astype(np.float64))
+    assert_layer_close(x.cpu().numpy(), ref, "layer output")
+    k, v = p.read_kv(kv, 0, w.context, 1)
+    rk, rv = oc.read(0, w.context, 1)
+    assert_layer_close(k, rk, "appended k")
+    assert_layer_close(v, rv, "appended v")
+    assert fq.fq_kv_len(kv) == w.context   # a layer step does not advance len
+    # prior positions are untouched
+    k0, _ = p.read_kv(kv, 0, 0, w.context)
+    rk0, _ = oc.read(0, 0, w.context)
+    assert np.array_equal(k0, rk0)
+
+
+# ---------------------------------------------------------------- decode steps
+
+def _compare_step(p, kvs, ocs, tokens, what):
+    d = p.dims
+    n = len(kvs)
+    logits = torch.empty((n, d.vocab_size), dtype=torch.float32, device=DEV)
+    lo = torch.empty((d.num_layers, n, d.hidden_size), dtype=torch.float32, device=DEV)
+    ri = rw = None
+    if d.is_moe:
+        ri = torch.empty((d.num_layers, n, d.num_experts_used), dtype=torch.int32, device=DEV)
+        rw = torch.empty((d.num_layers, n, d.num_experts_used), dtype=torch.float32, device=DEV)
+    fq.fq_decode_step_trace(p.model, kvs, tokens, logits.data_ptr(), lo.data_ptr(),
+                            ri.data_ptr() if ri is not None else 0, rw.data_ptr() if rw is not None else 0, stream())
+    torch.cuda.synchronize()
+    got_lg, got_lo = logits.cpu().numpy(), lo.cpu().numpy()
+    refs = []
+    for s in range(n):
+        lg, lo_ref, rix, rwx = p.om.decode_step(ocs[s], int(tokens[s]), ocs[s].len, trace=True)
+        refs.append(lg)
+        for L in range(d.num_layers):
+            assert_layer_close(got_lo[L, s], lo_ref[L], f"{what} seq {s} layer {L}")
+            if d.is_moe:
+                assert sorted(ri[L, s].cpu().tolist()) == sorted(rix[L].tolist()), (what, s, L)
+                gw = dict(zip(ri[L, s].cpu().tolist(), rw[L, s].cpu().tolist()))
+                for e, wt in zip(rix[L].tolist(), rwx[L].tolist()):
+                    assert abs(gw[e] - wt) <= 1e-4, (what, s, L, e)
+        assert_logits_close(got_lg[s], lg, f"{what} seq {s} logits")
+    return got_lg, np.stack(refs)
+
+
+@pytest.mark.parametrize("dims,wtype,kv", [(SMALL, "q8_0", "bf16"), (SMALL_G4, "q4_k", "bf16"),
+                                           (SMALL, "q8_0", "f32"), (SMALL_MOE, "q8_0", "bf16")])
+def test_decode_steps_match_oracle(pair_factory, dims, wtype, kv):
+    p = pair_factory(workload(dims, wtype, kv), max_positions=512)
+    kvc, oc = p.new_seq(capacity=128, ctx=100, seq=0)    # 100 + steps spans two 64-position chunks
+    tok = 17
+    for step in range(3):
+        got, ref = _compare_step(p, [kvc], [oc], [tok], f"step {step}")
+        tok = oracle.argmax(ref[0])                      # teacher-forced on the oracle's token
+    assert fq.fq_kv_len(kvc) == 103
+
+
+@pytest.mark.parametrize("dims", [SMALL_G4, SMALL_MOE])
+def test_batch_ragged_matches_oracle(pair_factory, dims):
+    p = pair_factory(workload(dims, "q8_0", "bf16", seed=33), max_positions=1024)
+    ctxs = [37, 100, 250, 1, 64]
+    kvs, ocs = [], []
+    for s, c in enumerate(ctxs):
+        kvc, oc = p.new_seq(capacity=300, ctx=c, seq=s)
+        kvs.append(kvc)
+        ocs.append(oc)
+    toks = synth.uniform_i32(33, 99, len(ctxs), 0, dims.vocab_size)
+    for step in range(2):
+        _, ref = _compare_step(p, kvs, ocs, toks, f"batch step {step}")
+        toks = ref.argmax(axis=1)
+
+
+def test_graph_replay_equals_direct_launches(pair_factory):
+    p = pair_factory(workload(SMALL_G4, "q8_0", "bf16"), max_positions=512, with_oracle=False)
+    a, _ = p.new_seq(capacity=256, ctx=150, seq=0, oracle_cache=False)
+    b, _ = p.new_seq(capacity=256, ctx=150, seq=0, oracle_cache=False)
+    la = torch.empty(SMALL_G4.vocab_size, dtype=torch.float32, device=DEV)
+    lb = torch.empty_like(la)
+    for t in (5, 6, 7):
+        fq.fq_decode_step(p.model, a, t, fq.fq_kv_len(a), la.data_ptr(), stream())        # graph
+        fq.fq_decode_step_trace(p.model, [b], [t], lb.data_ptr(), 0, 0, 0, stream())      # direct
+        torch.cuda.synchronize()
+        assert torch.equal(la, lb)
+
+
+def test_cached_steps_equal_oracle_cacheless_forward(pair_factory):
+    """The pages' own check: last logits of a cached prefill equal the no-cache forward."""
+    p = pair_factory(workload(SMALL, "q8_0", "bf16", seed=44), max_positions=256)
+    kvc, _ = p.new_seq(capacity=64, ctx=0, seq=0, oracle_cache=False)
+    toks = synth.uniform_i32(44, 5, 40, 0, SMALL.vocab_size)
+    logits = torch.empty(SMALL.vocab_size, dtype=torch.float32, device=DEV)
+    for pos, t in enumerate(toks):
+        fq.fq_decode_step(p.model, kvc, int(t), pos, logits.data_ptr(), stream())
+    torch.cuda.synchronize()
+    ref = p.om.forward_last_logits(toks)
+    assert_logits_close(logits.cpu().numpy(), ref, "cached vs cacheless")
+
+
+def test_greedy_chain_matches_oracle(pair_factory):
+    p = pair_factory(workload(SMALL_G4, "q8_0", "bf16", seed=55), max_positions=512)
+    ctxs = [90, 200]
+    kvs, ocs = [], []
+    for s, c in enumerate(ctxs):
+        kvc, oc = p.new_seq(capacity=256, ctx=c, seq=s)
+        kvs.append(kvc)
+        ocs.append(oc)
+    steps = 6
+    out = torch.empty((steps, 2), dtype=torch.int32, device=DEV)
+    logits = torch.empty((2, SMALL_G4.vocab_size), dtype=torch.float32, device=DEV)
+    first = [3, 4]
+    fq.fq_decode_greedy(p.model, kvs, first, steps, out.data_ptr(), logits.data_ptr(), stream())
+    torch.cuda.synchronize()
+    got = out.cpu().numpy()
+    for s in range(2):
+        tok, parted = first[s], False
+        for i in range(steps):
+            lg = p.om.decode_step(ocs[s], tok, ocs[s].len)
+            order = np.argsort(-lg)
+            if got[i, s] != order[0]:
+                gap = lg[order[0]] - lg[order[1]]
+                assert gap < 4e-2, f"seq {s} step {i}: token {got[i, s]} vs {order[0]} (gap {gap})"
+                parted = True                             # a near-tie: the chains may part here
+                break
+            tok = int(order[0])
+        assert fq.fq_kv_len(kvs[s]) == ctxs[s] + steps
+        if not parted:                                    # the last step's logits are returned
+            assert_logits_close(logits[s].cpu().numpy(), lg, f"greedy seq {s} last logits")
+
+
+# ---------------------------------------------------------------- contract errors
+
+def test_contract_errors_leave_state_unchanged(pair_factory):
+    p = pair_factory(workload(SMALL, "q8_0", "bf16"), max_positions=256, with_oracle=False)
+    q = pair_factory(workload(SMALL, "q8_0", "bf16"), max_positions=256, with_oracle=False)
+    a, _ = p.new_seq(capacity=8, ctx=7, seq=0, oracle_cache=False)
+    b, _ = p.new_seq(capacity=8, ctx=2, seq=1, oracle_cache=False)
+    other, _ = q.new_seq(capacity=8, ctx=2, seq=0, oracle_cache=False)
+    lg = torch.empty((2, SMALL.vocab_size), dtype=torch.float32, device=DEV)
+
+    def status(fn):
+        try:
+            fn()
+        except fq.FqError as e:
+            return e.status
+        return fq.OK
+
+    assert status(lambda: fq.fq_decode_step(p.model, a, 1, 6, lg.data_ptr(), stream())) == fq.INVALID_SEQUENCE_LENGTH
+    assert status(lambda: fq.fq_decode_step(p.model, a, SMALL.vocab_size, 7, lg.data_ptr(), stream())) == \
+        fq.INVALID_ARGUMENT
+    assert status(lambda: fq.fq_decode_step_batch(p.model, [a, a], [1, 2], lg.data_ptr(), stream())) == \
+        fq.MISMATCHED_KV_CACHES
+    assert status(lambda: fq.fq_decode_step_batch(p.model, [a, other], [1, 2], lg.data_ptr(), stream())) == \
+        fq.MISMATCHED_KV_CACHES
+    assert status(lambda: fq.fq_decode_greedy(p.model, [a], [1], 2, 0, 0, stream())) == fq.KV_CACHE_OVERFLOW
+    assert status(lambda: fq.fq_decode_step_batch(p.model, [], [], lg.data_ptr(), stream())) == \
+        fq.INVALID_SEQUENCE_LENGTH
+    assert status(lambda: fq.fq_kv_append(a, 0, 3, 1, lg.data_ptr(), lg.data_ptr(), stream())) == \
+        fq.INVALID_SEQUENCE_LENGTH
+    assert fq.fq_kv_len(a) == 7 and fq.fq_kv_len(b) == 2
+    fq.fq_decode_step(p.model, a, 1, 7, lg.data_ptr(), stream())     # fills the last slot
+    assert fq.fq_kv_len(a) == 8
+    assert status(lambda: fq.fq_decode_step(p.model, a, 1, 8, lg.data_ptr(), stream())) == fq.KV_CACHE_OVERFLOW
+    assert fq.fq_kv_len(a) == 8
+    torch.cuda.synchronize()
