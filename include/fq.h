@@ -101,7 +101,9 @@ typedef struct fq_layer_src {
 } fq_layer_src;
 
 /* tok_embd [vocab, hidden], output_norm f32 [hidden], output [vocab, hidden]; a NULL
- * output.data means tied embeddings (section 14.2 load specifics).  layers: host array of
+ * output.data means tied embeddings (section 14.2 load specifics).  A NULL tok_embd.data
+ * (with a NULL output) loads a layer-only model that serves fq_layer_step alone; the
+ * decode entry points reject it with FQ_ERR_INVALID_ARGUMENT.  layers: host array of
  * num_layers entries. */
 typedef struct fq_weight_src {
     fq_tensor tok_embd, output_norm, output;
@@ -137,6 +139,10 @@ uint32_t fq_kv_capacity(const fq_kv* kv);
 fq_status fq_kv_append(fq_kv* kv, uint32_t layer, uint32_t pos, uint32_t n_pos, const void* k, const void* v,
                        void* stream);
 fq_status fq_kv_commit(fq_kv* kv, uint32_t len);
+/* Rewind to a shorter length (the runner page's decoder contract lists rewind among the
+ * cache capabilities): len <= current len, else INVALID_SEQUENCE_LENGTH.  Positions from
+ * len on keep stale contents until later steps overwrite them.  Host-side only. */
+fq_status fq_kv_rewind(fq_kv* kv, uint32_t len);
 /* Copy positions [pos, pos+n_pos) of one layer out to device buffers in the cache dtype. */
 fq_status fq_kv_read(const fq_kv* kv, uint32_t layer, uint32_t pos, uint32_t n_pos, void* k, void* v,
                      void* stream);
@@ -180,6 +186,13 @@ fq_status fq_decode_step_trace(const fq_model* m, fq_kv* const* caches, uint32_t
                                float* logits, float* layer_out, int32_t* route_idx, float* route_w,
                                void* stream);
 
+/* fq_layer_step that also copies the layer's intermediates out (device f32, any may be
+ * NULL): qkv [(Hq + 2 Hkv) * head_dim] raw projections before QK-norm/rope (rows q | k | v),
+ * attn [Hq * head_dim] attention output per q head, ffn [intermediate_size] SwiGLU
+ * activations (dense models). */
+fq_status fq_layer_step_trace(const fq_model* m, uint32_t layer, fq_kv* kv, uint32_t pos, float* x, float* qkv,
+                              float* attn, float* ffn, void* stream);
+
 /* Which weight to inspect with fq_dequant_rows. */
 typedef enum fq_weight_id {
     FQ_W_TOK_EMBD = 0, FQ_W_OUTPUT = 1, FQ_W_Q = 2, FQ_W_K = 3, FQ_W_V = 4, FQ_W_O = 5,
@@ -191,6 +204,14 @@ typedef enum fq_weight_id {
  * decoding the GEMV kernels use. */
 fq_status fq_dequant_rows(const fq_model* m, uint32_t layer, fq_weight_id which, uint64_t row0, uint64_t n_rows,
                           float* out, void* stream);
+
+/* y[b][r] = sum_k W[r][k] x[b][k] for b < n (n <= 64) over one device-resident weight, with
+ * the launch configuration the decode step uses: x device f32 [n][cols], y device f32
+ * [n][rows].  which: FQ_W_Q selects the whole fused QKV matrix (rows q | k | v),
+ * FQ_W_GATE the fused gate_up matrix (rows interleaved gate_0, up_0, gate_1, ...),
+ * FQ_W_O, FQ_W_DOWN, FQ_W_OUTPUT the others (layer ignored for FQ_W_OUTPUT). */
+fq_status fq_gemv(const fq_model* m, uint32_t layer, fq_weight_id which, uint32_t n, const float* x, float* y,
+                  void* stream);
 
 const char* fq_last_error(void);
 const char* fq_status_str(fq_status s);

@@ -575,7 +575,8 @@ int or_layer_step(const or_model* m, int layer, or_cache* c, int pos, double* x,
             c->k[c->idx(layer, h, pos) + i] = to_cache(m, k[(size_t)h * D + i]);
             c->v[c->idx(layer, h, pos) + i] = to_cache(m, v[(size_t)h * D + i]);
         }
-    for (int h = 0; h < d.n_q; ++h) {
+#pragma omp parallel for schedule(static)
+    for (int h = 0; h < d.n_q; ++h) {   // heads are independent outputs
         int g = h / group;
         or_attention(&q[(size_t)h * D], &c->k[c->idx(layer, g, 0)], &c->v[c->idx(layer, g, 0)], pos + 1, D, D,
                      &o[(size_t)h * D]);

@@ -370,6 +370,7 @@ fq_status run_body(const Body& b, cudaStream_t s, int kv_bf16, int reps) {
 
 fq_status check_caches(const fq_model* m, fq_kv* const* caches, uint32_t n, uint32_t steps) {
     if (!m || !caches) return fail(FQ_ERR_INVALID_ARGUMENT, "null model or caches");
+    if (!m->tok_embd.q) return fail(FQ_ERR_INVALID_ARGUMENT, "layer-only model (loaded without tok_embd)");
     if (n == 0) return fail(FQ_ERR_INVALID_SEQUENCE_LENGTH, "empty batch");
     if (n > (uint32_t)MAX_SEQ) return fail(FQ_ERR_INVALID_ARGUMENT, "batch %u exceeds %d", n, MAX_SEQ);
     for (uint32_t s = 0; s < n; ++s) {
@@ -550,10 +551,12 @@ fq_status fq_load_weights(const fq_desc* d, const fq_weight_src* src, void* stre
     const uint64_t H = p.hidden_size, D = p.head_dim, Hq = p.num_attention_heads, Hkv = p.num_key_value_heads;
     const bool moe = p.num_experts > 0;
     // ---- validate everything before allocating
-    TRY(check_tensor(src->tok_embd, "tok_embd", p.vocab_size, H, true));
-    TRY(check_tensor(src->output_norm, "output_norm", H, 1, false) == FQ_OK
-            ? FQ_OK
-            : check_tensor(src->output_norm, "output_norm", 1, H, false));
+    const bool has_embd = src->tok_embd.data != nullptr;   // layer-only models have none
+    if (has_embd) TRY(check_tensor(src->tok_embd, "tok_embd", p.vocab_size, H, true));
+    if (!has_embd && src->output.data)
+        return fail(FQ_ERR_INVALID_ARGUMENT, "output without tok_embd");
+    if (has_embd && check_tensor(src->output_norm, "output_norm", H, 1, false) != FQ_OK)
+        TRY(check_tensor(src->output_norm, "output_norm", 1, H, false));
     if (src->output.data) TRY(check_tensor(src->output, "output", p.vocab_size, H, true));
     for (uint32_t L = 0; L < p.num_layers; ++L) {
         const fq_layer_src& l = src->layers[L];
@@ -612,10 +615,12 @@ fq_status fq_load_weights(const fq_desc* d, const fq_weight_src* src, void* stre
         return st;
     };
     fq_status st = [&]() -> fq_status {
-        TRY(ld.plain(src->tok_embd, m->tok_embd));
-        TRY(ld.vec(src->output_norm, &m->output_norm, H));
-        if (src->output.data) TRY(ld.plain(src->output, m->output));
-        else m->output = m->tok_embd;   // tied embeddings
+        if (has_embd) {
+            TRY(ld.plain(src->tok_embd, m->tok_embd));
+            TRY(ld.vec(src->output_norm, &m->output_norm, H));
+            if (src->output.data) TRY(ld.plain(src->output, m->output));
+            else m->output = m->tok_embd;   // tied embeddings
+        }
         for (uint32_t L = 0; L < p.num_layers; ++L) {
             const fq_layer_src& l = src->layers[L];
             LayerW& w = m->layers[L];
@@ -745,6 +750,13 @@ fq_status fq_kv_commit(fq_kv* kv, uint32_t len) {
     return FQ_OK;
 }
 
+fq_status fq_kv_rewind(fq_kv* kv, uint32_t len) {
+    if (!kv) return fail(FQ_ERR_INVALID_ARGUMENT, "null cache");
+    if (len > kv->len) return fail(FQ_ERR_INVALID_SEQUENCE_LENGTH, "rewind to %u beyond len %u", len, kv->len);
+    kv->len = len;
+    return FQ_OK;
+}
+
 fq_status fq_kv_read(const fq_kv* kv, uint32_t layer, uint32_t pos, uint32_t n_pos, void* k, void* v, void* stream) {
     if (!kv || !k || !v) return fail(FQ_ERR_INVALID_ARGUMENT, "null argument");
     if (layer >= kv->m->d.p.num_layers) return fail(FQ_ERR_INVALID_ARGUMENT, "layer %u out of range", layer);
@@ -829,6 +841,43 @@ fq_status fq_decode_step_trace(const fq_model* m, fq_kv* const* caches, uint32_t
     return FQ_OK;
 }
 
+fq_status fq_layer_step_trace(const fq_model* m, uint32_t layer, fq_kv* kv, uint32_t pos, float* x, float* qkv,
+                              float* attn, float* ffn, void* stream) {
+    TRY(fq_layer_step(m, layer, kv, pos, x, stream));
+    cudaStream_t s = (cudaStream_t)stream;
+    Workspace* w;
+    TRY(ensure_ws(m, s, 1, kv->cap, &w));
+    const auto& p = m->d.p;
+    if (qkv) CK(cudaMemcpyAsync(qkv, w->qkv, sizeof(float) * m->qkv_rows(), cudaMemcpyDeviceToDevice, s));
+    if (attn)
+        CK(cudaMemcpyAsync(attn, w->attn, sizeof(float) * p.num_attention_heads * HEAD_DIM, cudaMemcpyDeviceToDevice, s));
+    if (ffn && !m->moe()) CK(cudaMemcpyAsync(ffn, w->h, sizeof(float) * p.intermediate_size, cudaMemcpyDeviceToDevice, s));
+    return FQ_OK;
+}
+
+fq_status fq_gemv(const fq_model* m, uint32_t layer, fq_weight_id which, uint32_t n, const float* x, float* y,
+                  void* stream) {
+    if (!m || !x || !y) return fail(FQ_ERR_INVALID_ARGUMENT, "null argument");
+    if (n == 0 || n > (uint32_t)MAX_SEQ) return fail(FQ_ERR_INVALID_ARGUMENT, "n must be 1..%d", MAX_SEQ);
+    if (which != FQ_W_OUTPUT && layer >= m->d.p.num_layers) return fail(FQ_ERR_INVALID_ARGUMENT, "layer out of range");
+    QMat W;
+    switch (which) {
+        case FQ_W_Q: W = m->layers[layer].qkv; break;
+        case FQ_W_O: W = m->layers[layer].o; break;
+        case FQ_W_GATE: W = m->layers[layer].gate_up; break;
+        case FQ_W_DOWN: W = m->layers[layer].down; break;
+        case FQ_W_OUTPUT: W = m->output; break;
+        default: return fail(FQ_ERR_INVALID_ARGUMENT, "fq_gemv takes FQ_W_Q, FQ_W_O, FQ_W_GATE, FQ_W_DOWN or FQ_W_OUTPUT");
+    }
+    if (!W.q) return fail(FQ_ERR_INVALID_ARGUMENT, "weight not present in this model");
+    GemvArgs g;
+    g.W = W; g.B = (int)n; g.x = x; g.x_stride = W.K; g.y = y; g.y_stride = W.N; g.epi = EPI_STORE;
+    g.ksplit = choose_ksplit(W, rows_per_warp(W));
+    launch_gemv(g, (cudaStream_t)stream, false);
+    CK(cudaGetLastError());
+    return FQ_OK;
+}
+
 fq_status fq_dequant_rows(const fq_model* m, uint32_t layer, fq_weight_id which, uint64_t row0, uint64_t n_rows,
                           float* out, void* stream) {
     if (!m || !out) return fail(FQ_ERR_INVALID_ARGUMENT, "null argument");
@@ -840,8 +889,8 @@ fq_status fq_dequant_rows(const fq_model* m, uint32_t layer, fq_weight_id which,
     QMat W;
     uint64_t rows = 0, off = 0, step = 1, group = 0, gstride = 0;
     switch (which) {
-        case FQ_W_TOK_EMBD: W = m->tok_embd; rows = W.N; break;
-        case FQ_W_OUTPUT: W = m->output; rows = W.N; break;
+        case FQ_W_TOK_EMBD: W = m->tok_embd; rows = W.N; if (!W.q) return fail(FQ_ERR_INVALID_ARGUMENT, "no tok_embd"); break;
+        case FQ_W_OUTPUT: W = m->output; rows = W.N; if (!W.q) return fail(FQ_ERR_INVALID_ARGUMENT, "no output"); break;
         case FQ_W_Q: W = lw->qkv; rows = Hq * D; break;
         case FQ_W_K: W = lw->qkv; rows = Hkv * D; off = Hq * D; break;
         case FQ_W_V: W = lw->qkv; rows = Hkv * D; off = (Hq + Hkv) * D; break;

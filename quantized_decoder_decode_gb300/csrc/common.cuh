@@ -71,23 +71,25 @@ FQ_DEV float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
 FQ_DEV float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
 // Four int8 codes of one 32-bit word to exact floats: bias each byte to unsigned, place it
-// in the low mantissa bits of 2^23 (byte permute), subtract 2^23 + 128.
+// in the low mantissa bits of 2^23 (byte permute: selector nibble 0 picks source byte k of
+// u, nibbles 1-2 pick zero bytes and nibble 3 the 0x4B exponent byte of the constant),
+// subtract 2^23 + 128.
 FQ_DEV void s8x4_to_f32(uint32_t w, float* f) {
     uint32_t u = w ^ 0x80808080u;
     const float bias = 8388736.0f;  // 2^23 + 128
-    f[0] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7444)) - bias;
-    f[1] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7445)) - bias;
-    f[2] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7446)) - bias;
-    f[3] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7447)) - bias;
+    f[0] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7440)) - bias;
+    f[1] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7441)) - bias;
+    f[2] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7442)) - bias;
+    f[3] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7443)) - bias;
 }
 
 // Four unsigned bytes (values 0..255) to exact floats.
 FQ_DEV void u8x4_to_f32(uint32_t u, float* f) {
     const float bias = 8388608.0f;  // 2^23
-    f[0] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7444)) - bias;
-    f[1] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7445)) - bias;
-    f[2] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7446)) - bias;
-    f[3] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7447)) - bias;
+    f[0] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7440)) - bias;
+    f[1] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7441)) - bias;
+    f[2] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7442)) - bias;
+    f[3] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7443)) - bias;
 }
 
 // Order-preserving map of a float to u32 (larger float -> larger key).

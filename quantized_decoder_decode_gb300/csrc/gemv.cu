@@ -312,19 +312,25 @@ void launch_t(const GemvArgs& a, cudaStream_t s, bool pdl) {
 }
 
 template <int FMT, int R, int NBG>
-void prepare_t() {
-    cudaFuncSetAttribute(gemv_kernel<FMT, R, NBG>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+void prepare_t(int optin) {
+    cudaFuncAttributes fa;
+    cudaFuncGetAttributes(&fa, gemv_kernel<FMT, R, NBG>);
+    cudaFuncSetAttribute(gemv_kernel<FMT, R, NBG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         optin - (int)fa.sharedSizeBytes);
 }
 
 }  // namespace
 
 void gemv_prepare() {
-    prepare_t<FMT_Q8_0, 4, 1>();
-    prepare_t<FMT_Q8_0, 4, 4>();
-    prepare_t<FMT_Q4_K, 2, 1>();
-    prepare_t<FMT_Q4_K, 2, 4>();
-    prepare_t<FMT_F32, 4, 1>();
-    prepare_t<FMT_F32, 4, 4>();
+    int dev = 0, optin = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    prepare_t<FMT_Q8_0, 4, 1>(optin);
+    prepare_t<FMT_Q8_0, 4, 4>(optin);
+    prepare_t<FMT_Q4_K, 2, 1>(optin);
+    prepare_t<FMT_Q4_K, 2, 4>(optin);
+    prepare_t<FMT_F32, 4, 1>(optin);
+    prepare_t<FMT_F32, 4, 4>(optin);
 }
 
 void launch_gemv(const GemvArgs& a, cudaStream_t s, bool pdl) {

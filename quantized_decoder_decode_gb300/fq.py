@@ -78,6 +78,7 @@ def lib():
                 "fq_kv_init": [vp, u32, ctypes.c_int, vp],
                 "fq_kv_append": [vp, u32, u32, u32, vp, vp, vp],
                 "fq_kv_commit": [vp, u32],
+                "fq_kv_rewind": [vp, u32],
                 "fq_kv_read": [vp, u32, u32, u32, vp, vp, vp],
                 "fq_layer_step": [vp, u32, vp, u32, vp, vp],
                 "fq_decode_step": [vp, vp, i32, u32, vp, vp],
@@ -85,6 +86,8 @@ def lib():
                 "fq_decode_greedy": [vp, vp, u32, vp, u32, vp, vp, vp],
                 "fq_decode_step_trace": [vp, vp, u32, vp, vp, vp, vp, vp, vp],
                 "fq_dequant_rows": [vp, u32, ctypes.c_int, u64, u64, vp, vp],
+                "fq_layer_step_trace": [vp, u32, vp, u32, vp, vp, vp, vp, vp],
+                "fq_gemv": [vp, u32, ctypes.c_int, u32, vp, vp, vp],
             }
             for name, args in sig.items():
                 fn = getattr(L, name)
@@ -107,8 +110,9 @@ def lib():
 
 
 EXPORTED = ("fq_desc_init", "fq_load_weights", "fq_model_free", "fq_kv_init", "fq_kv_free", "fq_kv_len",
-            "fq_kv_capacity", "fq_kv_append", "fq_kv_commit", "fq_kv_read", "fq_layer_step", "fq_decode_step",
-            "fq_decode_step_batch", "fq_decode_greedy", "fq_decode_step_trace", "fq_dequant_rows", "fq_last_error",
+            "fq_kv_capacity", "fq_kv_append", "fq_kv_commit", "fq_kv_rewind", "fq_kv_read", "fq_layer_step", "fq_decode_step",
+            "fq_decode_step_batch", "fq_decode_greedy", "fq_decode_step_trace", "fq_dequant_rows", "fq_layer_step_trace",
+            "fq_gemv", "fq_last_error",
             "fq_status_str")
 
 
@@ -208,6 +212,10 @@ def fq_kv_commit(kv: int, length: int) -> None:
     _check(lib().fq_kv_commit(kv, length), "fq_kv_commit")
 
 
+def fq_kv_rewind(kv: int, length: int) -> None:
+    _check(lib().fq_kv_rewind(kv, length), "fq_kv_rewind")
+
+
 def fq_kv_read(kv: int, layer: int, pos: int, n_pos: int, k_ptr: int, v_ptr: int, stream: int = 0) -> None:
     _check(lib().fq_kv_read(kv, layer, pos, n_pos, k_ptr, v_ptr, stream), "fq_kv_read")
 
@@ -250,3 +258,13 @@ def fq_decode_step_trace(model: int, kvs, tokens, logits_ptr: int, layer_out_ptr
 
 def fq_dequant_rows(model: int, layer: int, which: int, row0: int, n_rows: int, out_ptr: int, stream: int = 0) -> None:
     _check(lib().fq_dequant_rows(model, layer, which, row0, n_rows, out_ptr, stream), "fq_dequant_rows")
+
+
+def fq_layer_step_trace(model: int, layer: int, kv: int, pos: int, x_ptr: int, qkv_ptr: int = 0, attn_ptr: int = 0,
+                        ffn_ptr: int = 0, stream: int = 0) -> None:
+    _check(lib().fq_layer_step_trace(model, layer, kv, pos, x_ptr, qkv_ptr or None, attn_ptr or None, ffn_ptr or None,
+                                     stream), "fq_layer_step_trace")
+
+
+def fq_gemv(model: int, layer: int, which: int, n: int, x_ptr: int, y_ptr: int, stream: int = 0) -> None:
+    _check(lib().fq_gemv(model, layer, which, n, x_ptr, y_ptr, stream), "fq_gemv")
