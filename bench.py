@@ -1,0 +1,395 @@
+"""Decode throughput of the fq library on GB300.
+
+Workload (N=1 line): the full 28-layer Qwen3-0.6B-shaped decoder with Q8_0 weights
+(seeded N(0, 0.02)), Q8_0 embedding and LM head, bf16 KV cache; 2048 positions are filled
+by running the model on seeded random token ids; then greedy decode chains of 64 steps,
+batch 1, each chain starting from those 2048 cached positions (the cache is rewound
+between chains, so every timed step is the same workload).  One "step" = one decode token
+through the whole hot path (embedding, 28 x [norm+QKV, QK-norm+rope+append+attention,
+O-proj, norm+gate_up+SwiGLU, down], output norm, LM head, argmax).
+
+Timing: W warm-up steps, then exactly K steps bracketed by a barrier and synchronisation,
+CUDA events on the launching stream, max over ranks.  Every step streams ~0.87 GB
+(weights + KV), far more than the 129 MB L2, so no flush is needed between steps.
+
+--impl reference times the CPU oracle (the f64 restatement of the pages) on the same
+workload: each of its steps is one of the 29 units of a decode token (28 layer steps at
+context 2048, then the output norm + LM head), cycling, and tokens/s = (K / 29) / time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode tokens/s at batch 1 and 32; achieved HBM GB/s vs GB300 peak"
+WORKLOAD = "qwen3-0.6b"
+CHAIN = 64
+CONTEXT = 2048
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            j = json.load(f)
+        return float(j["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def step_bytes(dims, ctx: int) -> dict:
+    """Algorithmic bytes of one batch-1 decode step at `ctx` cached positions."""
+    q8 = 34 / 32
+    H, F, L = dims.hidden_size, dims.intermediate_size, dims.num_layers
+    qd, kvd = dims.q_dim, dims.kv_dim
+    layer_w = (qd + 2 * kvd) * H + H * qd + 2 * F * H + H * F
+    weights = L * layer_w * q8 + L * (2 * H + 2 * dims.head_dim) * 4
+    head = dims.vocab_size * H * q8 + H * 4
+    embd_row = H * q8
+    kv_read = 2 * L * kvd * ctx * 2
+    kv_write = 2 * L * kvd * 2
+    return {"weights": weights, "lm_head": head, "embedding_row": embd_row, "kv_read": kv_read,
+            "kv_write": kv_write, "total": weights + head + embd_row + kv_read + kv_write}
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int, ms: int = 100):
+        self.index, self.ms = index, ms
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", f"-lms={self.ms}"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.t.join(timeout=2)
+
+    def summary(self) -> dict:
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": [], "samples": 0}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup(n_gpus: int):
+    import torch
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    return rank, world, local
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v: float, world: int) -> float:
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- CPU oracle (reference arm / baseline)
+
+def oracle_setup(w, W):
+    import oracle
+    import synth.workloads as wl
+    d = w.dims
+    m = oracle.Model(d, W, w.weight_dtype, w.kv_dtype)
+    c = m.new_cache(CONTEXT + 1)
+    for L in range(d.num_layers):
+        k, v = wl.make_kv_prior(w, 0, L, CONTEXT)
+        c.write(L, 0, k, v)
+    c.set_len(CONTEXT)
+    return m, c
+
+
+def oracle_unit(m, c, W, w, i, x):
+    """Unit i % 29 of a decode token: a layer step at context 2048, or the LM head."""
+    import oracle
+    d = w.dims
+    u = i % (d.num_layers + 1)
+    if u < d.num_layers:
+        m.layer_step(u, c, CONTEXT, x)
+    else:
+        xn = oracle.rmsnorm(x, W["output_norm"], d.rms_norm_eps)
+        oracle.gemv(w.weight_dtype, W["output"], d.vocab_size, d.hidden_size, xn)
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    import oracle
+    import synth.workloads as wl
+    w = wl.WORKLOADS[WORKLOAD]
+    W = wl.make_weights(w)
+    m, c = oracle_setup(w, W)
+    threads = oracle.set_threads(0)
+    x = wl.layer_input(w).astype(np.float64)
+    for i in range(args.warmup):
+        oracle_unit(m, c, W, w, i, x)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        oracle_unit(m, c, W, w, i, x)
+    dt = time.perf_counter() - t0
+    units = w.dims.num_layers + 1
+    value = (args.steps / units) / dt
+    sample = (f"{args.steps} oracle units (28 layer steps at context {CONTEXT} + output norm/LM head, cycling; "
+              f"{units} units = one token), KV prior N(0,1) bf16")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_dict(w),
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+def cpu_baseline(w, W, budget_s: float = 15.0) -> dict:
+    """The oracle as it stands, full decode steps at context 2048 on this host's cores."""
+    import oracle
+    m, c = oracle_setup(w, W)
+    threads = oracle.set_threads(0)
+    c.set_len(CONTEXT)
+    n, t0 = 0, time.perf_counter()
+    while True:
+        c.set_len(CONTEXT)
+        m.decode_step(c, 1 + n, CONTEXT)
+        n += 1
+        if time.perf_counter() - t0 >= budget_s or n >= 64:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": n / dt, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": f"{n} full oracle decode steps (28 layers + LM head, f64) at context {CONTEXT}, "
+                      f"KV prior N(0,1) bf16 instead of a model prefill"}
+
+
+def config_dict(w) -> dict:
+    d = w.dims
+    return {"workload": f"{w.name}: Qwen3-0.6B-shaped decoder, {d.num_layers} layers, hidden {d.hidden_size}, "
+                        f"{d.num_attention_heads}q/{d.num_key_value_heads}kv heads x {d.head_dim}, FFN "
+                        f"{d.intermediate_size}, vocab {d.vocab_size}, Q8_0 weights, bf16 KV; {CONTEXT} positions "
+                        f"filled by the model, greedy chains of {CHAIN} steps from context {CONTEXT}",
+            "batch": 1, "context": CONTEXT, "chain": CHAIN, "weights": "q8_0", "kv": "bf16",
+            "l2": "no flush: each step streams ~0.87 GB (weights + KV) >> 129 MB L2"}
+
+
+# ---------------------------------------------------------------- GPU arm
+
+def run_fq(args):
+    import torch
+    import synth
+    import synth.workloads as wl
+    from quantized_decoder_decode_gb300 import fq
+
+    rank, world, local = dist_setup(args.gpus)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    st = torch.cuda.current_stream(dev)
+    stream = st.cuda_stream
+    w = wl.WORKLOADS[WORKLOAD]
+    d = w.dims
+    W = wl.make_weights(w)
+    desc = fq.fq_desc_init(vocab_size=d.vocab_size, hidden_size=d.hidden_size, intermediate_size=d.intermediate_size,
+                           num_layers=d.num_layers, num_attention_heads=d.num_attention_heads,
+                           num_key_value_heads=d.num_key_value_heads, head_dim=d.head_dim,
+                           rms_norm_eps=d.rms_norm_eps, rope_theta=d.rope_theta, max_positions=4096)
+    src, keep = fq.weight_src(desc, W, w.weight_dtype)
+    model = fq.fq_load_weights(desc, src, stream)
+    kv = fq.fq_kv_init(model, CONTEXT + CHAIN, w.kv_dtype)
+
+    # fill 2048 positions by running the model on seeded random ids (not timed)
+    ids = wl.prefill_ids(w)
+    for p in range(CONTEXT - 1):
+        fq.fq_decode_step(model, kv, int(ids[p]), p, 0, stream)
+    toks = torch.empty((max(CHAIN, 1), 1), dtype=torch.int32, device=dev)
+    logits = torch.empty((1, d.vocab_size), dtype=torch.float32, device=dev)
+    fq.fq_decode_greedy(model, [kv], [int(ids[CONTEXT - 1])], 1, toks.data_ptr(), logits.data_ptr(), stream)
+    torch.cuda.synchronize()
+    first = int(toks[0, 0].item())
+
+    def chains(n_steps, sync_each=False, host_tok=None):
+        done = 0
+        while done < n_steps:
+            s = min(CHAIN, n_steps - done)
+            fq.fq_kv_rewind(kv, CONTEXT)
+            fq.fq_decode_greedy(model, [kv], [first], s, toks.data_ptr(), logits.data_ptr(), stream)
+            done += s
+        fq.fq_kv_rewind(kv, CONTEXT)
+
+    chains(max(args.warmup, 3))
+    torch.cuda.synchronize()
+    barrier(world)
+
+    # ---- timed region: exactly K steps
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        torch.cuda.synchronize()
+        barrier(world)
+        torch.cuda.nvtx.range_push("timed")
+        ev0.record(st)
+        chains(args.steps)
+        ev1.record(st)
+        torch.cuda.nvtx.range_pop()
+        torch.cuda.synchronize()
+        barrier(world)
+    dt = ev0.elapsed_time(ev1) / 1e3
+    dt = max_over_ranks(dt, world)
+    value = world * args.steps / dt
+
+    # ---- end to end through the public API with host buffers: per step, the token goes in
+    # from pinned host memory (by value through the call) and the chosen token comes back
+    # to pinned host memory before the next step is issued
+    host_tok = torch.empty(1, dtype=torch.int32, pin_memory=True)
+    e2e_steps = min(args.steps, 4 * CHAIN)
+    torch.cuda.synchronize()
+    barrier(world)
+    t0 = time.perf_counter()
+    tok = first
+    done = 0
+    while done < e2e_steps:
+        s = min(CHAIN, e2e_steps - done)
+        fq.fq_kv_rewind(kv, CONTEXT)
+        tok = first
+        for _ in range(s):
+            fq.fq_decode_greedy(model, [kv], [tok], 1, toks.data_ptr(), 0, stream)
+            host_tok.copy_(toks[0, 0:1], non_blocking=True)
+            st.synchronize()
+            tok = int(host_tok[0])
+        done += s
+    fq.fq_kv_rewind(kv, CONTEXT)
+    e2e_dt = max_over_ranks(time.perf_counter() - t0, world)
+    e2e_value = world * e2e_steps / e2e_dt
+
+    # ---- roofline of the dominant kernel: the Q8_0 dequant GEMV, timed live on the LM
+    # head (151936 x 1024, the largest launch of the step) with CUDA events on its stream
+    peak, peak_kind = measured_peaks()
+    x = torch.randn(d.hidden_size, device=dev)
+    y = torch.empty(d.vocab_size, device=dev)
+    reps = 20
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    for _ in range(3):
+        fq.fq_gemv(model, 0, fq.W_OUTPUT, 1, x.data_ptr(), y.data_ptr(), stream)
+    torch.cuda.synchronize()
+    for a, b in evs:
+        a.record(st)
+        fq.fq_gemv(model, 0, fq.W_OUTPUT, 1, x.data_ptr(), y.data_ptr(), stream)
+        b.record(st)
+    torch.cuda.synchronize()
+    kt = sum(a.elapsed_time(b) for a, b in evs) / reps / 1e3
+    kbytes = d.vocab_size * d.hidden_size * 34 / 32 + d.hidden_size * 4 + d.vocab_size * 4
+    achieved = kbytes / kt / 1e9
+
+    ctx_mean = CONTEXT + (CHAIN - 1) / 2
+    sb = step_bytes(d, int(round(ctx_mean)))
+    step_gbs = sb["total"] / (dt / args.steps) / 1e9
+    launches_per_step = 1 + d.num_layers * 5 + 2
+    n_chains = (args.steps + CHAIN - 1) // CHAIN
+
+    line = None
+    if rank == 0:
+        cb = cpu_baseline(w, W, budget_s=args.cpu_budget) if (world == 1 and not args.no_cpu_baseline) else None
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": max(args.warmup, 3), "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": config_dict(w),
+            "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": 4, "d2h_bytes_per_step": 4,
+                    "steps": e2e_steps},
+            "gpu_launches": args.steps * launches_per_step + n_chains,
+            "roofline": {"bound": "hbm", "kernel": "gemv_kernel<Q8_0> (LM head launch, 151936x1024)",
+                         "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                         "peak_kind": peak_kind, "bytes_per_launch": kbytes, "us_per_launch": kt * 1e6,
+                         "traffic": None},
+            "step_roofline": {"bytes_per_step": sb["total"], "achieved_gbs": step_gbs, "peak": peak,
+                              "frac": step_gbs / peak, "peak_kind": peak_kind,
+                              "breakdown": {k: v for k, v in sb.items() if k != "total"}},
+            "clocks": clk.summary(),
+            "cpu_baseline": cb,
+        }
+        print(json.dumps(line))
+    fq.fq_kv_free(kv)
+    fq.fq_model_free(model)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=6400)
+    ap.add_argument("--warmup", type=int, default=64)
+    ap.add_argument("--impl", default="fq", choices=["fq", "reference"])
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_fq(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())
