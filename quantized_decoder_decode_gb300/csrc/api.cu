@@ -134,14 +134,14 @@ fq_status dalloc(std::vector<void*>& owner, T** p, size_t count) {
     return FQ_OK;
 }
 
-// attention split: enough CTAs to cover the GPU at small batch, bounded chunk for balance
+// attention split: chunks of 128 positions (one 32-position tile per warp) or a multiple,
+// enough CTAs to cover the GPU at small batch, at most 4 tiles per warp for balance
 void attn_split(int n, int Hkv, uint32_t cap_max, int& chunk, int& splits) {
     int target = std::max(1, 304 / std::max(1, n * Hkv));
-    int c = (int)((cap_max + target - 1) / target);
-    c = (c + 31) / 32 * 32;
-    c = std::max(64, std::min(c, 512));
-    chunk = c;
-    splits = (int)((cap_max + c - 1) / c);
+    int m = (int)((cap_max + 128u * target - 1) / (128u * target));
+    m = std::max(1, std::min(m, 4));
+    chunk = 128 * m;
+    splits = (int)((cap_max + chunk - 1) / chunk);
 }
 
 int choose_ksplit(const QMat& W, int R) {

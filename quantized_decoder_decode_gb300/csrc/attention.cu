@@ -119,7 +119,8 @@ __global__ void __launch_bounds__(ATT_THREADS) attn_kernel(const AttnArgs a) {
     }
     __syncthreads();
 
-    // ---- tiles of 32 positions, interleaved over warps
+    // ---- tiles of 32 positions, interleaved over warps; every K and V load of a tile is
+    // issued before any arithmetic so that one memory latency covers the whole tile
     float m_run[G], l_run[G], acc[G][4];
 #pragma unroll
     for (int h = 0; h < G; ++h) {
@@ -128,49 +129,65 @@ __global__ void __launch_bounds__(ATT_THREADS) attn_kernel(const AttnArgs a) {
 #pragma unroll
         for (int j = 0; j < 4; ++j) acc[h][j] = 0.f;
     }
+    constexpr int KW = KVT == 1 ? 16 : 32;      // 16-byte words per K row
+    constexpr int VW = KVT == 1 ? 2 : 4;        // 32-bit words of one lane's 4 V dims
     for (int tb = t0 + warp * 32; tb < t1; tb += ATT_WARPS * 32) {
         const int t = tb + lane;
         const bool valid = t < t1;
+        const bool fresh = t == pos;            // the new position lives in shared memory
+        const int nvalid = min(32, t1 - tb);
         float sc[G];
 #pragma unroll
         for (int h = 0; h < G; ++h) sc[h] = 0.f;
-        if (valid) {
-            if (t == pos) {
-#pragma unroll 4
-                for (int d = 0; d < HEAD_DIM; d += 4) {
-                    float4 k4 = *reinterpret_cast<const float4*>(kn + d);
+        // V words of this lane's 4 dims for the tile's positions (loaded first, used last)
+        uint32_t vr[32][VW];
 #pragma unroll
-                    for (int h = 0; h < G; ++h) {
-                        float4 q4 = *reinterpret_cast<const float4*>(&qs[h][d]);
-                        sc[h] += q4.x * k4.x + q4.y * k4.y + q4.z * k4.z + q4.w * k4.w;
-                    }
-                }
-            } else {
-                const T* krow = Kc + (size_t)t * HEAD_DIM;
+        for (int i = 0; i < 32; ++i) {
+            const int ti = tb + i;
+            if (i < nvalid && ti != pos) {
                 if constexpr (KVT == 1) {
-#pragma unroll 4
-                    for (int c = 0; c < HEAD_DIM / 8; ++c) {
-                        uint4 w = ld_stream16(krow + 8 * c);
-                        float k8[8] = {bf_lo(w.x), bf_hi(w.x), bf_lo(w.y), bf_hi(w.y),
-                                       bf_lo(w.z), bf_hi(w.z), bf_lo(w.w), bf_hi(w.w)};
-#pragma unroll
-                        for (int h = 0; h < G; ++h) {
-                            float4 qa = *reinterpret_cast<const float4*>(&qs[h][8 * c]);
-                            float4 qb = *reinterpret_cast<const float4*>(&qs[h][8 * c + 4]);
-                            sc[h] += qa.x * k8[0] + qa.y * k8[1] + qa.z * k8[2] + qa.w * k8[3] + qb.x * k8[4] +
-                                     qb.y * k8[5] + qb.z * k8[6] + qb.w * k8[7];
-                        }
-                    }
+                    uint2 w = ld_stream8(Vc + (size_t)ti * HEAD_DIM + 4 * lane);
+                    vr[i][0] = w.x; vr[i][1] = w.y;
                 } else {
-#pragma unroll 4
-                    for (int c = 0; c < HEAD_DIM / 4; ++c) {
-                        uint4 w = ld_stream16(krow + 4 * c);
+                    uint4 w = ld_stream16(Vc + (size_t)ti * HEAD_DIM + 4 * lane);
+                    vr[i][0] = w.x; vr[i][1] = w.y; vr[i][2] = w.z; vr[i][3] = w.w;
+                }
+            }
+        }
+        // scores: one lane per position, the whole K row in flight
+        constexpr int KB = 16;                  // words per batch
 #pragma unroll
-                        for (int h = 0; h < G; ++h) {
-                            float4 q4 = *reinterpret_cast<const float4*>(&qs[h][4 * c]);
-                            sc[h] += q4.x * __uint_as_float(w.x) + q4.y * __uint_as_float(w.y) +
-                                     q4.z * __uint_as_float(w.z) + q4.w * __uint_as_float(w.w);
-                        }
+        for (int c0 = 0; c0 < KW; c0 += KB) {
+            uint4 kr[KB];
+            if (valid && !fresh) {
+                const T* krow = Kc + (size_t)t * HEAD_DIM;
+#pragma unroll
+                for (int c = 0; c < KB; ++c) kr[c] = ld_stream16(reinterpret_cast<const char*>(krow) + 16 * (c0 + c));
+            } else {
+#pragma unroll
+                for (int c = 0; c < KB; ++c) kr[c] = make_uint4(0u, 0u, 0u, 0u);   // unused: masked or fresh
+            }
+#pragma unroll
+            for (int c = 0; c < KB; ++c) {
+                float kf[KVT == 1 ? 8 : 4];
+                constexpr int EPW = KVT == 1 ? 8 : 4;   // elements per 16-byte word
+                const int e0 = (c0 + c) * EPW;
+                if (fresh) {
+#pragma unroll
+                    for (int e = 0; e < EPW; ++e) kf[e] = kn[e0 + e];
+                } else if constexpr (KVT == 1) {
+                    kf[0] = bf_lo(kr[c].x); kf[1] = bf_hi(kr[c].x); kf[2] = bf_lo(kr[c].y); kf[3] = bf_hi(kr[c].y);
+                    kf[4] = bf_lo(kr[c].z); kf[5] = bf_hi(kr[c].z); kf[6] = bf_lo(kr[c].w); kf[7] = bf_hi(kr[c].w);
+                } else {
+                    kf[0] = __uint_as_float(kr[c].x); kf[1] = __uint_as_float(kr[c].y);
+                    kf[2] = __uint_as_float(kr[c].z); kf[3] = __uint_as_float(kr[c].w);
+                }
+#pragma unroll
+                for (int h = 0; h < G; ++h) {
+#pragma unroll
+                    for (int e = 0; e < EPW; e += 4) {
+                        float4 q4 = *reinterpret_cast<const float4*>(&qs[h][e0 + e]);
+                        sc[h] += q4.x * kf[e] + q4.y * kf[e + 1] + q4.z * kf[e + 2] + q4.w * kf[e + 3];
                     }
                 }
             }
@@ -189,26 +206,25 @@ __global__ void __launch_bounds__(ATT_THREADS) attn_kernel(const AttnArgs a) {
             ps[warp][h][lane] = p;
         }
         __syncwarp();
-        const int nvalid = min(32, t1 - tb);
-        for (int i = 0; i < nvalid; ++i) {
-            const int ti = tb + i;
-            float v4[4];
-            if (ti == pos) {
-                float4 x = *reinterpret_cast<const float4*>(vn + 4 * lane);
-                v4[0] = x.x; v4[1] = x.y; v4[2] = x.z; v4[3] = x.w;
-            } else if constexpr (KVT == 1) {
-                uint2 w = ld_stream8(Vc + (size_t)ti * HEAD_DIM + 4 * lane);
-                v4[0] = bf_lo(w.x); v4[1] = bf_hi(w.x); v4[2] = bf_lo(w.y); v4[3] = bf_hi(w.y);
-            } else {
-                uint4 w = ld_stream16(Vc + (size_t)ti * HEAD_DIM + 4 * lane);
-                v4[0] = __uint_as_float(w.x); v4[1] = __uint_as_float(w.y);
-                v4[2] = __uint_as_float(w.z); v4[3] = __uint_as_float(w.w);
-            }
 #pragma unroll
-            for (int h = 0; h < G; ++h) {
-                float p = ps[warp][h][i];
+        for (int i = 0; i < 32; ++i) {
+            if (i < nvalid) {
+                float v4[4];
+                if (tb + i == pos) {
+                    float4 x = *reinterpret_cast<const float4*>(vn + 4 * lane);
+                    v4[0] = x.x; v4[1] = x.y; v4[2] = x.z; v4[3] = x.w;
+                } else if constexpr (KVT == 1) {
+                    v4[0] = bf_lo(vr[i][0]); v4[1] = bf_hi(vr[i][0]); v4[2] = bf_lo(vr[i][1]); v4[3] = bf_hi(vr[i][1]);
+                } else {
+                    v4[0] = __uint_as_float(vr[i][0]); v4[1] = __uint_as_float(vr[i][1]);
+                    v4[2] = __uint_as_float(vr[i][2]); v4[3] = __uint_as_float(vr[i][3]);
+                }
 #pragma unroll
-                for (int j = 0; j < 4; ++j) acc[h][j] = fmaf(p, v4[j], acc[h][j]);
+                for (int h = 0; h < G; ++h) {
+                    float p = ps[warp][h][i];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) acc[h][j] = fmaf(p, v4[j], acc[h][j]);
+                }
             }
         }
         __syncwarp();

@@ -21,6 +21,8 @@
 #include "kernels.h"
 #include "quant.cuh"
 
+#include <algorithm>
+
 namespace fq {
 
 namespace {
@@ -58,11 +60,39 @@ FQ_DEV Raw load_unit(const QMat& W, int row, int u) {
     return r;
 }
 
-// Partial dot of one unit with activation row xs (shared memory), xsum16: per-16 sums.
+// Activations of one unit, loaded from shared memory once and shared by the warp's rows.
+template <int FMT> struct XFrag { float v[Unit<FMT>::ELEMS]; };
+
 template <int FMT>
-FQ_DEV float dot_unit(const Raw& r, int u, const float* xs, const float* xsum16) {
+FQ_DEV void load_x(const float* xs, int u, XFrag<FMT>& f) {
     if constexpr (FMT == FMT_Q8_0) {
-        const float4* xv = reinterpret_cast<const float4*>(xs + u * 16);
+        const float4* p = reinterpret_cast<const float4*>(xs + u * 16);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            float4 t = p[i];
+            f.v[4 * i] = t.x; f.v[4 * i + 1] = t.y; f.v[4 * i + 2] = t.z; f.v[4 * i + 3] = t.w;
+        }
+    } else if constexpr (FMT == FMT_Q4_K) {
+        const int e_lo = (u >> 3) * 256 + 64 * ((u & 7) >> 1) + 16 * (u & 1);
+        const float4* pl = reinterpret_cast<const float4*>(xs + e_lo);
+        const float4* ph = reinterpret_cast<const float4*>(xs + e_lo + 32);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            float4 t = pl[i], h = ph[i];
+            f.v[4 * i] = t.x; f.v[4 * i + 1] = t.y; f.v[4 * i + 2] = t.z; f.v[4 * i + 3] = t.w;
+            f.v[16 + 4 * i] = h.x; f.v[16 + 4 * i + 1] = h.y; f.v[16 + 4 * i + 2] = h.z; f.v[16 + 4 * i + 3] = h.w;
+        }
+    } else {
+        float4 t = reinterpret_cast<const float4*>(xs)[u];
+        f.v[0] = t.x; f.v[1] = t.y; f.v[2] = t.z; f.v[3] = t.w;
+    }
+}
+
+// Partial dot of one unit of one row with its activation fragment; xsum16: per-16 sums of
+// the staged activations (Q4_K min terms).
+template <int FMT>
+FQ_DEV float dot_frag(const Raw& r, int u, const XFrag<FMT>& x, const float* xsum16) {
+    if constexpr (FMT == FMT_Q8_0) {
         float f[16];
         s8x4_to_f32(r.q.x, f);
         s8x4_to_f32(r.q.y, f + 4);
@@ -70,20 +100,11 @@ FQ_DEV float dot_unit(const Raw& r, int u, const float* xs, const float* xsum16)
         s8x4_to_f32(r.q.w, f + 12);
         float acc = 0.f;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            float4 x = xv[i];
-            acc = fmaf(f[4 * i + 0], x.x, acc);
-            acc = fmaf(f[4 * i + 1], x.y, acc);
-            acc = fmaf(f[4 * i + 2], x.z, acc);
-            acc = fmaf(f[4 * i + 3], x.w, acc);
-        }
+        for (int i = 0; i < 16; ++i) acc = fmaf(f[i], x.v[i], acc);
         return h2f(r.sc) * acc;
     } else if constexpr (FMT == FMT_Q4_K) {
-        int sb = u >> 3, c = (u & 7) >> 1, h = u & 1;
-        int e_lo = sb * 256 + 64 * c + 16 * h;          // first element of the low half
-        int e_hi = e_lo + 32;
-        const float4* xl = reinterpret_cast<const float4*>(xs + e_lo);
-        const float4* xh = reinterpret_cast<const float4*>(xs + e_hi);
+        const int c = (u & 7) >> 1;
+        const int e_lo = (u >> 3) * 256 + 64 * c + 16 * (u & 1);
         uint32_t w[4] = {r.q.x, r.q.y, r.q.z, r.q.w};
         float slo = 0.f, shi = 0.f;
 #pragma unroll
@@ -91,25 +112,30 @@ FQ_DEV float dot_unit(const Raw& r, int u, const float* xs, const float* xsum16)
             float lo[4], hi[4];
             u8x4_to_f32(w[i] & 0x0F0F0F0Fu, lo);
             u8x4_to_f32((w[i] >> 4) & 0x0F0F0F0Fu, hi);
-            float4 a = xl[i], b = xh[i];
-            slo = fmaf(lo[0], a.x, slo); slo = fmaf(lo[1], a.y, slo);
-            slo = fmaf(lo[2], a.z, slo); slo = fmaf(lo[3], a.w, slo);
-            shi = fmaf(hi[0], b.x, shi); shi = fmaf(hi[1], b.y, shi);
-            shi = fmaf(hi[2], b.z, shi); shi = fmaf(hi[3], b.w, shi);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                slo = fmaf(lo[j], x.v[4 * i + j], slo);
+                shi = fmaf(hi[j], x.v[16 + 4 * i + j], shi);
+            }
         }
         float d = h2f((unsigned short)(r.hdr.x & 0xFFFFu)), dmin = h2f((unsigned short)(r.hdr.x >> 16));
         uint32_t sc0, mn0, sc1, mn1;
         q4k_scale_min(r.hdr, 2 * c, sc0, mn0);
         q4k_scale_min(r.hdr, 2 * c + 1, sc1, mn1);
         float d1 = d * (float)sc0, m1 = dmin * (float)mn0, d2 = d * (float)sc1, m2 = dmin * (float)mn1;
-        return d1 * slo - m1 * xsum16[e_lo >> 4] + d2 * shi - m2 * xsum16[e_hi >> 4];
+        return d1 * slo - m1 * xsum16[e_lo >> 4] + d2 * shi - m2 * xsum16[(e_lo + 32) >> 4];
     } else {
-        float4 x = reinterpret_cast<const float4*>(xs)[u];
-        return __uint_as_float(r.q.x) * x.x + __uint_as_float(r.q.y) * x.y + __uint_as_float(r.q.z) * x.z +
-               __uint_as_float(r.q.w) * x.w;
+        return __uint_as_float(r.q.x) * x.v[0] + __uint_as_float(r.q.y) * x.v[1] + __uint_as_float(r.q.z) * x.v[2] +
+               __uint_as_float(r.q.w) * x.v[3];
     }
 }
 
+// One CTA owns a tile of rows_per_cta = (8 / ksplit) * R rows at a time and walks the tiles
+// with a CTA stride, so the input rows are staged (and their RMS computed) once per CTA.
+// Warp w serves row group w / ksplit over K part w % ksplit; lanes stride over the units of
+// that part, two units per iteration so that 2R independent 16-byte loads are in flight.
+// An RMSNorm prologue stages x * g and applies 1/rms to the finished dot products
+// (W (x/rms * g) = (W (x * g)) / rms), so no block reduction sits before the first load.
 template <int FMT, int R, int NBG>
 __global__ void __launch_bounds__(THREADS) gemv_kernel(const GemvArgs a) {
     extern __shared__ __align__(16) float smem[];
@@ -118,13 +144,13 @@ __global__ void __launch_bounds__(THREADS) gemv_kernel(const GemvArgs a) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int ksplit = a.ksplit;
     const int rows_per_cta = (WARPS / ksplit) * R;
-    const int r0 = blockIdx.x * rows_per_cta;
     int B = a.B;
     const int32_t* ptok = nullptr;
     const int32_t* pslot = nullptr;
 
     if (a.route == nullptr) {
-        // weights do not depend on earlier kernels: start streaming them into L2 now
+        // weights do not depend on earlier kernels: start streaming this CTA's first tile
+        const int r0 = blockIdx.x * rows_per_cta;
         int nrows = min(rows_per_cta, W.N - r0);
         if (nrows > 0) {
             size_t rb = W.row_bytes();
@@ -159,45 +185,58 @@ __global__ void __launch_bounds__(THREADS) gemv_kernel(const GemvArgs a) {
         return a.y + r * a.y_stride;
     };
 
-    float* xs = smem;                                   // [NBG][K]
-    float* xsum16 = smem + NBG * K;                     // [NBG][K/16] (Q4_K)
-    float* red = xsum16 + (FMT == FMT_Q4_K ? NBG * (K / 16) : 0);   // [WARPS][R][NBG] + 32
+    float* xs = smem;                                                 // [NBG][K]
+    float* xsum16 = smem + NBG * K;                                   // [NBG][K/16] (Q4_K)
+    float* red = xsum16 + (FMT == FMT_Q4_K ? NBG * (K / 16) : 0);     // [WARPS][R][NBG]
+    float* ssw = red + WARPS * R * NBG;                               // [WARPS][NBG]
     __shared__ unsigned long long best[NBG];
 
     const int n_units = K / Unit<FMT>::ELEMS;
     const int rg = warp / ksplit, kp = warp % ksplit;
     const int upp = (n_units + ksplit - 1) / ksplit;
     const int u_begin = kp * upp, u_end = min(n_units, u_begin + upp);
-    const int row_base = r0 + rg * R;
+    const int n_tiles = (W.N + rows_per_cta - 1) / rows_per_cta;
 
     for (int b0 = 0; b0 < B; b0 += NBG) {
         const int nb = min(NBG, B - b0);
-        // ---- prologue: input rows (RMSNorm-ed when a gain is given) into shared memory
+        // ---- prologue: x (times the norm gain) into shared memory, partial sums of x^2
         for (int b = 0; b < nb; ++b) {
             const float* xin = in_row(b0 + b);
-            float inv = 1.f;
-            if (a.norm_g) {
-                float ss = 0.f;
-                for (int k = tid * 4; k < K; k += THREADS * 4) {
-                    float4 v = *reinterpret_cast<const float4*>(xin + k);
-                    ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
-                }
-                ss = block_sum(ss, red + WARPS * R * NBG);
-                inv = rsqrtf(ss / (float)K + a.eps);
-            }
+            float ss = 0.f;
             for (int k = tid * 4; k < K; k += THREADS * 4) {
                 float4 v = *reinterpret_cast<const float4*>(xin + k);
+                ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
                 if (a.norm_g) {
                     float4 g = *reinterpret_cast<const float4*>(a.norm_g + k);
-                    v.x = v.x * inv * g.x; v.y = v.y * inv * g.y; v.z = v.z * inv * g.z; v.w = v.w * inv * g.w;
+                    v.x *= g.x; v.y *= g.y; v.z *= g.z; v.w *= g.w;
                 }
                 *reinterpret_cast<float4*>(xs + b * K + k) = v;
-                if (a.xn_out && blockIdx.x == 0)
-                    *reinterpret_cast<float4*>(a.xn_out + (size_t)(b0 + b) * a.xn_stride + k) = v;
             }
+            ss = warp_sum(ss);
+            if (lane == 0) ssw[warp * NBG + b] = ss;
         }
         if (tid < NBG) best[tid] = 0ull;
         __syncthreads();
+        float inv[NBG];
+#pragma unroll
+        for (int b = 0; b < NBG; ++b) {
+            float t = 0.f;
+            if (b < nb)
+                for (int w = 0; w < WARPS; ++w) t += ssw[w * NBG + b];
+            inv[b] = a.norm_g ? rsqrtf(t / (float)K + a.eps) : 1.f;
+        }
+        if (a.xn_out && blockIdx.x == 0) {
+            for (int i = tid * 4; i < nb * K; i += THREADS * 4) {
+                int b = i / K, k = i % K;
+                float4 v = *reinterpret_cast<const float4*>(xs + i);
+                float s = inv[0];
+#pragma unroll
+                for (int bb = 1; bb < NBG; ++bb)
+                    if (bb == b) s = inv[bb];
+                v.x *= s; v.y *= s; v.z *= s; v.w *= s;
+                *reinterpret_cast<float4*>(a.xn_out + (size_t)(b0 + b) * a.xn_stride + k) = v;
+            }
+        }
         if (FMT == FMT_Q4_K) {
             for (int i = tid; i < nb * (K / 16); i += THREADS) {
                 int b = i / (K / 16), j = i % (K / 16);
@@ -210,93 +249,133 @@ __global__ void __launch_bounds__(THREADS) gemv_kernel(const GemvArgs a) {
             __syncthreads();
         }
 
-        // ---- main loop: R rows per warp, lanes stride over the units of this K part
-        float acc[R][NBG];
-#pragma unroll
-        for (int r = 0; r < R; ++r)
-#pragma unroll
-            for (int b = 0; b < NBG; ++b) acc[r][b] = 0.f;
-
-        bool row_ok[R];
-#pragma unroll
-        for (int r = 0; r < R; ++r) row_ok[r] = row_base + r < W.N;
-
-        for (int u = u_begin + lane; u < u_end; u += 32) {
-            Raw raw[R];
+        for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+            const int row_base = tile * rows_per_cta + rg * R;
+            float acc[R][NBG];
 #pragma unroll
             for (int r = 0; r < R; ++r)
-                if (row_ok[r]) raw[r] = load_unit<FMT>(W, row_base + r, u);
 #pragma unroll
-            for (int b = 0; b < NBG; ++b) {
-                if (b < nb) {
+                for (int b = 0; b < NBG; ++b) acc[r][b] = 0.f;
+            bool row_ok[R];
 #pragma unroll
-                    for (int r = 0; r < R; ++r)
-                        if (row_ok[r]) acc[r][b] += dot_unit<FMT>(raw[r], u, xs + b * K, xsum16 + b * (K / 16));
-                }
-            }
-        }
+            for (int r = 0; r < R; ++r) row_ok[r] = row_base + r < W.N;
 
-        // ---- reduce: lanes, then the K parts of a row group
-#pragma unroll
-        for (int r = 0; r < R; ++r)
-#pragma unroll
-            for (int b = 0; b < NBG; ++b) acc[r][b] = warp_sum(acc[r][b]);
-        if (ksplit > 1) {
-            if (lane == 0)
+            int u = u_begin + lane;
+            for (; u + 32 < u_end; u += 64) {
+                Raw r0[R], r1[R];
 #pragma unroll
                 for (int r = 0; r < R; ++r)
+                    if (row_ok[r]) {
+                        r0[r] = load_unit<FMT>(W, row_base + r, u);
+                        r1[r] = load_unit<FMT>(W, row_base + r, u + 32);
+                    }
 #pragma unroll
-                    for (int b = 0; b < NBG; ++b) red[(warp * R + r) * NBG + b] = acc[r][b];
-            __syncthreads();
-            if (kp == 0 && lane == 0) {
-                for (int w = 1; w < ksplit; ++w)
+                for (int b = 0; b < NBG; ++b) {
+                    if (b < nb) {
+                        XFrag<FMT> x0, x1;
+                        load_x<FMT>(xs + b * K, u, x0);
+                        load_x<FMT>(xs + b * K, u + 32, x1);
+#pragma unroll
+                        for (int r = 0; r < R; ++r)
+                            if (row_ok[r])
+                                acc[r][b] += dot_frag<FMT>(r0[r], u, x0, xsum16 + b * (K / 16)) +
+                                             dot_frag<FMT>(r1[r], u + 32, x1, xsum16 + b * (K / 16));
+                    }
+                }
+            }
+            if (u < u_end) {
+                Raw r0[R];
+#pragma unroll
+                for (int r = 0; r < R; ++r)
+                    if (row_ok[r]) r0[r] = load_unit<FMT>(W, row_base + r, u);
+#pragma unroll
+                for (int b = 0; b < NBG; ++b) {
+                    if (b < nb) {
+                        XFrag<FMT> x0;
+                        load_x<FMT>(xs + b * K, u, x0);
+#pragma unroll
+                        for (int r = 0; r < R; ++r)
+                            if (row_ok[r]) acc[r][b] += dot_frag<FMT>(r0[r], u, x0, xsum16 + b * (K / 16));
+                    }
+                }
+            }
+
+            // ---- reduce: lanes, then the K parts of a row group
+#pragma unroll
+            for (int r = 0; r < R; ++r)
+#pragma unroll
+                for (int b = 0; b < NBG; ++b) acc[r][b] = warp_sum(acc[r][b]);
+            if (ksplit > 1) {
+                if (lane == 0)
 #pragma unroll
                     for (int r = 0; r < R; ++r)
 #pragma unroll
-                        for (int b = 0; b < NBG; ++b) acc[r][b] += red[((warp + w) * R + r) * NBG + b];
-            }
-        }
-
-        // ---- epilogue (one lane per row group)
-        if (kp == 0 && lane == 0) {
-            for (int b = 0; b < nb; ++b) {
-                float* yrow = out_row(b0 + b);
-                if (a.epi == EPI_SWIGLU) {
+                        for (int b = 0; b < NBG; ++b) red[(warp * R + r) * NBG + b] = acc[r][b];
+                __syncthreads();
+                if (kp == 0 && lane == 0) {
+                    for (int w = 1; w < ksplit; ++w)
 #pragma unroll
-                    for (int r = 0; r + 1 < R; r += 2)
-                        if (row_ok[r + 1]) yrow[(row_base + r) >> 1] = silu(acc[r][b]) * acc[r + 1][b];
-                } else {
-                    unsigned long long kbest = 0ull;
+                        for (int r = 0; r < R; ++r)
 #pragma unroll
-                    for (int r = 0; r < R; ++r) {
-                        if (!row_ok[r]) continue;
-                        int row = row_base + r;
-                        if (a.epi == EPI_ADD) yrow[row] += acc[r][b];
-                        else yrow[row] = acc[r][b];
-                        if (a.epi == EPI_LOGITS) {
-                            unsigned long long kk = argmax_key(acc[r][b], (uint32_t)row);
-                            kbest = kk > kbest ? kk : kbest;
-                        }
-                    }
-                    if (a.epi == EPI_LOGITS) atomicMax(&best[b], kbest);
+                            for (int b = 0; b < NBG; ++b) acc[r][b] += red[((warp + w) * R + r) * NBG + b];
                 }
             }
+
+            // ---- epilogue (one lane per row group)
+            if (kp == 0 && lane == 0) {
+#pragma unroll
+                for (int b = 0; b < NBG; ++b) {
+                    if (b >= nb) continue;
+                    float* yrow = out_row(b0 + b);
+#pragma unroll
+                    for (int r = 0; r < R; ++r) acc[r][b] *= inv[b];
+                    if (a.epi == EPI_SWIGLU) {
+#pragma unroll
+                        for (int r = 0; r + 1 < R; r += 2)
+                            if (row_ok[r + 1]) yrow[(row_base + r) >> 1] = silu(acc[r][b]) * acc[r + 1][b];
+                    } else {
+                        unsigned long long kbest = 0ull;
+#pragma unroll
+                        for (int r = 0; r < R; ++r) {
+                            if (!row_ok[r]) continue;
+                            int row = row_base + r;
+                            if (a.epi == EPI_ADD) yrow[row] += acc[r][b];
+                            else yrow[row] = acc[r][b];
+                            if (a.epi == EPI_LOGITS) {
+                                unsigned long long kk = argmax_key(acc[r][b], (uint32_t)row);
+                                kbest = kk > kbest ? kk : kbest;
+                            }
+                        }
+                        if (a.epi == EPI_LOGITS) atomicMax(&best[b], kbest);
+                    }
+                }
+            }
+            if (ksplit > 1) __syncthreads();   // red is reused by the next tile
         }
-        if (a.epi == EPI_LOGITS) {
-            __syncthreads();
-            if (tid < nb) atomicMax(&a.st->keys[b0 + tid], best[tid]);
-        }
+        __syncthreads();
+        if (a.epi == EPI_LOGITS && tid < nb) atomicMax(&a.st->keys[b0 + tid], best[tid]);
         __syncthreads();
     }
 }
+
+int g_sms = 152;   // set by gemv_prepare
+
+template <int FMT, int R, int NBG>
+struct Occ {
+    static int ctas_per_sm;   // resident CTAs per SM at the kernel's register / smem use
+};
+template <int FMT, int R, int NBG>
+int Occ<FMT, R, NBG>::ctas_per_sm = 2;
 
 template <int FMT, int R, int NBG>
 void launch_t(const GemvArgs& a, cudaStream_t s, bool pdl) {
     const int rows_per_cta = (WARPS / a.ksplit) * R;
     const int rows = a.route ? a.rows_per_expert : a.W.N;
-    dim3 grid((rows + rows_per_cta - 1) / rows_per_cta, a.route ? a.max_experts : 1);
+    const int tiles = (rows + rows_per_cta - 1) / rows_per_cta;
+    // one wave of resident CTAs; larger matrices loop over tiles inside each CTA
+    dim3 grid(a.route ? tiles : std::min(tiles, Occ<FMT, R, NBG>::ctas_per_sm * g_sms), a.route ? a.max_experts : 1);
     size_t smem = (size_t)NBG * a.W.K * 4 + (FMT == FMT_Q4_K ? (size_t)NBG * (a.W.K / 16) * 4 : 0) +
-                  (WARPS * R * NBG + 32) * 4;
+                  (size_t)(WARPS * R * NBG + WARPS * NBG) * 4;
     auto kern = gemv_kernel<FMT, R, NBG>;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
@@ -317,6 +396,11 @@ void prepare_t(int optin) {
     cudaFuncGetAttributes(&fa, gemv_kernel<FMT, R, NBG>);
     cudaFuncSetAttribute(gemv_kernel<FMT, R, NBG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          optin - (int)fa.sharedSizeBytes);
+    int occ = 0;
+    // typical stage: hidden 4096 in shared memory for each of NBG rows
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, gemv_kernel<FMT, R, NBG>, THREADS,
+                                                  (size_t)NBG * 4096 * 4 + 2048);
+    Occ<FMT, R, NBG>::ctas_per_sm = occ > 0 ? occ : 1;
 }
 
 }  // namespace
@@ -325,6 +409,7 @@ void gemv_prepare() {
     int dev = 0, optin = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    cudaDeviceGetAttribute(&g_sms, cudaDevAttrMultiProcessorCount, dev);
     prepare_t<FMT_Q8_0, 4, 1>(optin);
     prepare_t<FMT_Q8_0, 4, 4>(optin);
     prepare_t<FMT_Q4_K, 2, 1>(optin);
