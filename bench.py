@@ -377,8 +377,69 @@ def run_fq(args):
     return 0
 
 
+def run_kernel(args):
+    """Kernel-level timing for profiling: the LM-head GEMV alone (--kernel lm_head) or one
+    decoder layer step at context 2048 (--kernel layer), `--steps` launches after
+    `--warmup`, on the 0.6B workload's weights."""
+    import torch
+    import synth.workloads as wl
+    from quantized_decoder_decode_gb300 import fq
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    st = torch.cuda.current_stream(dev)
+    stream = st.cuda_stream
+    w = wl.WORKLOADS[WORKLOAD]
+    d = w.dims
+    W = wl.make_weights(wl.scaled(w, num_layers=1), layers=range(1))
+    desc = fq.fq_desc_init(vocab_size=d.vocab_size, hidden_size=d.hidden_size, intermediate_size=d.intermediate_size,
+                           num_layers=1, num_attention_heads=d.num_attention_heads,
+                           num_key_value_heads=d.num_key_value_heads, head_dim=d.head_dim, max_positions=4096)
+    src, keep = fq.weight_src(desc, W, w.weight_dtype)
+    model = fq.fq_load_weights(desc, src, stream)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    if args.kernel == "lm_head":
+        x = torch.randn(d.hidden_size, device=dev)
+        y = torch.empty(d.vocab_size, device=dev)
+        call = lambda: fq.fq_gemv(model, 0, fq.W_OUTPUT, 1, x.data_ptr(), y.data_ptr(), stream)  # noqa: E731
+        nbytes = d.vocab_size * d.hidden_size * 34 / 32
+    else:
+        kv = fq.fq_kv_init(model, CONTEXT + 1, "bf16")
+        k, v = wl.make_kv_prior(w, 0, 0, CONTEXT)
+        kt = torch.from_numpy(k.view(np.int16)).to(dev)
+        vt = torch.from_numpy(v.view(np.int16)).to(dev)
+        fq.fq_kv_append(kv, 0, 0, CONTEXT, kt.data_ptr(), vt.data_ptr(), stream)
+        fq.fq_kv_commit(kv, CONTEXT)
+        x = torch.from_numpy(wl.layer_input(w)).to(dev)
+        call = lambda: fq.fq_layer_step(model, 0, kv, CONTEXT, x.data_ptr(), stream)  # noqa: E731
+        sb = step_bytes(dataclasses_replace_layers(d), CONTEXT)
+        nbytes = sb["weights"] + sb["kv_read"] + sb["kv_write"]
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize()
+    for a, b in evs:
+        a.record(st)
+        call()
+        b.record(st)
+    torch.cuda.synchronize()
+    t = [a.elapsed_time(b) / 1e3 for a, b in evs]
+    mean = sum(t) / len(t)
+    peak, kind = measured_peaks()
+    print(json.dumps({"kernel": args.kernel, "launches": len(t), "us_mean": mean * 1e6, "us_min": min(t) * 1e6,
+                      "bytes": nbytes, "gbs": nbytes / mean / 1e9, "frac": nbytes / mean / 1e9 / peak,
+                      "peak": peak, "peak_kind": kind}))
+    fq.fq_model_free(model)
+    return 0
+
+
+def dataclasses_replace_layers(d):
+    import dataclasses
+    return dataclasses.replace(d, num_layers=1)
+
+
 def main():
     ap = argparse.ArgumentParser()
+    ap.add_argument("--kernel", choices=["lm_head", "layer"], default=None,
+                    help="time one kernel family instead of the decode loop (profiling)")
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=6400)
     ap.add_argument("--warmup", type=int, default=64)
@@ -386,6 +447,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
+    if args.kernel:
+        return run_kernel(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_fq(args)

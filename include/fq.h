@@ -213,6 +213,11 @@ fq_status fq_dequant_rows(const fq_model* m, uint32_t layer, fq_weight_id which,
 fq_status fq_gemv(const fq_model* m, uint32_t layer, fq_weight_id which, uint32_t n, const float* x, float* y,
                   void* stream);
 
+/* Synchronise `stream` and report device-side failures recorded since the last check:
+ * FQ_ERR_DEVICE_TIMEOUT when a kernel's bounded wait on its own copy pipeline gave up
+ * (the kernel returned early; results of that step are invalid).  Clears the record. */
+fq_status fq_check_device(const fq_model* m, void* stream);
+
 const char* fq_last_error(void);
 const char* fq_status_str(fq_status s);
 

@@ -75,6 +75,7 @@ struct fq_model {
     std::vector<LayerW> layers;
     float2* rope = nullptr;
     int max_pos = 0;
+    uint32_t* err = nullptr;       // device error word (bounded waits that gave up)
     std::vector<void*> allocs;
     std::mutex ws_mu;
     std::map<cudaStream_t, Workspace*> ws;
@@ -238,6 +239,7 @@ fq_status enqueue_step(const Body& b, cudaStream_t s, int kv_bf16, float* x_over
         g.W = lw.qkv; g.B = n; g.x = x; g.x_stride = H; g.norm_g = lw.attn_norm; g.eps = p.rms_norm_eps;
         g.y = w->qkv; g.y_stride = m->qkv_rows(); g.epi = EPI_STORE;
         g.ksplit = choose_ksplit(g.W, rows_per_warp(g.W));
+        g.err = m->err;
         launch_gemv(g, s, pdl());
 
         AttnArgs a;
@@ -250,6 +252,7 @@ fq_status enqueue_step(const Body& b, cudaStream_t s, int kv_bf16, float* x_over
         GemvArgs o;
         o.W = lw.o; o.B = n; o.x = w->attn; o.x_stride = Hq * HEAD_DIM; o.y = x; o.y_stride = H; o.epi = EPI_ADD;
         o.ksplit = choose_ksplit(o.W, rows_per_warp(o.W));
+        o.err = m->err;
         launch_gemv(o, s, pdl());
 
         if (!m->moe()) {
@@ -257,11 +260,13 @@ fq_status enqueue_step(const Body& b, cudaStream_t s, int kv_bf16, float* x_over
             gu.W = lw.gate_up; gu.B = n; gu.x = x; gu.x_stride = H; gu.norm_g = lw.ffn_norm; gu.eps = p.rms_norm_eps;
             gu.y = w->h; gu.y_stride = p.intermediate_size; gu.epi = EPI_SWIGLU;
             gu.ksplit = choose_ksplit(gu.W, rows_per_warp(gu.W));
+            gu.err = m->err;
             launch_gemv(gu, s, pdl());
 
             GemvArgs dn;
             dn.W = lw.down; dn.B = n; dn.x = w->h; dn.x_stride = p.intermediate_size; dn.y = x; dn.y_stride = H;
             dn.epi = EPI_ADD; dn.ksplit = choose_ksplit(dn.W, rows_per_warp(dn.W));
+            dn.err = m->err;
             launch_gemv(dn, s, pdl());
         } else {
             const int E = p.num_experts, k = p.num_experts_used, Fe = p.moe_intermediate_size;
@@ -269,6 +274,7 @@ fq_status enqueue_step(const Body& b, cudaStream_t s, int kv_bf16, float* x_over
             r.W = lw.router; r.B = n; r.x = x; r.x_stride = H; r.norm_g = lw.ffn_norm; r.eps = p.rms_norm_eps;
             r.y = w->rlogits; r.y_stride = E; r.epi = EPI_STORE; r.xn_out = w->xn; r.xn_stride = H;
             r.ksplit = choose_ksplit(r.W, 4);
+            r.err = m->err;
             launch_gemv(r, s, pdl());
             launch_moe_route(w->rlogits, E, k, n, p.norm_topk_prob, w->route, s, pdl());
 
@@ -277,6 +283,7 @@ fq_status enqueue_step(const Body& b, cudaStream_t s, int kv_bf16, float* x_over
             eg.epi = EPI_SWIGLU; eg.route = w->route; eg.moe_k = k; eg.rows_per_expert = 2 * Fe; eg.x_by_pair = 0;
             eg.max_experts = std::min(E, n * k);
             eg.ksplit = 1;
+            eg.err = m->err;
             launch_gemv(eg, s, pdl());
 
             GemvArgs ed;
@@ -284,6 +291,7 @@ fq_status enqueue_step(const Body& b, cudaStream_t s, int kv_bf16, float* x_over
             ed.route = w->route; ed.moe_k = k; ed.rows_per_expert = H; ed.x_by_pair = 1;
             ed.max_experts = std::min(E, n * k);
             ed.ksplit = 2;
+            ed.err = m->err;
             launch_gemv(ed, s, pdl());
             launch_moe_combine(x, w->ye, w->route, n, k, H, s, pdl());
 
@@ -305,6 +313,7 @@ fq_status enqueue_step(const Body& b, cudaStream_t s, int kv_bf16, float* x_over
         lm.W = m->output; lm.B = n; lm.x = x; lm.x_stride = H; lm.norm_g = m->output_norm; lm.eps = p.rms_norm_eps;
         lm.y = b.logits; lm.y_stride = p.vocab_size; lm.epi = b.greedy ? EPI_LOGITS : EPI_STORE; lm.st = w->st;
         lm.ksplit = choose_ksplit(lm.W, rows_per_warp(lm.W));
+        lm.err = m->err;
         launch_gemv(lm, s, pdl());
         if (b.greedy) launch_lm_finish(w->st, n, (int)p.vocab_size, s, pdl());
     }
@@ -650,6 +659,10 @@ fq_status fq_load_weights(const fq_desc* d, const fq_weight_src* src, void* stre
                 TRY(ld.plain(l.down_exps, w.down_exps));
             }
         }
+        uint32_t* errw;
+        TRY(dalloc(m->allocs, &errw, 1));
+        CK(cudaMemsetAsync(errw, 0, sizeof(uint32_t), s));
+        m->err = errw;
         m->max_pos = (int)p.max_positions;
         float2* rope;
         TRY(dalloc(m->allocs, &rope, (size_t)m->max_pos * (HEAD_DIM / 2)));
@@ -873,8 +886,22 @@ fq_status fq_gemv(const fq_model* m, uint32_t layer, fq_weight_id which, uint32_
     GemvArgs g;
     g.W = W; g.B = (int)n; g.x = x; g.x_stride = W.K; g.y = y; g.y_stride = W.N; g.epi = EPI_STORE;
     g.ksplit = choose_ksplit(W, rows_per_warp(W));
+    g.err = m->err;
     launch_gemv(g, (cudaStream_t)stream, false);
     CK(cudaGetLastError());
+    return FQ_OK;
+}
+
+fq_status fq_check_device(const fq_model* m, void* stream) {
+    if (!m) return fail(FQ_ERR_INVALID_ARGUMENT, "null model");
+    cudaStream_t s = (cudaStream_t)stream;
+    uint32_t host = 0;
+    CK(cudaMemcpyAsync(&host, m->err, sizeof host, cudaMemcpyDeviceToHost, s));
+    CK(cudaStreamSynchronize(s));
+    if (host) {
+        CK(cudaMemsetAsync(m->err, 0, sizeof(uint32_t), s));
+        return fail(FQ_ERR_DEVICE_TIMEOUT, "a bounded device wait gave up (code %u)", host);
+    }
     return FQ_OK;
 }
 

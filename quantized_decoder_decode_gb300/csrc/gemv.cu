@@ -22,6 +22,7 @@
 #include "quant.cuh"
 
 #include <algorithm>
+#include <cstdlib>
 
 namespace fq {
 
@@ -29,106 +30,6 @@ namespace {
 
 constexpr int THREADS = 256;
 constexpr int WARPS = THREADS / 32;
-
-// Q8_0 unit: 16 consecutive codes of one row (16 bytes) sharing one fp16 scale.
-// Q4_K unit: 16 bytes of nibbles = 16 elements of sub-block 2c (low) and 16 of 2c+1 (high).
-template <int FMT> struct Unit;
-template <> struct Unit<FMT_Q8_0> { static constexpr int ELEMS = 16; };
-template <> struct Unit<FMT_Q4_K> { static constexpr int ELEMS = 32; };
-template <> struct Unit<FMT_F32> { static constexpr int ELEMS = 4; };
-
-struct Raw {
-    uint4 q;        // 16 bytes of codes (Q8_0, Q4_K) or 4 floats (F32)
-    uint4 hdr;      // Q4_K: d, dmin, 12 scale bytes
-    uint16_t sc;    // Q8_0 scale
-};
-
-template <int FMT>
-FQ_DEV Raw load_unit(const QMat& W, int row, int u) {
-    Raw r;
-    if constexpr (FMT == FMT_Q8_0) {
-        r.q = ld_stream16(W.q + (size_t)row * W.K + (size_t)u * 16);
-        r.sc = ld_stream2(W.s + (size_t)row * (W.K / 32) + (u >> 1));
-    } else if constexpr (FMT == FMT_Q4_K) {
-        const uint8_t* blk = W.q + (size_t)row * ((size_t)W.K / 256 * 144) + (size_t)(u >> 3) * 144;
-        int c = (u & 7) >> 1, h = u & 1;
-        r.q = ld_stream16(blk + 16 + 32 * c + 16 * h);
-        r.hdr = ld_stream16(blk);
-    } else {
-        r.q = ld_stream16((const float*)W.q + (size_t)row * W.K + (size_t)u * 4);
-    }
-    return r;
-}
-
-// Activations of one unit, loaded from shared memory once and shared by the warp's rows.
-template <int FMT> struct XFrag { float v[Unit<FMT>::ELEMS]; };
-
-template <int FMT>
-FQ_DEV void load_x(const float* xs, int u, XFrag<FMT>& f) {
-    if constexpr (FMT == FMT_Q8_0) {
-        const float4* p = reinterpret_cast<const float4*>(xs + u * 16);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            float4 t = p[i];
-            f.v[4 * i] = t.x; f.v[4 * i + 1] = t.y; f.v[4 * i + 2] = t.z; f.v[4 * i + 3] = t.w;
-        }
-    } else if constexpr (FMT == FMT_Q4_K) {
-        const int e_lo = (u >> 3) * 256 + 64 * ((u & 7) >> 1) + 16 * (u & 1);
-        const float4* pl = reinterpret_cast<const float4*>(xs + e_lo);
-        const float4* ph = reinterpret_cast<const float4*>(xs + e_lo + 32);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            float4 t = pl[i], h = ph[i];
-            f.v[4 * i] = t.x; f.v[4 * i + 1] = t.y; f.v[4 * i + 2] = t.z; f.v[4 * i + 3] = t.w;
-            f.v[16 + 4 * i] = h.x; f.v[16 + 4 * i + 1] = h.y; f.v[16 + 4 * i + 2] = h.z; f.v[16 + 4 * i + 3] = h.w;
-        }
-    } else {
-        float4 t = reinterpret_cast<const float4*>(xs)[u];
-        f.v[0] = t.x; f.v[1] = t.y; f.v[2] = t.z; f.v[3] = t.w;
-    }
-}
-
-// Partial dot of one unit of one row with its activation fragment; xsum16: per-16 sums of
-// the staged activations (Q4_K min terms).
-template <int FMT>
-FQ_DEV float dot_frag(const Raw& r, int u, const XFrag<FMT>& x, const float* xsum16) {
-    if constexpr (FMT == FMT_Q8_0) {
-        float f[16];
-        s8x4_to_f32(r.q.x, f);
-        s8x4_to_f32(r.q.y, f + 4);
-        s8x4_to_f32(r.q.z, f + 8);
-        s8x4_to_f32(r.q.w, f + 12);
-        float acc = 0.f;
-#pragma unroll
-        for (int i = 0; i < 16; ++i) acc = fmaf(f[i], x.v[i], acc);
-        return h2f(r.sc) * acc;
-    } else if constexpr (FMT == FMT_Q4_K) {
-        const int c = (u & 7) >> 1;
-        const int e_lo = (u >> 3) * 256 + 64 * c + 16 * (u & 1);
-        uint32_t w[4] = {r.q.x, r.q.y, r.q.z, r.q.w};
-        float slo = 0.f, shi = 0.f;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            float lo[4], hi[4];
-            u8x4_to_f32(w[i] & 0x0F0F0F0Fu, lo);
-            u8x4_to_f32((w[i] >> 4) & 0x0F0F0F0Fu, hi);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                slo = fmaf(lo[j], x.v[4 * i + j], slo);
-                shi = fmaf(hi[j], x.v[16 + 4 * i + j], shi);
-            }
-        }
-        float d = h2f((unsigned short)(r.hdr.x & 0xFFFFu)), dmin = h2f((unsigned short)(r.hdr.x >> 16));
-        uint32_t sc0, mn0, sc1, mn1;
-        q4k_scale_min(r.hdr, 2 * c, sc0, mn0);
-        q4k_scale_min(r.hdr, 2 * c + 1, sc1, mn1);
-        float d1 = d * (float)sc0, m1 = dmin * (float)mn0, d2 = d * (float)sc1, m2 = dmin * (float)mn1;
-        return d1 * slo - m1 * xsum16[e_lo >> 4] + d2 * shi - m2 * xsum16[(e_lo + 32) >> 4];
-    } else {
-        return __uint_as_float(r.q.x) * x.v[0] + __uint_as_float(r.q.y) * x.v[1] + __uint_as_float(r.q.z) * x.v[2] +
-               __uint_as_float(r.q.w) * x.v[3];
-    }
-}
 
 // One CTA owns a tile of rows_per_cta = (8 / ksplit) * R rows at a time and walks the tiles
 // with a CTA stride, so the input rows are staged (and their RMS computed) once per CTA.
@@ -416,9 +317,11 @@ void gemv_prepare() {
     prepare_t<FMT_Q4_K, 2, 4>(optin);
     prepare_t<FMT_F32, 4, 1>(optin);
     prepare_t<FMT_F32, 4, 4>(optin);
+    gemv_tma_prepare();
 }
 
 void launch_gemv(const GemvArgs& a, cudaStream_t s, bool pdl) {
+    if (!getenv("FQ_NO_TMA") && launch_gemv_tma(a, s, pdl)) return;
     const bool one = a.B == 1;
     switch (a.W.fmt) {
         case FMT_Q8_0:

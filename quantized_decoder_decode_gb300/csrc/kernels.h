@@ -85,11 +85,15 @@ struct GemvArgs {
     int rows_per_expert = 0;
     int x_by_pair = 0;            // input row = token*moe_k + slot (else token)
     int max_experts = 0;          // grid.y
+    uint32_t* err = nullptr;      // device error word: bit set when a bounded wait gave up
 };
 
 void launch_gemv(const GemvArgs& a, cudaStream_t s, bool pdl);
 // one-time kernel attributes (large dynamic shared memory); call before any graph capture
 void gemv_prepare();
+// the bulk-copy fed variant; returns false when the shape is not covered (caller falls back)
+bool launch_gemv_tma(const GemvArgs& a, cudaStream_t s, bool pdl);
+void gemv_tma_prepare();
 
 // Attention with fused QK-norm + rope + KV append (one query row per sequence).
 struct AttnArgs {
