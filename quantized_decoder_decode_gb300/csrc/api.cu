@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <deque>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -76,6 +77,7 @@ struct fq_model {
     float2* rope = nullptr;
     int max_pos = 0;
     uint32_t* err = nullptr;       // device error word (bounded waits that gave up)
+    std::deque<TmaMaps> tmaps;     // tensor maps of the dense weights (stable addresses)
     std::vector<void*> allocs;
     std::mutex ws_mu;
     std::map<cudaStream_t, Workspace*> ws;
@@ -663,6 +665,18 @@ fq_status fq_load_weights(const fq_desc* d, const fq_weight_src* src, void* stre
         TRY(dalloc(m->allocs, &errw, 1));
         CK(cudaMemsetAsync(errw, 0, sizeof(uint32_t), s));
         m->err = errw;
+        // tensor maps for the bulk-copy GEMV (expert stacks keep the register-fed path)
+        auto attach = [&](QMat& q) {
+            if (!q.q) return;
+            m->tmaps.emplace_back();
+            if (make_tma_maps(q, &m->tmaps.back())) q.tm = &m->tmaps.back();
+        };
+        attach(m->tok_embd);
+        if (m->output.q != m->tok_embd.q) attach(m->output);
+        else m->output.tm = m->tok_embd.tm;
+        for (auto& lw : m->layers) {
+            attach(lw.qkv); attach(lw.o); attach(lw.gate_up); attach(lw.down); attach(lw.router);
+        }
         m->max_pos = (int)p.max_positions;
         float2* rope;
         TRY(dalloc(m->allocs, &rope, (size_t)m->max_pos * (HEAD_DIM / 2)));

@@ -4,14 +4,19 @@
 // input rows; store, residual add, SwiGLU over interleaved gate/up rows, logits + argmax
 // keys), but the weight bytes travel global -> shared memory through cp.async.bulk into a
 // ring of STAGES buffers guarded by mbarriers:
-//   * one producer warp walks this CTA's (row tile, K chunk) pairs and issues one bulk copy
-//     per row (and per row of Q8_0 scales) into the next free stage;
+//   * one producer warp walks this CTA's (row tile, K chunk) pairs and issues the copies of
+//     the next free stage;
 //   * eight consumer warps wait for a stage, decode codes to exact floats in registers,
 //     multiply-accumulate against the activations staged in shared memory, release the
 //     stage, and reduce + apply the epilogue at the end of each row tile.
+// Each stage is one 2-D tensor-map copy of the codes (a box of rows x K-chunk) plus, for
+// Q8_0, one of the scales; boxes that run past the last row or column are zero-filled.
 // The producer starts before griddepcontrol.wait (weights never depend on an earlier
 // kernel), so the first STAGES chunks are already landing while the previous kernel of
 // the step finishes; only the consumers wait for the activations.
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
 
 #include <algorithm>
 
@@ -35,6 +40,12 @@ template <> struct TCfg<FMT_Q8_0> { static constexpr int R = 4, RT = 32, KC = 51
 template <> struct TCfg<FMT_Q4_K> { static constexpr int R = 2, RT = 16, KC = 2048, UPL = 2; };
 template <> struct TCfg<FMT_F32> { static constexpr int R = 4, RT = 32, KC = 128, UPL = 1; };
 
+// elements per K chunk in the tensor maps' view of the planes
+template <int FMT> struct TView;
+template <> struct TView<FMT_Q8_0> { static constexpr int X = 128; };   // codes as u32
+template <> struct TView<FMT_Q4_K> { static constexpr int X = 144; };   // blocks as u64
+template <> struct TView<FMT_F32> { static constexpr int X = 128; };
+
 template <int FMT>
 FQ_HD constexpr int chunk_bytes(int kc) {   // bytes of kc elements of one row
     return FMT == FMT_Q8_0 ? kc : FMT == FMT_Q4_K ? kc / 256 * 144 : kc * 4;
@@ -51,11 +62,17 @@ struct TLayout {
     }
 };
 
+struct TmaParams {
+    TmaMaps maps;
+    GemvArgs a;
+};
+
 template <int FMT, int NBG>
-__global__ void __launch_bounds__(THREADS_T) gemv_tma_kernel(const GemvArgs a) {
+__global__ void __launch_bounds__(THREADS_T) gemv_tma_kernel(const __grid_constant__ TmaParams prm) {
     using C = TCfg<FMT>;
     using Lay = TLayout<FMT, NBG>;
-    extern __shared__ __align__(128) uint8_t smem[];
+    const GemvArgs& a = prm.a;
+    extern __shared__ __align__(1024) uint8_t smem[];
     const QMat W = a.W;
     const int K = W.K, N = W.N;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -88,7 +105,7 @@ __global__ void __launch_bounds__(THREADS_T) gemv_tma_kernel(const GemvArgs a) {
 
     if (warp == CONSUMER_WARPS) {
         // ---------------- producer: weights only, so no wait for the previous kernel
-        const size_t row_bytes = W.row_bytes();
+        constexpr uint32_t STAGE_BYTES = (uint32_t)(Lay::QSTAGE + Lay::SSTAGE);
         for (int it = 0; it < n_iters; ++it) {
             const int stage = it % STAGES;
             const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
@@ -96,22 +113,16 @@ __global__ void __launch_bounds__(THREADS_T) gemv_tma_kernel(const GemvArgs a) {
                 if (a.err && lane == 0) atomicOr(a.err, 1u);
                 break;
             }
-            const int tile = blockIdx.x + (it / n_chunks) * gridDim.x, chunk = it % n_chunks;
-            const int row0 = tile * C::RT, nrows = min(C::RT, N - row0);
-            const int kc = min(C::KC, K - chunk * C::KC);
-            const uint32_t qb = (uint32_t)chunk_bytes<FMT>(kc);
-            const uint32_t sb = FMT == FMT_Q8_0 ? (uint32_t)(kc / 16) : 0u;
-            if (lane == 0) mbar_arrive_expect_tx(&full[stage], (uint32_t)nrows * (qb + sb));
-            __syncwarp();
-            for (int r = lane; r < nrows; r += 32) {
-                const size_t row = (size_t)(row0 + r);
-                bulk_g2s(qbuf + (size_t)stage * Lay::QSTAGE + (size_t)r * chunk_bytes<FMT>(C::KC),
-                         W.q + row * row_bytes + (size_t)chunk * chunk_bytes<FMT>(C::KC), qb, &full[stage]);
+            if (lane == 0) {
+                const int tile = blockIdx.x + (it / n_chunks) * gridDim.x, chunk = it % n_chunks;
+                mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
+                tma_load_2d(qbuf + (size_t)stage * Lay::QSTAGE, prm.maps.q, chunk * TView<FMT>::X, tile * C::RT,
+                            &full[stage]);
                 if (FMT == FMT_Q8_0)
-                    bulk_g2s(sbuf + (size_t)stage * Lay::SSTAGE + (size_t)r * (C::KC / 16),
-                             reinterpret_cast<const uint8_t*>(W.s) + row * (K / 16) + (size_t)chunk * (C::KC / 16),
-                             sb, &full[stage]);
+                    tma_load_2d(sbuf + (size_t)stage * Lay::SSTAGE, prm.maps.s, chunk * (C::KC / 32), tile * C::RT,
+                                &full[stage]);
             }
+            __syncwarp();
         }
         pdl_wait();   // every thread of the grid waits before the grid may complete
         return;
@@ -282,6 +293,9 @@ bool launch_t(const GemvArgs& a, cudaStream_t s, bool pdl) {
     const size_t smem = TLayout<FMT, NBG>::bytes(a.W.K);
     if (smem > 200 * 1024) return false;
     const int tiles = (a.W.N + C::RT - 1) / C::RT;
+    TmaParams prm;
+    prm.maps = *a.W.tm;
+    prm.a = a;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(std::min(tiles, OccT<FMT, NBG>::ctas_per_sm * g_sms_t));
     cfg.blockDim = dim3(THREADS_T);
@@ -292,8 +306,22 @@ bool launch_t(const GemvArgs& a, cudaStream_t s, bool pdl) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    cudaLaunchKernelEx(&cfg, gemv_tma_kernel<FMT, NBG>, a);
+    cudaLaunchKernelEx(&cfg, gemv_tma_kernel<FMT, NBG>, prm);
     return true;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+bool encode(void* map, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t rows, uint64_t row_bytes,
+            uint32_t box_inner, uint32_t box_rows) {
+    cuuint64_t dims[2] = {inner, rows};
+    cuuint64_t strides[1] = {row_bytes};
+    cuuint32_t box[2] = {box_inner, box_rows};
+    cuuint32_t es[2] = {1, 1};
+    CUresult r = g_encode(reinterpret_cast<CUtensorMap*>(map), dt, 2, const_cast<void*>(base), dims, strides, box, es,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
 }
 
 template <int FMT, int NBG>
@@ -323,8 +351,38 @@ void gemv_tma_prepare() {
     prepare_t<FMT_F32, 4>(optin);
 }
 
+bool make_tma_maps(const QMat& W, TmaMaps* out) {
+    out->ok = 0;
+    if (!g_encode) {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult qr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &qr) !=
+                cudaSuccess ||
+            qr != cudaDriverEntryPointSuccess || !fn)
+            return false;
+        g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    if (W.K % 256 != 0 || W.N <= 0) return false;
+    const uint64_t rb = W.row_bytes();
+    bool ok = false;
+    if (W.fmt == FMT_Q8_0) {
+        ok = encode(out->q, CU_TENSOR_MAP_DATA_TYPE_UINT32, W.q, (uint64_t)W.K / 4, W.N, rb, TView<FMT_Q8_0>::X,
+                    TCfg<FMT_Q8_0>::RT) &&
+             encode(out->s, CU_TENSOR_MAP_DATA_TYPE_UINT16, W.s, (uint64_t)W.K / 32, W.N, (uint64_t)W.K / 16,
+                    TCfg<FMT_Q8_0>::KC / 32, TCfg<FMT_Q8_0>::RT);
+    } else if (W.fmt == FMT_Q4_K) {
+        ok = encode(out->q, CU_TENSOR_MAP_DATA_TYPE_UINT64, W.q, rb / 8, W.N, rb, TView<FMT_Q4_K>::X,
+                    TCfg<FMT_Q4_K>::RT);
+    } else if (W.fmt == FMT_F32) {
+        ok = encode(out->q, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, W.q, (uint64_t)W.K, W.N, rb, TView<FMT_F32>::X,
+                    TCfg<FMT_F32>::RT);
+    }
+    out->ok = ok ? 1 : 0;
+    return ok;
+}
+
 bool launch_gemv_tma(const GemvArgs& a, cudaStream_t s, bool pdl) {
-    if (a.route || a.B > 4 || a.W.K % 256 != 0 || g_sms_t == 0) return false;
+    if (a.route || a.B > 4 || a.W.K % 256 != 0 || g_sms_t == 0 || !a.W.tm || !a.W.tm->ok) return false;
     const bool one = a.B == 1;
     switch (a.W.fmt) {
         case FMT_Q8_0: return one ? launch_t<FMT_Q8_0, 1>(a, s, pdl) : launch_t<FMT_Q8_0, 4>(a, s, pdl);

@@ -18,6 +18,14 @@ constexpr int MAX_EXPERTS = 256;
 
 enum Fmt : int { FMT_F32 = 0, FMT_BF16 = 1, FMT_Q8_0 = 8, FMT_Q4_K = 12 };
 
+// Tensor maps (TMA descriptors) of one weight's planes, built at load time; opaque bytes
+// of CUtensorMap.  ok == 0 when the shape is not served by the bulk-copy GEMV.
+struct TmaMaps {
+    alignas(64) unsigned long long q[16];
+    alignas(64) unsigned long long s[16];
+    int ok = 0;
+};
+
 // One device-resident weight matrix [N rows, K cols].
 //   Q8_0: repacked into two 16-byte-aligned planes, q int8 [N][K] and s fp16 [N][K/32]
 //         (the same bytes as the ggml blocks, split so that 16-byte loads line up);
@@ -28,6 +36,7 @@ struct QMat {
     int N = 0, K = 0;
     const uint8_t* q = nullptr;
     const uint16_t* s = nullptr;
+    const TmaMaps* tm = nullptr;   // host pointer (model-owned); never read on the device
     FQ_HD size_t row_bytes() const {
         return fmt == FMT_Q8_0 ? (size_t)K : fmt == FMT_Q4_K ? (size_t)K / 256 * 144 : (size_t)K * 4;
     }
@@ -94,6 +103,8 @@ void gemv_prepare();
 // the bulk-copy fed variant; returns false when the shape is not covered (caller falls back)
 bool launch_gemv_tma(const GemvArgs& a, cudaStream_t s, bool pdl);
 void gemv_tma_prepare();
+// build the tensor maps of W's planes for the bulk-copy GEMV (false: not applicable)
+bool make_tma_maps(const QMat& W, TmaMaps* out);
 
 // Attention with fused QK-norm + rope + KV append (one query row per sequence).
 struct AttnArgs {

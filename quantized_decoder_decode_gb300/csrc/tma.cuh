@@ -55,6 +55,17 @@ FQ_DEV void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) 
         : "memory");
 }
 
+// 2-D tiled copy of the box at (x, y) of the tensor described by tmap (a __grid_constant__
+// kernel parameter) into shared memory (128-byte aligned); x * element size must be a
+// multiple of 16 bytes.  Out-of-range parts of the box are zero-filled and still counted.
+FQ_DEV void tma_load_2d(void* dst, const void* tmap, int x, int y, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+            smem_u32(dst)),
+        "l"(tmap), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+
 // Named barrier over the first `threads` threads of the CTA (id 1; id 0 is __syncthreads).
 FQ_DEV void bar_sync_consumers(int threads) { asm volatile("bar.sync 1, %0;" ::"r"(threads) : "memory"); }
 
