@@ -230,7 +230,10 @@ fq_status enqueue_step(const Body& b, cudaStream_t s, int kv_bf16, float* x_over
     const auto& p = m->d.p;
     const int n = b.n, H = p.hidden_size, Hq = p.num_attention_heads, Hkv = p.num_key_value_heads;
     bool first = true;
-    auto pdl = [&]() { bool r = !first; first = false; return r; };
+    // Programmatic dependent launch is opt-in: measured on GB300 the early-resident CTAs of
+    // the next kernel slowed the step down (FQ_PDL=1 enables it)
+    static const bool use_pdl = env_flag("FQ_PDL");
+    auto pdl = [&]() { bool r = !first && use_pdl; first = false; return r; };
     float* x = x_override ? x_override : w->x;
 
     if (layer_only < 0) launch_embed(m->tok_embd, w->st, n, x, s, pdl());
