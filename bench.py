@@ -228,19 +228,40 @@ def cpu_baseline(w, W, budget_s: float = 15.0) -> dict:
 
 def config_dict(w) -> dict:
     d = w.dims
-    return {"workload": f"{w.name}: Qwen3-0.6B-shaped decoder, {d.num_layers} layers, hidden {d.hidden_size}, "
-                        f"{d.num_attention_heads}q/{d.num_key_value_heads}kv heads x {d.head_dim}, FFN "
-                        f"{d.intermediate_size}, vocab {d.vocab_size}, Q8_0 weights, bf16 KV; {CONTEXT} positions "
-                        f"filled by the model, greedy chains of {CHAIN} steps from context {CONTEXT}",
-            "batch": 1, "context": CONTEXT, "chain": CHAIN, "weights": "q8_0", "kv": "bf16",
-            "l2": "no flush: each step streams ~0.87 GB (weights + KV) >> 129 MB L2"}
+    ctx = (f"{CONTEXT} positions filled by the model" if w.prefill_from_model else
+           f"KV prior N(0,1) {w.kv_dtype} at context "
+           + (f"U[{w.context_range[0]},{w.context_range[1]}]" if w.context_range else str(w.context)))
+    moe = (f", {d.num_experts} experts top-{d.num_experts_used} (expert FFN {d.moe_intermediate_size})"
+           if d.is_moe else f", FFN {d.intermediate_size}")
+    return {"workload": f"{w.name}: {d.num_layers} layers, hidden {d.hidden_size}, {d.num_attention_heads}q/"
+                        f"{d.num_key_value_heads}kv heads x {d.head_dim}{moe}, vocab {d.vocab_size}, "
+                        f"{w.weight_dtype.upper()} weights, {w.kv_dtype} KV; batch {w.batch}; {ctx}; greedy chains "
+                        f"of {w.steps} steps from that context",
+            "batch": w.batch, "context": (list(w.context_range) if w.context_range else w.context),
+            "chain": w.steps, "weights": w.weight_dtype, "kv": w.kv_dtype,
+            "l2": "no flush: every step streams far more than the 129 MB L2 (weights + KV)"}
 
 
-# ---------------------------------------------------------------- GPU arm
+def weight_bytes(w, experts_per_layer=None) -> dict:
+    """Algorithmic weight bytes touched by one step (ggml block sizes)."""
+    d = w.dims
+    bpw = 34 / 32 if w.weight_dtype == "q8_0" else 144 / 256
+    H, L = d.hidden_size, d.num_layers
+    attn = ((d.q_dim + 2 * d.kv_dim) * H + H * d.q_dim) * bpw
+    norms = (2 * H + 2 * d.head_dim) * 4
+    if d.is_moe:
+        per_expert = 3 * H * d.moe_intermediate_size * bpw
+        router = d.num_experts * H * 4
+        ne = experts_per_layer if experts_per_layer is not None else [d.num_experts_used] * L
+        ffn = sum(ne) * per_expert + L * router
+    else:
+        ffn = L * 3 * H * d.intermediate_size * bpw
+    head = d.vocab_size * H * bpw + H * 4
+    return {"layers": L * (attn + norms) + ffn, "lm_head": head, "embedding_rows": w.batch * H * bpw}
+
 
 def run_fq(args):
     import torch
-    import synth
     import synth.workloads as wl
     from quantized_decoder_decode_gb300 import fq
 
@@ -248,41 +269,62 @@ def run_fq(args):
     dev = torch.device("cuda", torch.cuda.current_device())
     st = torch.cuda.current_stream(dev)
     stream = st.cuda_stream
-    w = wl.WORKLOADS[WORKLOAD]
+    w = wl.WORKLOADS[args.workload]
     d = w.dims
+    n = w.batch
+    chain = w.steps
     W = wl.make_weights(w)
+    ctxs = [CONTEXT] * n if w.prefill_from_model else [int(c) for c in w.contexts()]
+    cap_max = max(ctxs) + chain
     desc = fq.fq_desc_init(vocab_size=d.vocab_size, hidden_size=d.hidden_size, intermediate_size=d.intermediate_size,
                            num_layers=d.num_layers, num_attention_heads=d.num_attention_heads,
                            num_key_value_heads=d.num_key_value_heads, head_dim=d.head_dim,
-                           rms_norm_eps=d.rms_norm_eps, rope_theta=d.rope_theta, max_positions=4096)
+                           rms_norm_eps=d.rms_norm_eps, rope_theta=d.rope_theta, num_experts=d.num_experts,
+                           num_experts_used=d.num_experts_used, moe_intermediate_size=d.moe_intermediate_size,
+                           max_positions=cap_max + 64)
     src, keep = fq.weight_src(desc, W, w.weight_dtype)
     model = fq.fq_load_weights(desc, src, stream)
-    kv = fq.fq_kv_init(model, CONTEXT + CHAIN, w.kv_dtype)
+    del src, keep
+    kvs = [fq.fq_kv_init(model, c + chain, w.kv_dtype) for c in ctxs]
+    toks = torch.empty((chain, n), dtype=torch.int32, device=dev)
+    logits = torch.empty((n, d.vocab_size), dtype=torch.float32, device=dev)
+    if w.prefill_from_model:
+        # fill the context by running the model on seeded random ids (not timed)
+        ids = wl.prefill_ids(w)
+        for p in range(CONTEXT - 1):
+            fq.fq_decode_step(model, kvs[0], int(ids[p]), p, 0, stream)
+        fq.fq_decode_greedy(model, kvs, [int(ids[CONTEXT - 1])], 1, toks.data_ptr(), logits.data_ptr(), stream)
+        torch.cuda.synchronize()
+        first = [int(toks[0, 0].item())]
+    else:
+        for s_i, (kv, c) in enumerate(zip(kvs, ctxs)):
+            for L in range(d.num_layers):
+                k, v = wl.make_kv_prior(w, s_i, L, c)
+                kt = torch.from_numpy(k.view(np.int16)).to(dev)
+                vt = torch.from_numpy(v.view(np.int16)).to(dev)
+                fq.fq_kv_append(kv, L, 0, c, kt.data_ptr(), vt.data_ptr(), stream)
+            fq.fq_kv_commit(kv, c)
+        torch.cuda.synchronize()
+        first = [int(t) for t in wl.first_ids(w)]
 
-    # fill 2048 positions by running the model on seeded random ids (not timed)
-    ids = wl.prefill_ids(w)
-    for p in range(CONTEXT - 1):
-        fq.fq_decode_step(model, kv, int(ids[p]), p, 0, stream)
-    toks = torch.empty((max(CHAIN, 1), 1), dtype=torch.int32, device=dev)
-    logits = torch.empty((1, d.vocab_size), dtype=torch.float32, device=dev)
-    fq.fq_decode_greedy(model, [kv], [int(ids[CONTEXT - 1])], 1, toks.data_ptr(), logits.data_ptr(), stream)
-    torch.cuda.synchronize()
-    first = int(toks[0, 0].item())
+    def rewind():
+        for kv, c in zip(kvs, ctxs):
+            fq.fq_kv_rewind(kv, c)
 
-    def chains(n_steps, sync_each=False, host_tok=None):
+    def chains(n_steps):
         done = 0
         while done < n_steps:
-            s = min(CHAIN, n_steps - done)
-            fq.fq_kv_rewind(kv, CONTEXT)
-            fq.fq_decode_greedy(model, [kv], [first], s, toks.data_ptr(), logits.data_ptr(), stream)
-            done += s
-        fq.fq_kv_rewind(kv, CONTEXT)
+            s_ = min(chain, n_steps - done)
+            rewind()
+            fq.fq_decode_greedy(model, kvs, first, s_, toks.data_ptr(), logits.data_ptr(), stream)
+            done += s_
+        rewind()
 
     chains(max(args.warmup, 3))
     torch.cuda.synchronize()
     barrier(world)
 
-    # ---- timed region: exactly K steps
+    # ---- timed region: exactly K steps (each step = one token for each of the n sequences)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clk:
         torch.cuda.synchronize()
@@ -294,36 +336,44 @@ def run_fq(args):
         torch.cuda.nvtx.range_pop()
         torch.cuda.synchronize()
         barrier(world)
-    dt = ev0.elapsed_time(ev1) / 1e3
-    dt = max_over_ranks(dt, world)
-    value = world * args.steps / dt
+    dt = max_over_ranks(ev0.elapsed_time(ev1) / 1e3, world)
+    value = world * n * args.steps / dt
 
-    # ---- end to end through the public API with host buffers: per step, the token goes in
-    # from pinned host memory (by value through the call) and the chosen token comes back
+    # ---- end to end through the public API with host buffers: per step the tokens go in
+    # from pinned host memory (by value through the call) and the chosen tokens come back
     # to pinned host memory before the next step is issued
-    host_tok = torch.empty(1, dtype=torch.int32, pin_memory=True)
-    e2e_steps = min(args.steps, 4 * CHAIN)
+    host_tok = torch.empty(n, dtype=torch.int32, pin_memory=True)
+    e2e_steps = min(args.steps, 4 * chain)
     torch.cuda.synchronize()
     barrier(world)
     t0 = time.perf_counter()
-    tok = first
     done = 0
     while done < e2e_steps:
-        s = min(CHAIN, e2e_steps - done)
-        fq.fq_kv_rewind(kv, CONTEXT)
-        tok = first
-        for _ in range(s):
-            fq.fq_decode_greedy(model, [kv], [tok], 1, toks.data_ptr(), 0, stream)
-            host_tok.copy_(toks[0, 0:1], non_blocking=True)
+        s_ = min(chain, e2e_steps - done)
+        rewind()
+        cur = list(first)
+        for _ in range(s_):
+            fq.fq_decode_greedy(model, kvs, cur, 1, toks.data_ptr(), 0, stream)
+            host_tok.copy_(toks[0], non_blocking=True)
             st.synchronize()
-            tok = int(host_tok[0])
-        done += s
-    fq.fq_kv_rewind(kv, CONTEXT)
+            cur = host_tok.tolist()
+        done += s_
+    rewind()
     e2e_dt = max_over_ranks(time.perf_counter() - t0, world)
-    e2e_value = world * e2e_steps / e2e_dt
+    e2e_value = world * n * e2e_steps / e2e_dt
 
-    # ---- roofline of the dominant kernel: the Q8_0 dequant GEMV, timed live on the LM
-    # head (151936 x 1024, the largest launch of the step) with CUDA events on its stream
+    # ---- experts touched per layer (MoE): from one traced step
+    experts = None
+    if d.is_moe:
+        ri = torch.empty((d.num_layers, n, d.num_experts_used), dtype=torch.int32, device=dev)
+        rw = torch.empty_like(ri, dtype=torch.float32)
+        fq.fq_decode_step_trace(model, kvs, first, 0, 0, ri.data_ptr(), rw.data_ptr(), stream)
+        torch.cuda.synchronize()
+        rewind()
+        experts = [len(set(ri[L].flatten().tolist())) for L in range(d.num_layers)]
+
+    # ---- roofline of the dominant kernel: the dequant GEMV, timed live on the LM head (the
+    # largest single launch of the step) with CUDA events on its stream
     peak, peak_kind = measured_peaks()
     x = torch.randn(d.hidden_size, device=dev)
     y = torch.empty(d.vocab_size, device=dev)
@@ -332,44 +382,54 @@ def run_fq(args):
     for _ in range(3):
         fq.fq_gemv(model, 0, fq.W_OUTPUT, 1, x.data_ptr(), y.data_ptr(), stream)
     torch.cuda.synchronize()
-    for a, b in evs:
-        a.record(st)
+    for a_, b_ in evs:
+        a_.record(st)
         fq.fq_gemv(model, 0, fq.W_OUTPUT, 1, x.data_ptr(), y.data_ptr(), stream)
-        b.record(st)
+        b_.record(st)
     torch.cuda.synchronize()
-    kt = sum(a.elapsed_time(b) for a, b in evs) / reps / 1e3
-    kbytes = d.vocab_size * d.hidden_size * 34 / 32 + d.hidden_size * 4 + d.vocab_size * 4
+    kt = sum(a_.elapsed_time(b_) for a_, b_ in evs) / reps / 1e3
+    bpw = 34 / 32 if w.weight_dtype == "q8_0" else 144 / 256
+    kbytes = d.vocab_size * d.hidden_size * bpw + d.hidden_size * 4 + d.vocab_size * 4
     achieved = kbytes / kt / 1e9
 
-    ctx_mean = CONTEXT + (CHAIN - 1) / 2
-    sb = step_bytes(d, int(round(ctx_mean)))
-    step_gbs = sb["total"] / (dt / args.steps) / 1e9
-    launches_per_step = 1 + d.num_layers * 5 + 2
-    n_chains = (args.steps + CHAIN - 1) // CHAIN
+    wb = weight_bytes(w, experts)
+    kv_read = sum(2 * d.num_layers * d.kv_dim * (c + (chain - 1) / 2) * 2 for c in ctxs)
+    kv_write = n * 2 * d.num_layers * d.kv_dim * 2
+    total = wb["layers"] + wb["lm_head"] + wb["embedding_rows"] + kv_read + kv_write
+    step_gbs = total / (dt / args.steps) / 1e9
+    per_layer = 5 if not d.is_moe else 8
+    launches_per_step = 1 + d.num_layers * per_layer + 2
+    n_chains = (args.steps + chain - 1) // chain
 
-    line = None
     if rank == 0:
-        cb = cpu_baseline(w, W, budget_s=args.cpu_budget) if (world == 1 and not args.no_cpu_baseline) else None
+        cb = None
+        if world == 1 and not args.no_cpu_baseline and w.prefill_from_model:
+            cb = cpu_baseline(w, W, budget_s=args.cpu_budget)
         line = {
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": max(args.warmup, 3), "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": config_dict(w),
-            "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": 4, "d2h_bytes_per_step": 4,
-                    "steps": e2e_steps},
+            "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": 4 * n,
+                    "d2h_bytes_per_step": 4 * n, "steps": e2e_steps},
             "gpu_launches": args.steps * launches_per_step + n_chains,
-            "roofline": {"bound": "hbm", "kernel": "gemv_kernel<Q8_0> (LM head launch, 151936x1024)",
+            "roofline": {"bound": "hbm", "kernel": f"dequant GEMV ({w.weight_dtype}), LM head launch "
+                                                   f"{d.vocab_size}x{d.hidden_size}",
                          "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                          "peak_kind": peak_kind, "bytes_per_launch": kbytes, "us_per_launch": kt * 1e6,
                          "traffic": None},
-            "step_roofline": {"bytes_per_step": sb["total"], "achieved_gbs": step_gbs, "peak": peak,
+            "step_roofline": {"bytes_per_step": total, "achieved_gbs": step_gbs, "peak": peak,
                               "frac": step_gbs / peak, "peak_kind": peak_kind,
-                              "breakdown": {k: v for k, v in sb.items() if k != "total"}},
+                              "breakdown": {"weights_layers": wb["layers"], "lm_head": wb["lm_head"],
+                                            "embedding_rows": wb["embedding_rows"], "kv_read": kv_read,
+                                            "kv_write": kv_write},
+                              "experts_per_layer": (sum(experts) / len(experts)) if experts else None},
             "clocks": clk.summary(),
             "cpu_baseline": cb,
         }
         print(json.dumps(line))
-    fq.fq_kv_free(kv)
+    for kv in kvs:
+        fq.fq_kv_free(kv)
     fq.fq_model_free(model)
     if world > 1:
         import torch.distributed as dist
@@ -441,6 +501,9 @@ def main():
     ap.add_argument("--kernel", choices=["lm_head", "layer"], default=None,
                     help="time one kernel family instead of the decode loop (profiling)")
     ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--workload", default=WORKLOAD,
+                    choices=["qwen3-0.6b", "qwen3-8b-q4k", "qwen3-8b-batch32", "qwen3-30b-a3b-batch16"],
+                    help="the default is the benchmark line; the others are measured the same way")
     ap.add_argument("--steps", type=int, default=6400)
     ap.add_argument("--warmup", type=int, default=64)
     ap.add_argument("--impl", default="fq", choices=["fq", "reference"])
@@ -450,6 +513,9 @@ def main():
     if args.kernel:
         return run_kernel(args)
     if args.impl == "reference":
+        if args.workload != WORKLOAD:
+            print(json.dumps({"impl": "reference", "unavailable": "the oracle arm times the default workload only"}))
+            return 0
         return run_reference(args)
     return run_fq(args)
 
