@@ -213,6 +213,20 @@ fq_status fq_dequant_rows(const fq_model* m, uint32_t layer, fq_weight_id which,
 fq_status fq_gemv(const fq_model* m, uint32_t layer, fq_weight_id which, uint32_t n, const float* x, float* y,
                   void* stream);
 
+/* fq_layer_step for callers that cannot allocate device memory at call time -- a host whose
+ * allocator forbids allocations after start-up, code running while a CUDA graph is being
+ * captured, an embedder that accounts for every device byte up front.  (The paper has no
+ * counterpart; this is an interface of this library.)  Same arguments, contract, errors and
+ * results as fq_layer_step, but it allocates nothing: all of the layer's scratch lives in one
+ * 2 MiB array built into the library, which every GPU that loads the library holds until
+ * the process exits.  A model + cache capacity whose layer scratch does not fit is rejected
+ * with FQ_ERR_INVALID_ARGUMENT and a message giving the size (a 0.6B- or 8B-shaped dense layer
+ * fits at any capacity up to 16K positions).  The first call on a device looks up the
+ * array's device address (once, with that device current), so make that first call before
+ * any stream capture.  Every call shares the array: calls whose GPU work overlaps (other
+ * streams, other threads) race and give wrong results; serialise them. */
+fq_status fq_layer_step_noalloc(const fq_model* m, uint32_t layer, fq_kv* kv, uint32_t pos, float* x, void* stream);
+
 /* Synchronise `stream` and report device-side failures recorded since the last check:
  * FQ_ERR_DEVICE_TIMEOUT when a kernel's bounded wait on its own copy pipeline gave up
  * (the kernel returned early; results of that step are invalid).  Clears the record. */

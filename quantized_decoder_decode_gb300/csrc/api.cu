@@ -971,3 +971,104 @@ fq_status fq_dequant_rows(const fq_model* m, uint32_t layer, fq_weight_id which,
 }
 
 }  // extern "C"
+
+// ==================================================================== layer step without allocation
+//
+// For callers that cannot call cudaMalloc (or must not have a library do it for them):
+// an allocator that forbids device allocations after start-up, a CUDA graph that is being
+// captured, or a host that pre-plans every byte of device memory.  The one layer step below
+// keeps all of its scratch -- the step state, the raw QKV projections, the attention
+// output and split-K partials, the arrival counters, the FFN activations -- in one
+// file-scope device array instead of the per-stream workspace.  Every GPU that loads this
+// library holds the array until the process exits.
+
+namespace {
+
+constexpr size_t NOALLOC_SCRATCH_BYTES = 2u << 20;   // 2 MiB
+__device__ __align__(256) unsigned char g_noalloc_scratch[NOALLOC_SCRATCH_BYTES];
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[64] = {};
+
+// Device address of the array on the current device.  In host code the symbol is only a
+// host-side stand-in, so the address is looked up once per device (with that device
+// current) and cached.
+fq_status noalloc_base(void** out) {
+    int dev = 0;
+    CK(cudaGetDevice(&dev));
+    if (dev < 0 || dev >= 64) return fail(FQ_ERR_INVALID_ARGUMENT, "device %d beyond the scratch table", dev);
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void* p = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess || !p)
+            return fail(FQ_ERR_CUDA, "cudaGetSymbolAddress(scratch): %s", cudaGetErrorString(e));
+        g_noalloc_ptr[dev] = p;
+    }
+    *out = g_noalloc_ptr[dev];
+    return FQ_OK;
+}
+
+}  // namespace
+
+extern "C" fq_status fq_layer_step_noalloc(const fq_model* m, uint32_t layer, fq_kv* kv, uint32_t pos, float* x,
+                                           void* stream) {
+    if (!m || !kv || !x) return fail(FQ_ERR_INVALID_ARGUMENT, "null argument");
+    if (layer >= m->d.p.num_layers) return fail(FQ_ERR_INVALID_ARGUMENT, "layer %u out of range", layer);
+    if (kv->m != m) return fail(FQ_ERR_MISMATCHED_KV_CACHES, "cache belongs to another model");
+    if (pos != kv->len) return fail(FQ_ERR_INVALID_SEQUENCE_LENGTH, "pos %u != len %u", pos, kv->len);
+    if ((uint64_t)pos + 1 > kv->cap) return fail(FQ_ERR_KV_CACHE_OVERFLOW, "len %u at capacity", kv->len);
+    const auto& p = m->d.p;
+    int chunk, splits;
+    attn_split(1, p.num_key_value_heads, kv->cap, chunk, splits);
+
+    // carve the array: every piece 256-byte aligned
+    size_t off = 0;
+    auto take = [&](size_t bytes) { size_t o = off; off += (bytes + 255) & ~(size_t)255; return o; };
+    const size_t o_st = take(sizeof(StepState));
+    const size_t o_qkv = take(sizeof(float) * m->qkv_rows());
+    const size_t o_attn = take(sizeof(float) * p.num_attention_heads * HEAD_DIM);
+    const size_t o_part = take(sizeof(float) * p.num_attention_heads * splits * (HEAD_DIM + 2));
+    const size_t o_ctr = take(sizeof(uint32_t) * p.num_key_value_heads);
+    size_t o_h = 0, o_xn = 0, o_rl = 0, o_he = 0, o_ye = 0, o_route = 0;
+    if (!m->moe()) {
+        o_h = take(sizeof(float) * p.intermediate_size);
+    } else {
+        o_xn = take(sizeof(float) * p.hidden_size);
+        o_rl = take(sizeof(float) * p.num_experts);
+        o_he = take(sizeof(float) * p.num_experts_used * p.moe_intermediate_size);
+        o_ye = take(sizeof(float) * p.num_experts_used * p.hidden_size);
+        o_route = take(sizeof(MoeRoute));
+    }
+    if (off > NOALLOC_SCRATCH_BYTES)
+        return fail(FQ_ERR_INVALID_ARGUMENT,
+                    "layer step needs %zu bytes of scratch for this model and cache capacity; the built-in "
+                    "array holds %zu (use fq_layer_step)",
+                    off, NOALLOC_SCRATCH_BYTES);
+    void* base = nullptr;
+    TRY(noalloc_base(&base));
+    unsigned char* b = (unsigned char*)base;
+    Workspace w;   // a view into the array; owns nothing
+    w.n_cap = 1;
+    w.st = (StepState*)(b + o_st);
+    w.qkv = (float*)(b + o_qkv);
+    w.attn = (float*)(b + o_attn);
+    w.part = (float*)(b + o_part);
+    w.counters = (uint32_t*)(b + o_ctr);
+    if (!m->moe()) {
+        w.h = (float*)(b + o_h);
+    } else {
+        w.xn = (float*)(b + o_xn);
+        w.rlogits = (float*)(b + o_rl);
+        w.he = (float*)(b + o_he);
+        w.ye = (float*)(b + o_ye);
+        w.route = (MoeRoute*)(b + o_route);
+    }
+    cudaStream_t s = (cudaStream_t)stream;
+    // the arrival counters must start at zero; the array keeps whatever the last call left
+    CK(cudaMemsetAsync(w.counters, 0, sizeof(uint32_t) * p.num_key_value_heads, s));
+    fq_kv* caches[1] = {kv};
+    TRY(setup_state(&w, caches, nullptr, 1, false, nullptr, nullptr, s));
+    Body body{m, &w, 1, chunk, splits, nullptr, false};
+    return enqueue_step(body, s, kv->bf16, x, (int)layer);
+}

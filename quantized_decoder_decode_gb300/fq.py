@@ -89,6 +89,7 @@ def lib():
                 "fq_layer_step_trace": [vp, u32, vp, u32, vp, vp, vp, vp, vp],
                 "fq_gemv": [vp, u32, ctypes.c_int, u32, vp, vp, vp],
                 "fq_check_device": [vp, vp],
+                "fq_layer_step_noalloc": [vp, u32, vp, u32, vp, vp],
             }
             for name, args in sig.items():
                 fn = getattr(L, name)
@@ -113,7 +114,7 @@ def lib():
 EXPORTED = ("fq_desc_init", "fq_load_weights", "fq_model_free", "fq_kv_init", "fq_kv_free", "fq_kv_len",
             "fq_kv_capacity", "fq_kv_append", "fq_kv_commit", "fq_kv_rewind", "fq_kv_read", "fq_layer_step", "fq_decode_step",
             "fq_decode_step_batch", "fq_decode_greedy", "fq_decode_step_trace", "fq_dequant_rows", "fq_layer_step_trace",
-            "fq_gemv", "fq_check_device", "fq_last_error",
+            "fq_gemv", "fq_check_device", "fq_layer_step_noalloc", "fq_last_error",
             "fq_status_str")
 
 
@@ -273,3 +274,8 @@ def fq_gemv(model: int, layer: int, which: int, n: int, x_ptr: int, y_ptr: int, 
 
 def fq_check_device(model: int, stream: int = 0) -> None:
     _check(lib().fq_check_device(model, stream), "fq_check_device")
+
+
+def fq_layer_step_noalloc(model: int, layer: int, kv: int, pos: int, x_ptr: int, stream: int = 0) -> None:
+    """fq_layer_step without any device allocation (scratch lives in a built-in array)."""
+    _check(lib().fq_layer_step_noalloc(model, layer, kv, pos, x_ptr, stream), "fq_layer_step_noalloc")
