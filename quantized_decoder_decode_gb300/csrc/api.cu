@@ -101,6 +101,7 @@ struct Workspace {
     StepState* st = nullptr;
     float *x = nullptr, *qkv = nullptr, *attn = nullptr, *h = nullptr, *part = nullptr, *logits = nullptr;
     float *xn = nullptr, *rlogits = nullptr, *he = nullptr, *ye = nullptr;
+    void* xh = nullptr;        // f16 hi/lo activations for the tensor-core GEMM (batches >= 8)
     uint32_t* counters = nullptr;
     MoeRoute* route = nullptr;
     std::vector<void*> allocs;
@@ -190,6 +191,13 @@ fq_status ensure_ws(const fq_model* mc, cudaStream_t stream, int n, uint32_t cap
         TRY(dalloc(A, &w->counters, (size_t)nn * p.num_key_value_heads));
         TRY(dalloc(A, &w->logits, (size_t)nn * p.vocab_size));
         CK(cudaMemsetAsync(w->counters, 0, sizeof(uint32_t) * nn * p.num_key_value_heads, stream));
+        if (nn >= TC_MIN_BATCH) {
+            const int kmax = (int)std::max<size_t>({H, (size_t)p.num_attention_heads * HEAD_DIM,
+                                                     (size_t)std::max<uint32_t>(p.intermediate_size, 1)});
+            uint16_t* xh;
+            TRY(dalloc(A, &xh, gemm_tc_xh_elems(kmax)));
+            w->xh = xh;
+        }
         CK(cudaMemsetAsync(w->st, 0, sizeof(StepState), stream));
         if (m->moe()) {
             size_t k = p.num_experts_used;
@@ -233,7 +241,18 @@ fq_status enqueue_step(const Body& b, cudaStream_t s, int kv_bf16, float* x_over
     // Programmatic dependent launch is opt-in: measured on GB300 the early-resident CTAs of
     // the next kernel slowed the step down (FQ_PDL=1 enables it)
     static const bool use_pdl = env_flag("FQ_PDL");
+    static const bool no_tc = env_flag("FQ_NO_TC");
     auto pdl = [&]() { bool r = !first && use_pdl; first = false; return r; };
+    // dense projection: tensor cores for lockstep batches, the GEMV kernels otherwise
+    auto proj = [&](GemvArgs& g) {
+        g.err = m->err;
+        if (!no_tc && w->xh && gemm_tc_applicable(g)) {
+            const bool p0 = pdl();
+            launch_gemm_tc(g, w->xh, s, p0, use_pdl);
+        } else {
+            launch_gemv(g, s, pdl());
+        }
+    };
     float* x = x_override ? x_override : w->x;
 
     if (layer_only < 0) launch_embed(m->tok_embd, w->st, n, x, s, pdl());
@@ -244,8 +263,7 @@ fq_status enqueue_step(const Body& b, cudaStream_t s, int kv_bf16, float* x_over
         g.W = lw.qkv; g.B = n; g.x = x; g.x_stride = H; g.norm_g = lw.attn_norm; g.eps = p.rms_norm_eps;
         g.y = w->qkv; g.y_stride = m->qkv_rows(); g.epi = EPI_STORE;
         g.ksplit = choose_ksplit(g.W, rows_per_warp(g.W));
-        g.err = m->err;
-        launch_gemv(g, s, pdl());
+        proj(g);
 
         AttnArgs a;
         a.qkv = w->qkv; a.qkv_stride = m->qkv_rows(); a.q_norm = lw.q_norm; a.k_norm = lw.k_norm;
@@ -257,22 +275,19 @@ fq_status enqueue_step(const Body& b, cudaStream_t s, int kv_bf16, float* x_over
         GemvArgs o;
         o.W = lw.o; o.B = n; o.x = w->attn; o.x_stride = Hq * HEAD_DIM; o.y = x; o.y_stride = H; o.epi = EPI_ADD;
         o.ksplit = choose_ksplit(o.W, rows_per_warp(o.W));
-        o.err = m->err;
-        launch_gemv(o, s, pdl());
+        proj(o);
 
         if (!m->moe()) {
             GemvArgs gu;
             gu.W = lw.gate_up; gu.B = n; gu.x = x; gu.x_stride = H; gu.norm_g = lw.ffn_norm; gu.eps = p.rms_norm_eps;
             gu.y = w->h; gu.y_stride = p.intermediate_size; gu.epi = EPI_SWIGLU;
             gu.ksplit = choose_ksplit(gu.W, rows_per_warp(gu.W));
-            gu.err = m->err;
-            launch_gemv(gu, s, pdl());
+            proj(gu);
 
             GemvArgs dn;
             dn.W = lw.down; dn.B = n; dn.x = w->h; dn.x_stride = p.intermediate_size; dn.y = x; dn.y_stride = H;
             dn.epi = EPI_ADD; dn.ksplit = choose_ksplit(dn.W, rows_per_warp(dn.W));
-            dn.err = m->err;
-            launch_gemv(dn, s, pdl());
+            proj(dn);
         } else {
             const int E = p.num_experts, k = p.num_experts_used, Fe = p.moe_intermediate_size;
             GemvArgs r;
@@ -318,8 +333,7 @@ fq_status enqueue_step(const Body& b, cudaStream_t s, int kv_bf16, float* x_over
         lm.W = m->output; lm.B = n; lm.x = x; lm.x_stride = H; lm.norm_g = m->output_norm; lm.eps = p.rms_norm_eps;
         lm.y = b.logits; lm.y_stride = p.vocab_size; lm.epi = b.greedy ? EPI_LOGITS : EPI_STORE; lm.st = w->st;
         lm.ksplit = choose_ksplit(lm.W, rows_per_warp(lm.W));
-        lm.err = m->err;
-        launch_gemv(lm, s, pdl());
+        proj(lm);
         if (b.greedy) launch_lm_finish(w->st, n, (int)p.vocab_size, s, pdl());
     }
     CK(cudaGetLastError());
@@ -612,6 +626,7 @@ fq_status fq_load_weights(const fq_desc* d, const fq_weight_src* src, void* stre
     int dev = 0;
     CK(cudaGetDevice(&dev));
     gemv_prepare();
+    gemm_tc_prepare();
     CK(cudaGetLastError());
     fq_model* m = new fq_model();
     m->d = *d;
@@ -904,7 +919,11 @@ fq_status fq_gemv(const fq_model* m, uint32_t layer, fq_weight_id which, uint32_
     g.W = W; g.B = (int)n; g.x = x; g.x_stride = W.K; g.y = y; g.y_stride = W.N; g.epi = EPI_STORE;
     g.ksplit = choose_ksplit(W, rows_per_warp(W));
     g.err = m->err;
-    launch_gemv(g, (cudaStream_t)stream, false);
+    cudaStream_t s = (cudaStream_t)stream;
+    Workspace* w = nullptr;
+    if (n >= (uint32_t)TC_MIN_BATCH) TRY(ensure_ws(m, s, (int)n, 1, &w));
+    if (w && w->xh && gemm_tc_applicable(g) && !env_flag("FQ_NO_TC")) launch_gemm_tc(g, w->xh, s, false, false);
+    else launch_gemv(g, s, false);
     CK(cudaGetLastError());
     return FQ_OK;
 }

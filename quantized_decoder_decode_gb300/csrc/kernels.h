@@ -106,6 +106,14 @@ void gemv_tma_prepare();
 // build the tensor maps of W's planes for the bulk-copy GEMV (false: not applicable)
 bool make_tma_maps(const QMat& W, TmaMaps* out);
 
+// tcgen05 GEMM for lockstep batches of TC_MIN_BATCH..32 rows over Q8_0 weights: a prep
+// kernel (RMSNorm + f16 hi/lo split into xh, 64 x K halves) and the GEMM
+constexpr int TC_MIN_BATCH = 8;
+void gemm_tc_prepare();
+bool gemm_tc_applicable(const GemvArgs& a);
+size_t gemm_tc_xh_elems(int K);
+void launch_gemm_tc(const GemvArgs& a, void* xh, cudaStream_t s, bool pdl_prep, bool pdl);
+
 // Attention with fused QK-norm + rope + KV append (one query row per sequence).
 struct AttnArgs {
     const float* qkv;             // [n][(Hq + 2 Hkv) * 128] raw projections

@@ -134,10 +134,12 @@ def test_decode_steps_match_oracle(pair_factory, dims, wtype, kv):
     assert fq.fq_kv_len(kvc) == 103
 
 
-@pytest.mark.parametrize("dims", [SMALL_G4, SMALL_MOE])
-def test_batch_ragged_matches_oracle(pair_factory, dims):
+@pytest.mark.parametrize("dims,ctxs", [(SMALL_G4, [37, 100, 250, 1, 64]), (SMALL_MOE, [37, 100, 250, 1, 64]),
+                                       (SMALL_G4, [37, 100, 250, 1, 64, 5, 129, 200, 77, 33, 160, 2]),
+                                       (SMALL_MOE, [70, 3, 250, 129, 64, 90, 11, 130, 190])])
+def test_batch_ragged_matches_oracle(pair_factory, dims, ctxs):
+    """Batches of 8+ run the dense projections on the tcgen05 GEMM."""
     p = pair_factory(workload(dims, "q8_0", "bf16", seed=33), max_positions=1024)
-    ctxs = [37, 100, 250, 1, 64]
     kvs, ocs = [], []
     for s, c in enumerate(ctxs):
         kvc, oc = p.new_seq(capacity=300, ctx=c, seq=s)

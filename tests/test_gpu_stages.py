@@ -36,9 +36,10 @@ def _gemv_ref(wtype, W, rows, cols, x):
     return oracle.gemv(wtype, W, rows, cols, x)
 
 
-@pytest.mark.parametrize("wtype", ["q8_0", "q4_k"])
-@pytest.mark.parametrize("n", [1, 3, 6])
+@pytest.mark.parametrize("wtype,n", [("q8_0", 1), ("q8_0", 3), ("q8_0", 6), ("q4_k", 1), ("q4_k", 3), ("q4_k", 6),
+                                     ("q8_0", 8), ("q8_0", 13), ("q8_0", 32)])
 def test_weight_gemv_matches_oracle(pair_factory, wtype, n):
+    """n >= 8 on Q8_0 runs the tcgen05 GEMM (f16 weights, f16 hi/lo activations)."""
     d = dataclasses.replace(SMALL, hidden_size=512, intermediate_size=768 if wtype == "q8_0" else 1024)
     p = pair_factory(wl.Workload("g", d, wtype, "bf16", seed=71), with_oracle=False)
     lw = p.W["layers"][1]
