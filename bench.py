@@ -439,8 +439,9 @@ def run_fq(args):
 
 def run_kernel(args):
     """Kernel-level timing for profiling: the LM-head GEMV alone (--kernel lm_head) or one
-    decoder layer step at context 2048 (--kernel layer), `--steps` launches after
-    `--warmup`, on the 0.6B workload's weights."""
+    decoder layer step at the workload's context (--kernel layer), `--steps` launches after
+    `--warmup`, on one layer of the chosen workload's weights."""
+    import dataclasses
     import torch
     import synth.workloads as wl
     from quantized_decoder_decode_gb300 import fq
@@ -448,45 +449,50 @@ def run_kernel(args):
     dev = torch.device("cuda", 0)
     st = torch.cuda.current_stream(dev)
     stream = st.cuda_stream
-    w = wl.WORKLOADS[WORKLOAD]
+    w = wl.WORKLOADS[args.workload]
     d = w.dims
-    W = wl.make_weights(wl.scaled(w, num_layers=1), layers=range(1))
+    ctx = CONTEXT if w.prefill_from_model else int(w.contexts().max())
+    w1 = wl.scaled(w, num_layers=1)
+    W = wl.make_weights(w1)
     desc = fq.fq_desc_init(vocab_size=d.vocab_size, hidden_size=d.hidden_size, intermediate_size=d.intermediate_size,
                            num_layers=1, num_attention_heads=d.num_attention_heads,
-                           num_key_value_heads=d.num_key_value_heads, head_dim=d.head_dim, max_positions=4096)
+                           num_key_value_heads=d.num_key_value_heads, head_dim=d.head_dim,
+                           num_experts=d.num_experts, num_experts_used=d.num_experts_used,
+                           moe_intermediate_size=d.moe_intermediate_size, max_positions=ctx + 64)
     src, keep = fq.weight_src(desc, W, w.weight_dtype)
     model = fq.fq_load_weights(desc, src, stream)
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    bpw = 34 / 32 if w.weight_dtype == "q8_0" else 144 / 256
     if args.kernel == "lm_head":
         x = torch.randn(d.hidden_size, device=dev)
         y = torch.empty(d.vocab_size, device=dev)
         call = lambda: fq.fq_gemv(model, 0, fq.W_OUTPUT, 1, x.data_ptr(), y.data_ptr(), stream)  # noqa: E731
-        nbytes = d.vocab_size * d.hidden_size * 34 / 32
+        nbytes = d.vocab_size * d.hidden_size * bpw
     else:
-        kv = fq.fq_kv_init(model, CONTEXT + 1, "bf16")
-        k, v = wl.make_kv_prior(w, 0, 0, CONTEXT)
+        kv = fq.fq_kv_init(model, ctx + 1, "bf16")
+        k, v = wl.make_kv_prior(w1, 0, 0, ctx)
         kt = torch.from_numpy(k.view(np.int16)).to(dev)
         vt = torch.from_numpy(v.view(np.int16)).to(dev)
-        fq.fq_kv_append(kv, 0, 0, CONTEXT, kt.data_ptr(), vt.data_ptr(), stream)
-        fq.fq_kv_commit(kv, CONTEXT)
-        x = torch.from_numpy(wl.layer_input(w)).to(dev)
-        call = lambda: fq.fq_layer_step(model, 0, kv, CONTEXT, x.data_ptr(), stream)  # noqa: E731
-        sb = step_bytes(dataclasses_replace_layers(d), CONTEXT)
-        nbytes = sb["weights"] + sb["kv_read"] + sb["kv_write"]
+        fq.fq_kv_append(kv, 0, 0, ctx, kt.data_ptr(), vt.data_ptr(), stream)
+        fq.fq_kv_commit(kv, ctx)
+        x = torch.from_numpy(wl.layer_input(w1)).to(dev)
+        call = lambda: fq.fq_layer_step(model, 0, kv, ctx, x.data_ptr(), stream)  # noqa: E731
+        wb = weight_bytes(dataclasses.replace(w1, batch=1))
+        nbytes = wb["layers"] + 2 * d.kv_dim * ctx * 2
     for _ in range(args.warmup):
         call()
     torch.cuda.synchronize()
-    for a, b in evs:
-        a.record(st)
+    for a_, b_ in evs:
+        a_.record(st)
         call()
-        b.record(st)
+        b_.record(st)
     torch.cuda.synchronize()
-    t = [a.elapsed_time(b) / 1e3 for a, b in evs]
+    t = [a_.elapsed_time(b_) / 1e3 for a_, b_ in evs]
     mean = sum(t) / len(t)
     peak, kind = measured_peaks()
-    print(json.dumps({"kernel": args.kernel, "launches": len(t), "us_mean": mean * 1e6, "us_min": min(t) * 1e6,
-                      "bytes": nbytes, "gbs": nbytes / mean / 1e9, "frac": nbytes / mean / 1e9 / peak,
-                      "peak": peak, "peak_kind": kind}))
+    print(json.dumps({"kernel": args.kernel, "workload": w.name, "launches": len(t), "us_mean": mean * 1e6,
+                      "us_min": min(t) * 1e6, "bytes": nbytes, "gbs": nbytes / mean / 1e9,
+                      "frac": nbytes / mean / 1e9 / peak, "peak": peak, "peak_kind": kind}))
     fq.fq_model_free(model)
     return 0
 

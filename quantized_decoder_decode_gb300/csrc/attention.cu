@@ -95,6 +95,51 @@ __global__ void __launch_bounds__(ATT_THREADS) attn_kernel(const AttnArgs a) {
     const float2* rope_row = a.rope + (size_t)pos * (HEAD_DIM / 2);
     const float qscale = LOG2E * rsqrtf((float)HEAD_DIM);
 
+    // ---- the warp's first tile of K/V rows goes out before anything else: its latency is
+    // then shared with the q prologue below.  Rows before pos were written by earlier steps.
+    float m_run[G], l_run[G], acc[G][4];
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+        m_run[h] = -INFINITY;
+        l_run[h] = 0.f;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[h][j] = 0.f;
+    }
+    constexpr int KW = KVT == 1 ? 16 : 32;      // 16-byte words per K row
+    constexpr int VW = KVT == 1 ? 2 : 4;        // 32-bit words of one lane's 4 V dims
+    constexpr int KPRE = KVT == 1 ? 16 : 1;     // K words held in registers across the prologue
+    uint32_t vr[32][VW];
+    uint4 kr[KPRE];
+    auto issue = [&](int tb) {
+        const int t = tb + lane;
+        const int nvalid = min(32, t1 - tb);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            const int ti = tb + i;
+            if (i < nvalid && ti != pos) {
+                if constexpr (KVT == 1) {
+                    uint2 w = ld_stream8(Vc + (size_t)ti * HEAD_DIM + 4 * lane);
+                    vr[i][0] = w.x; vr[i][1] = w.y;
+                } else {
+                    uint4 w = ld_stream16(Vc + (size_t)ti * HEAD_DIM + 4 * lane);
+                    vr[i][0] = w.x; vr[i][1] = w.y; vr[i][2] = w.z; vr[i][3] = w.w;
+                }
+            }
+        }
+        if constexpr (KVT == 1) {
+            if (t < t1 && t != pos) {
+                const char* krow = reinterpret_cast<const char*>(Kc + (size_t)t * HEAD_DIM);
+#pragma unroll
+                for (int c = 0; c < KPRE; ++c) kr[c] = ld_stream16(krow + 16 * c);
+            } else {
+#pragma unroll
+                for (int c = 0; c < KPRE; ++c) kr[c] = make_uint4(0u, 0u, 0u, 0u);   // masked or fresh
+            }
+        }
+    };
+    int tb = t0 + warp * 32;
+    if (tb < t1) issue(tb);
+
     // ---- q heads of the group: RMSNorm, rope, scale
     for (int hh = warp; hh < G; hh += ATT_WARPS) {
         int h = g * G + hh;
@@ -119,19 +164,10 @@ __global__ void __launch_bounds__(ATT_THREADS) attn_kernel(const AttnArgs a) {
     }
     __syncthreads();
 
-    // ---- tiles of 32 positions, interleaved over warps; every K and V load of a tile is
-    // issued before any arithmetic so that one memory latency covers the whole tile
-    float m_run[G], l_run[G], acc[G][4];
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-        m_run[h] = -INFINITY;
-        l_run[h] = 0.f;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) acc[h][j] = 0.f;
-    }
-    constexpr int KW = KVT == 1 ? 16 : 32;      // 16-byte words per K row
-    constexpr int VW = KVT == 1 ? 2 : 4;        // 32-bit words of one lane's 4 V dims
-    for (int tb = t0 + warp * 32; tb < t1; tb += ATT_WARPS * 32) {
+    // ---- tiles of 32 positions, interleaved over warps; every K and V load of a tile is in
+    // flight before its arithmetic starts
+    for (bool first = true; tb < t1; tb += ATT_WARPS * 32, first = false) {
+        if (!first) issue(tb);
         const int t = tb + lane;
         const bool valid = t < t1;
         const bool fresh = t == pos;            // the new position lives in shared memory
@@ -139,33 +175,23 @@ __global__ void __launch_bounds__(ATT_THREADS) attn_kernel(const AttnArgs a) {
         float sc[G];
 #pragma unroll
         for (int h = 0; h < G; ++h) sc[h] = 0.f;
-        // V words of this lane's 4 dims for the tile's positions (loaded first, used last)
-        uint32_t vr[32][VW];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            const int ti = tb + i;
-            if (i < nvalid && ti != pos) {
-                if constexpr (KVT == 1) {
-                    uint2 w = ld_stream8(Vc + (size_t)ti * HEAD_DIM + 4 * lane);
-                    vr[i][0] = w.x; vr[i][1] = w.y;
-                } else {
-                    uint4 w = ld_stream16(Vc + (size_t)ti * HEAD_DIM + 4 * lane);
-                    vr[i][0] = w.x; vr[i][1] = w.y; vr[i][2] = w.z; vr[i][3] = w.w;
-                }
-            }
-        }
-        // scores: one lane per position, the whole K row in flight
+        // scores: one lane per position along its K row
         constexpr int KB = 16;                  // words per batch
 #pragma unroll
         for (int c0 = 0; c0 < KW; c0 += KB) {
-            uint4 kr[KB];
-            if (valid && !fresh) {
-                const T* krow = Kc + (size_t)t * HEAD_DIM;
+            uint4 kb[KB];
+            if constexpr (KVT == 1) {
 #pragma unroll
-                for (int c = 0; c < KB; ++c) kr[c] = ld_stream16(reinterpret_cast<const char*>(krow) + 16 * (c0 + c));
+                for (int c = 0; c < KB; ++c) kb[c] = kr[c];
             } else {
+                if (valid && !fresh) {
+                    const char* krow = reinterpret_cast<const char*>(Kc + (size_t)t * HEAD_DIM);
 #pragma unroll
-                for (int c = 0; c < KB; ++c) kr[c] = make_uint4(0u, 0u, 0u, 0u);   // unused: masked or fresh
+                    for (int c = 0; c < KB; ++c) kb[c] = ld_stream16(krow + 16 * (c0 + c));
+                } else {
+#pragma unroll
+                    for (int c = 0; c < KB; ++c) kb[c] = make_uint4(0u, 0u, 0u, 0u);
+                }
             }
 #pragma unroll
             for (int c = 0; c < KB; ++c) {
@@ -176,11 +202,11 @@ __global__ void __launch_bounds__(ATT_THREADS) attn_kernel(const AttnArgs a) {
 #pragma unroll
                     for (int e = 0; e < EPW; ++e) kf[e] = kn[e0 + e];
                 } else if constexpr (KVT == 1) {
-                    kf[0] = bf_lo(kr[c].x); kf[1] = bf_hi(kr[c].x); kf[2] = bf_lo(kr[c].y); kf[3] = bf_hi(kr[c].y);
-                    kf[4] = bf_lo(kr[c].z); kf[5] = bf_hi(kr[c].z); kf[6] = bf_lo(kr[c].w); kf[7] = bf_hi(kr[c].w);
+                    kf[0] = bf_lo(kb[c].x); kf[1] = bf_hi(kb[c].x); kf[2] = bf_lo(kb[c].y); kf[3] = bf_hi(kb[c].y);
+                    kf[4] = bf_lo(kb[c].z); kf[5] = bf_hi(kb[c].z); kf[6] = bf_lo(kb[c].w); kf[7] = bf_hi(kb[c].w);
                 } else {
-                    kf[0] = __uint_as_float(kr[c].x); kf[1] = __uint_as_float(kr[c].y);
-                    kf[2] = __uint_as_float(kr[c].z); kf[3] = __uint_as_float(kr[c].w);
+                    kf[0] = __uint_as_float(kb[c].x); kf[1] = __uint_as_float(kb[c].y);
+                    kf[2] = __uint_as_float(kb[c].z); kf[3] = __uint_as_float(kb[c].w);
                 }
 #pragma unroll
                 for (int h = 0; h < G; ++h) {
@@ -261,10 +287,10 @@ __global__ void __launch_bounds__(ATT_THREADS) attn_kernel(const AttnArgs a) {
     }
     if (n_act == 1) return;
 
-    // ---- last CTA of this (sequence, kv head) merges the chunks
-    __threadfence();
+    // ---- last CTA of this (sequence, kv head) merges the chunks (atomic ticket, no waiting)
     __syncthreads();
     if (tid == 0) {
+        __threadfence();                        // release this CTA's partial (written above)
         uint32_t* ctr = a.counters + (size_t)b * a.Hkv + g;
         uint32_t prev = atomicAdd(ctr, 1u);
         is_last = (prev == (uint32_t)(n_act - 1));
@@ -273,19 +299,60 @@ __global__ void __launch_bounds__(ATT_THREADS) attn_kernel(const AttnArgs a) {
     __syncthreads();
     if (!is_last) return;
     __threadfence();
+    // (m, l) of every (head, chunk) into shared memory (reusing ow), then per-chunk weights
+    // exp2(m - M) / L, then each thread d sums the chunks' o[d] with independent loads
+    float* wm = &ow[0][0][0];                   // [G][n_act]
+    float* wl = wm + G * n_act;
+    __shared__ float hM[G], hL[G];
+    const bool fits = 2 * G * n_act <= ATT_WARPS * G * HEAD_DIM;
     for (int h = 0; h < G; ++h) {
         const int hq = g * G + h;
         const float* base = a.part + ((size_t)b * a.Hq + hq) * a.splits * (HEAD_DIM + 2);
-        float M = -INFINITY;
-        for (int c = 0; c < n_act; ++c) M = fmaxf(M, __ldcg(base + (size_t)c * (HEAD_DIM + 2)));
-        float L = 0.f, O = 0.f;
-        for (int c = 0; c < n_act; ++c) {
-            const float* p = base + (size_t)c * (HEAD_DIM + 2);
-            float w = exp2f(__ldcg(p) - M);
-            L += __ldcg(p + 1) * w;
-            O += __ldcg(p + 2 + d) * w;
+        if (!fits) {                            // very long caches: plain loop
+            float M = -INFINITY;
+            for (int c = 0; c < n_act; ++c) M = fmaxf(M, __ldcg(base + (size_t)c * (HEAD_DIM + 2)));
+            float L = 0.f, O = 0.f;
+            for (int c = 0; c < n_act; ++c) {
+                const float* p = base + (size_t)c * (HEAD_DIM + 2);
+                float w = exp2f(__ldcg(p) - M);
+                L += __ldcg(p + 1) * w;
+                O += __ldcg(p + 2 + d) * w;
+            }
+            outb[(size_t)hq * HEAD_DIM + d] = O / L;
         }
-        outb[(size_t)hq * HEAD_DIM + d] = O / L;
+    }
+    if (fits) {
+        for (int i = tid; i < G * n_act; i += ATT_THREADS) {
+            const int h = i / n_act, c = i % n_act;
+            const float* p = a.part + (((size_t)b * a.Hq + g * G + h) * a.splits + c) * (HEAD_DIM + 2);
+            wm[i] = __ldcg(p);
+            wl[i] = __ldcg(p + 1);
+        }
+        __syncthreads();
+        if (tid < G) {
+            float M = -INFINITY, L = 0.f;
+            for (int c = 0; c < n_act; ++c) M = fmaxf(M, wm[tid * n_act + c]);
+            for (int c = 0; c < n_act; ++c) L += wl[tid * n_act + c] * exp2f(wm[tid * n_act + c] - M);
+            hM[tid] = M;
+            hL[tid] = 1.f / L;
+        }
+        __syncthreads();
+        for (int i = tid; i < G * n_act; i += ATT_THREADS) wm[i] = exp2f(wm[i] - hM[i / n_act]) * hL[i / n_act];
+        __syncthreads();
+        for (int h = 0; h < G; ++h) {
+            const int hq = g * G + h;
+            const float* base = a.part + ((size_t)b * a.Hq + hq) * a.splits * (HEAD_DIM + 2) + 2 + d;
+            float O = 0.f;
+            for (int c0 = 0; c0 < n_act; c0 += 8) {
+                float v[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) v[j] = c0 + j < n_act ? __ldcg(base + (size_t)(c0 + j) * (HEAD_DIM + 2)) : 0.f;
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    if (c0 + j < n_act) O = fmaf(wm[h * n_act + c0 + j], v[j], O);
+            }
+            outb[(size_t)hq * HEAD_DIM + d] = O;
+        }
     }
 }
 
