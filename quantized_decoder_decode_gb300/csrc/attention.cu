@@ -172,9 +172,9 @@ __global__ void __launch_bounds__(ATT_THREADS) attn_kernel(const AttnArgs a) {
         const bool valid = t < t1;
         const bool fresh = t == pos;            // the new position lives in shared memory
         const int nvalid = min(32, t1 - tb);
-        float sc[G];
+        float sc[G], sc2[G];                    // two partial sums per head (shorter chains)
 #pragma unroll
-        for (int h = 0; h < G; ++h) sc[h] = 0.f;
+        for (int h = 0; h < G; ++h) sc[h] = sc2[h] = 0.f;
         // scores: one lane per position along its K row
         constexpr int KB = 16;                  // words per batch
 #pragma unroll
@@ -213,12 +213,18 @@ __global__ void __launch_bounds__(ATT_THREADS) attn_kernel(const AttnArgs a) {
 #pragma unroll
                     for (int e = 0; e < EPW; e += 4) {
                         float4 q4 = *reinterpret_cast<const float4*>(&qs[h][e0 + e]);
-                        sc[h] += q4.x * kf[e] + q4.y * kf[e + 1] + q4.z * kf[e + 2] + q4.w * kf[e + 3];
+                        float& acc_h = ((c + e / 4) & 1) ? sc2[h] : sc[h];
+                        acc_h = fmaf(q4.x, kf[e], acc_h);
+                        acc_h = fmaf(q4.y, kf[e + 1], acc_h);
+                        acc_h = fmaf(q4.z, kf[e + 2], acc_h);
+                        acc_h = fmaf(q4.w, kf[e + 3], acc_h);
                     }
                 }
             }
         }
         // online softmax over the tile (base 2; q carries log2(e)/sqrt(D))
+#pragma unroll
+        for (int h = 0; h < G; ++h) sc[h] += sc2[h];
 #pragma unroll
         for (int h = 0; h < G; ++h) {
             float mt = warp_max(valid ? sc[h] : -INFINITY);

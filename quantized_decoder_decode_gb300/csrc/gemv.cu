@@ -86,8 +86,9 @@ __global__ void __launch_bounds__(THREADS) gemv_kernel(const GemvArgs a) {
         return a.y + r * a.y_stride;
     };
 
-    float* xs = smem;                                                 // [NBG][K]
-    float* xsum16 = smem + NBG * K;                                   // [NBG][K/16] (Q4_K)
+    const int KP = xpad_len<FMT>(K);                                  // padded row length
+    float* xs = smem;                                                 // [NBG][KP]
+    float* xsum16 = smem + NBG * KP;                                  // [NBG][K/16] (Q4_K)
     float* red = xsum16 + (FMT == FMT_Q4_K ? NBG * (K / 16) : 0);     // [WARPS][R][NBG]
     float* ssw = red + WARPS * R * NBG;                               // [WARPS][NBG]
     __shared__ unsigned long long best[NBG];
@@ -111,7 +112,7 @@ __global__ void __launch_bounds__(THREADS) gemv_kernel(const GemvArgs a) {
                     float4 g = *reinterpret_cast<const float4*>(a.norm_g + k);
                     v.x *= g.x; v.y *= g.y; v.z *= g.z; v.w *= g.w;
                 }
-                *reinterpret_cast<float4*>(xs + b * K + k) = v;
+                *reinterpret_cast<float4*>(xs + b * KP + xpad<FMT>(k)) = v;
             }
             ss = warp_sum(ss);
             if (lane == 0) ssw[warp * NBG + b] = ss;
@@ -129,7 +130,7 @@ __global__ void __launch_bounds__(THREADS) gemv_kernel(const GemvArgs a) {
         if (a.xn_out && blockIdx.x == 0) {
             for (int i = tid * 4; i < nb * K; i += THREADS * 4) {
                 int b = i / K, k = i % K;
-                float4 v = *reinterpret_cast<const float4*>(xs + i);
+                float4 v = *reinterpret_cast<const float4*>(xs + b * KP + xpad<FMT>(k));
                 float s = inv[0];
 #pragma unroll
                 for (int bb = 1; bb < NBG; ++bb)
@@ -141,7 +142,7 @@ __global__ void __launch_bounds__(THREADS) gemv_kernel(const GemvArgs a) {
         if (FMT == FMT_Q4_K) {
             for (int i = tid; i < nb * (K / 16); i += THREADS) {
                 int b = i / (K / 16), j = i % (K / 16);
-                const float4* p = reinterpret_cast<const float4*>(xs + b * K + 16 * j);
+                const float4* p = reinterpret_cast<const float4*>(xs + b * KP + xpad<FMT>(16 * j));
                 float s = 0.f;
 #pragma unroll
                 for (int t = 0; t < 4; ++t) { float4 v = p[t]; s += v.x + v.y + v.z + v.w; }
@@ -174,8 +175,8 @@ __global__ void __launch_bounds__(THREADS) gemv_kernel(const GemvArgs a) {
                 for (int b = 0; b < NBG; ++b) {
                     if (b < nb) {
                         XFrag<FMT> x0, x1;
-                        load_x<FMT>(xs + b * K, u, x0);
-                        load_x<FMT>(xs + b * K, u + 32, x1);
+                        load_x<FMT>(xs + b * KP, u, x0);
+                        load_x<FMT>(xs + b * KP, u + 32, x1);
 #pragma unroll
                         for (int r = 0; r < R; ++r)
                             if (row_ok[r])
@@ -193,7 +194,7 @@ __global__ void __launch_bounds__(THREADS) gemv_kernel(const GemvArgs a) {
                 for (int b = 0; b < NBG; ++b) {
                     if (b < nb) {
                         XFrag<FMT> x0;
-                        load_x<FMT>(xs + b * K, u, x0);
+                        load_x<FMT>(xs + b * KP, u, x0);
 #pragma unroll
                         for (int r = 0; r < R; ++r)
                             if (row_ok[r]) acc[r][b] += dot_frag<FMT>(r0[r], u, x0, xsum16 + b * (K / 16));
@@ -275,7 +276,7 @@ void launch_t(const GemvArgs& a, cudaStream_t s, bool pdl) {
     const int tiles = (rows + rows_per_cta - 1) / rows_per_cta;
     // one wave of resident CTAs; larger matrices loop over tiles inside each CTA
     dim3 grid(a.route ? tiles : std::min(tiles, Occ<FMT, R, NBG>::ctas_per_sm * g_sms), a.route ? a.max_experts : 1);
-    size_t smem = (size_t)NBG * a.W.K * 4 + (FMT == FMT_Q4_K ? (size_t)NBG * (a.W.K / 16) * 4 : 0) +
+    size_t smem = (size_t)NBG * xpad_len<FMT>(a.W.K) * 4 + (FMT == FMT_Q4_K ? (size_t)NBG * (a.W.K / 16) * 4 : 0) +
                   (size_t)(WARPS * R * NBG + WARPS * NBG) * 4;
     auto kern = gemv_kernel<FMT, R, NBG>;
     cudaLaunchConfig_t cfg = {};

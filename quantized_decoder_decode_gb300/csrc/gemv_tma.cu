@@ -56,7 +56,7 @@ struct TLayout {
     static constexpr int QSTAGE = TCfg<FMT>::RT * chunk_bytes<FMT>(TCfg<FMT>::KC);
     static constexpr int SSTAGE = FMT == FMT_Q8_0 ? TCfg<FMT>::RT * (TCfg<FMT>::KC / 16) : 0;
     static size_t bytes(int K) {
-        return (size_t)STAGES * (QSTAGE + SSTAGE) + (size_t)NBG * K * 4 +
+        return (size_t)STAGES * (QSTAGE + SSTAGE) + (size_t)NBG * xpad_len<FMT>(K) * 4 +
                (FMT == FMT_Q4_K ? (size_t)NBG * (K / 16) * 4 : 0) + (size_t)CONSUMER_WARPS * NBG * 4 +
                2 * STAGES * 8 + 64;
     }
@@ -79,8 +79,9 @@ __global__ void __launch_bounds__(THREADS_T) gemv_tma_kernel(const __grid_consta
 
     uint8_t* qbuf = smem;                                                    // [STAGES][RT][chunk bytes]
     uint8_t* sbuf = qbuf + (size_t)STAGES * Lay::QSTAGE;                     // [STAGES][RT][KC/16] (Q8_0)
-    float* xs = reinterpret_cast<float*>(sbuf + (size_t)STAGES * Lay::SSTAGE);   // [NBG][K]
-    float* xsum16 = xs + (size_t)NBG * K;                                    // [NBG][K/16] (Q4_K)
+    const int KP = xpad_len<FMT>(K);                                         // padded row length
+    float* xs = reinterpret_cast<float*>(sbuf + (size_t)STAGES * Lay::SSTAGE);   // [NBG][KP]
+    float* xsum16 = xs + (size_t)NBG * KP;                                   // [NBG][K/16] (Q4_K)
     float* ssw = xsum16 + (FMT == FMT_Q4_K ? (size_t)NBG * (K / 16) : 0);    // [CONSUMER_WARPS][NBG]
     uint64_t* full = reinterpret_cast<uint64_t*>(
         (reinterpret_cast<uintptr_t>(ssw + CONSUMER_WARPS * NBG) + 15) & ~(uintptr_t)15);
@@ -140,7 +141,7 @@ __global__ void __launch_bounds__(THREADS_T) gemv_tma_kernel(const __grid_consta
                 float4 g = *reinterpret_cast<const float4*>(a.norm_g + k);
                 v.x *= g.x; v.y *= g.y; v.z *= g.z; v.w *= g.w;
             }
-            *reinterpret_cast<float4*>(xs + (size_t)b * K + k) = v;
+            *reinterpret_cast<float4*>(xs + (size_t)b * KP + xpad<FMT>(k)) = v;
         }
         ss = warp_sum(ss);
         if (lane == 0) ssw[warp * NBG + b] = ss;
@@ -161,7 +162,7 @@ __global__ void __launch_bounds__(THREADS_T) gemv_tma_kernel(const __grid_consta
 #pragma unroll
             for (int bb = 1; bb < NBG; ++bb)
                 if (bb == b) s = inv[bb];
-            float4 v = *reinterpret_cast<const float4*>(xs + i);
+            float4 v = *reinterpret_cast<const float4*>(xs + (size_t)b * KP + xpad<FMT>(k));
             v.x *= s; v.y *= s; v.z *= s; v.w *= s;
             *reinterpret_cast<float4*>(a.xn_out + (size_t)b * a.xn_stride + k) = v;
         }
@@ -169,7 +170,7 @@ __global__ void __launch_bounds__(THREADS_T) gemv_tma_kernel(const __grid_consta
     if (FMT == FMT_Q4_K) {
         for (int i = tid; i < a.B * (K / 16); i += CONSUMERS) {
             const int b = i / (K / 16), j = i % (K / 16);
-            const float4* p = reinterpret_cast<const float4*>(xs + (size_t)b * K + 16 * j);
+            const float4* p = reinterpret_cast<const float4*>(xs + (size_t)b * KP + xpad<FMT>(16 * j));
             float s = 0.f;
 #pragma unroll
             for (int t = 0; t < 4; ++t) { float4 v = p[t]; s += v.x + v.y + v.z + v.w; }
@@ -226,7 +227,7 @@ __global__ void __launch_bounds__(THREADS_T) gemv_tma_kernel(const __grid_consta
                     for (int b = 0; b < NBG; ++b) {
                         if (b < a.B) {
                             XFrag<FMT> xf;
-                            load_x<FMT>(xs + (size_t)b * K, u, xf);
+                            load_x<FMT>(xs + (size_t)b * KP, u, xf);
 #pragma unroll
                             for (int r = 0; r < C::R; ++r)
                                 acc[r][b] += dot_frag<FMT>(raw[r], u, xf, xsum16 + (size_t)b * (K / 16));

@@ -85,10 +85,22 @@ FQ_DEV Raw load_unit(const QMat& W, int row, int u) {
 // Activations of one unit, loaded from shared memory once and shared by the warp's rows.
 template <int FMT> struct XFrag { float v[Unit<FMT>::ELEMS]; };
 
+// Staged activations carry 4 floats of padding after every 32 (Q8_0) or 64 (Q4_K) elements so
+// that the 16-float runs read by the 8 lanes of one shared-memory phase start in distinct
+// 16-byte bank groups (unpadded they all start at multiples of 256 or 64 bytes).
+template <int FMT>
+FQ_HD constexpr int xpad(int e) {
+    return FMT == FMT_Q8_0 ? e + ((e >> 5) << 2) : FMT == FMT_Q4_K ? e + ((e >> 6) << 2) : e;
+}
+template <int FMT>
+FQ_HD constexpr int xpad_len(int K) {
+    return FMT == FMT_Q8_0 ? K + K / 8 : FMT == FMT_Q4_K ? K + K / 16 : K;
+}
+
 template <int FMT>
 FQ_DEV void load_x(const float* xs, int u, XFrag<FMT>& f) {
     if constexpr (FMT == FMT_Q8_0) {
-        const float4* p = reinterpret_cast<const float4*>(xs + u * 16);
+        const float4* p = reinterpret_cast<const float4*>(xs + xpad<FMT>(u * 16));
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             float4 t = p[i];
@@ -96,8 +108,8 @@ FQ_DEV void load_x(const float* xs, int u, XFrag<FMT>& f) {
         }
     } else if constexpr (FMT == FMT_Q4_K) {
         const int e_lo = (u >> 3) * 256 + 64 * ((u & 7) >> 1) + 16 * (u & 1);
-        const float4* pl = reinterpret_cast<const float4*>(xs + e_lo);
-        const float4* ph = reinterpret_cast<const float4*>(xs + e_lo + 32);
+        const float4* pl = reinterpret_cast<const float4*>(xs + xpad<FMT>(e_lo));
+        const float4* ph = reinterpret_cast<const float4*>(xs + xpad<FMT>(e_lo + 32));
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             float4 t = pl[i], h = ph[i];
@@ -141,9 +153,19 @@ FQ_DEV float dot_frag(const Raw& r, int u, const XFrag<FMT>& x, const float* xsu
             }
         }
         float d = h2f((unsigned short)(r.hdr.x & 0xFFFFu)), dmin = h2f((unsigned short)(r.hdr.x >> 16));
+        // (scale, min) of sub-blocks 2c and 2c+1 straight from the three 32-bit scale words
+        const uint32_t W0 = r.hdr.y, W1 = r.hdr.z, W2 = r.hdr.w;
         uint32_t sc0, mn0, sc1, mn1;
-        q4k_scale_min(r.hdr, 2 * c, sc0, mn0);
-        q4k_scale_min(r.hdr, 2 * c + 1, sc1, mn1);
+        if (c < 2) {
+            const uint32_t sh = 16u * c;
+            sc0 = (W0 >> sh) & 63u; sc1 = (W0 >> (sh + 8)) & 63u;
+            mn0 = (W1 >> sh) & 63u; mn1 = (W1 >> (sh + 8)) & 63u;
+        } else {
+            const uint32_t sh = 16u * (c - 2);
+            const uint32_t a = W2 >> sh, b0 = W0 >> sh, b1 = W1 >> sh;
+            sc0 = (a & 15u) | ((b0 >> 2) & 48u); sc1 = ((a >> 8) & 15u) | ((b0 >> 10) & 48u);
+            mn0 = ((a >> 4) & 15u) | ((b1 >> 2) & 48u); mn1 = ((a >> 12) & 15u) | ((b1 >> 10) & 48u);
+        }
         float d1 = d * (float)sc0, m1 = dmin * (float)mn0, d2 = d * (float)sc1, m2 = dmin * (float)mn1;
         return d1 * slo - m1 * xsum16[e_lo >> 4] + d2 * shi - m2 * xsum16[(e_lo + 32) >> 4];
     } else {
