@@ -37,7 +37,7 @@ constexpr int STAGES = 4;
 template <int FMT> struct TCfg;
 // rows per warp R, rows per tile RT, K elements per chunk KC, unit passes per lane
 template <> struct TCfg<FMT_Q8_0> { static constexpr int R = 4, RT = 32, KC = 512, UPL = 1; };
-template <> struct TCfg<FMT_Q4_K> { static constexpr int R = 2, RT = 16, KC = 2048, UPL = 2; };
+template <> struct TCfg<FMT_Q4_K> { static constexpr int R = 2, RT = 16, KC = 2048, UPL = 1; };
 template <> struct TCfg<FMT_F32> { static constexpr int R = 4, RT = 32, KC = 128, UPL = 1; };
 
 // elements per K chunk in the tensor maps' view of the planes
@@ -68,7 +68,7 @@ struct TmaParams {
 };
 
 template <int FMT, int NBG>
-__global__ void __launch_bounds__(THREADS_T) gemv_tma_kernel(const __grid_constant__ TmaParams prm) {
+__global__ void __launch_bounds__(THREADS_T, 2) gemv_tma_kernel(const __grid_constant__ TmaParams prm) {
     using C = TCfg<FMT>;
     using Lay = TLayout<FMT, NBG>;
     const GemvArgs& a = prm.a;
@@ -216,8 +216,9 @@ __global__ void __launch_bounds__(THREADS_T) gemv_tma_kernel(const __grid_consta
                             raw[r].q = *reinterpret_cast<const uint4*>(srow + 16 * ul);
                             raw[r].sc = sc[(warp * C::R + r) * (C::KC / 32) + (ul >> 1)];
                         } else if constexpr (FMT == FMT_Q4_K) {
-                            const uint8_t* blk = srow + (ul >> 3) * 144;
-                            raw[r].q = *reinterpret_cast<const uint4*>(blk + 16 + 32 * ((ul & 7) >> 1) + 16 * (ul & 1));
+                            const uint8_t* blk = srow + (ul >> 2) * 144;
+                            raw[r].q = *reinterpret_cast<const uint4*>(blk + 16 + 32 * (ul & 3));
+                            raw[r].q2 = *reinterpret_cast<const uint4*>(blk + 32 + 32 * (ul & 3));
                             raw[r].hdr = *reinterpret_cast<const uint4*>(blk);
                         } else {
                             raw[r].q = *reinterpret_cast<const uint4*>(srow + 16 * ul);

@@ -53,14 +53,17 @@ FQ_DEV float dequant_one(const QMat& W, int64_t row, int64_t k) {
 // ---------------------------------------------------------------- GEMV units
 
 // Q8_0 unit: 16 consecutive codes of one row (16 bytes) sharing one fp16 scale.
-// Q4_K unit: 16 bytes of nibbles = 16 elements of sub-block 2c (low) and 16 of 2c+1 (high).
+// Q4_K unit: one 32-byte nibble chunk c of a super-block = all 32 elements of sub-block 2c
+// (low nibbles) and of sub-block 2c+1 (high nibbles), so a lane decodes one (scale, min)
+// pair per 32 weights.
 template <int FMT> struct Unit;
 template <> struct Unit<FMT_Q8_0> { static constexpr int ELEMS = 16; };
-template <> struct Unit<FMT_Q4_K> { static constexpr int ELEMS = 32; };
+template <> struct Unit<FMT_Q4_K> { static constexpr int ELEMS = 64; };
 template <> struct Unit<FMT_F32> { static constexpr int ELEMS = 4; };
 
 struct Raw {
-    uint4 q;        // 16 bytes of codes (Q8_0, Q4_K) or 4 floats (F32)
+    uint4 q;        // 16 bytes of codes (Q8_0; Q4_K first half of the chunk) or 4 floats (F32)
+    uint4 q2;       // Q4_K: second 16 bytes of the chunk
     uint4 hdr;      // Q4_K: d, dmin, 12 scale bytes
     uint16_t sc;    // Q8_0 scale
 };
@@ -72,9 +75,10 @@ FQ_DEV Raw load_unit(const QMat& W, int row, int u) {
         r.q = ld_stream16(W.q + (size_t)row * W.K + (size_t)u * 16);
         r.sc = ld_stream2(W.s + (size_t)row * (W.K / 32) + (u >> 1));
     } else if constexpr (FMT == FMT_Q4_K) {
-        const uint8_t* blk = W.q + (size_t)row * ((size_t)W.K / 256 * 144) + (size_t)(u >> 3) * 144;
-        int c = (u & 7) >> 1, h = u & 1;
-        r.q = ld_stream16(blk + 16 + 32 * c + 16 * h);
+        const uint8_t* blk = W.q + (size_t)row * ((size_t)W.K / 256 * 144) + (size_t)(u >> 2) * 144;
+        const int c = u & 3;
+        r.q = ld_stream16(blk + 16 + 32 * c);
+        r.q2 = ld_stream16(blk + 32 + 32 * c);
         r.hdr = ld_stream16(blk);
     } else {
         r.q = ld_stream16((const float*)W.q + (size_t)row * W.K + (size_t)u * 4);
@@ -107,14 +111,12 @@ FQ_DEV void load_x(const float* xs, int u, XFrag<FMT>& f) {
             f.v[4 * i] = t.x; f.v[4 * i + 1] = t.y; f.v[4 * i + 2] = t.z; f.v[4 * i + 3] = t.w;
         }
     } else if constexpr (FMT == FMT_Q4_K) {
-        const int e_lo = (u >> 3) * 256 + 64 * ((u & 7) >> 1) + 16 * (u & 1);
-        const float4* pl = reinterpret_cast<const float4*>(xs + xpad<FMT>(e_lo));
-        const float4* ph = reinterpret_cast<const float4*>(xs + xpad<FMT>(e_lo + 32));
+        const int e0 = (u >> 2) * 256 + 64 * (u & 3);   // 32 low-nibble elements, then 32 high
+        const float4* p = reinterpret_cast<const float4*>(xs + xpad<FMT>(e0));
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            float4 t = pl[i], h = ph[i];
+        for (int i = 0; i < 16; ++i) {
+            float4 t = p[i];
             f.v[4 * i] = t.x; f.v[4 * i + 1] = t.y; f.v[4 * i + 2] = t.z; f.v[4 * i + 3] = t.w;
-            f.v[16 + 4 * i] = h.x; f.v[16 + 4 * i + 1] = h.y; f.v[16 + 4 * i + 2] = h.z; f.v[16 + 4 * i + 3] = h.w;
         }
     } else {
         float4 t = reinterpret_cast<const float4*>(xs)[u];
@@ -137,21 +139,25 @@ FQ_DEV float dot_frag(const Raw& r, int u, const XFrag<FMT>& x, const float* xsu
         for (int i = 0; i < 16; ++i) acc = fmaf(f[i], x.v[i], acc);
         return h2f(r.sc) * acc;
     } else if constexpr (FMT == FMT_Q4_K) {
-        const int c = (u & 7) >> 1;
-        const int e_lo = (u >> 3) * 256 + 64 * c + 16 * (u & 1);
-        uint32_t w[4] = {r.q.x, r.q.y, r.q.z, r.q.w};
-        float slo = 0.f, shi = 0.f;
+        const int c = u & 3;
+        const int e0 = (u >> 2) * 256 + 64 * c;
+        const uint32_t w[8] = {r.q.x, r.q.y, r.q.z, r.q.w, r.q2.x, r.q2.y, r.q2.z, r.q2.w};
+        float slo = 0.f, shi = 0.f, slo2 = 0.f, shi2 = 0.f;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
+        for (int i = 0; i < 8; ++i) {
             float lo[4], hi[4];
             u8x4_to_f32(w[i] & 0x0F0F0F0Fu, lo);
             u8x4_to_f32((w[i] >> 4) & 0x0F0F0F0Fu, hi);
+            float& al = (i & 1) ? slo2 : slo;
+            float& ah = (i & 1) ? shi2 : shi;
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                slo = fmaf(lo[j], x.v[4 * i + j], slo);
-                shi = fmaf(hi[j], x.v[16 + 4 * i + j], shi);
+                al = fmaf(lo[j], x.v[4 * i + j], al);
+                ah = fmaf(hi[j], x.v[32 + 4 * i + j], ah);
             }
         }
+        slo += slo2;
+        shi += shi2;
         float d = h2f((unsigned short)(r.hdr.x & 0xFFFFu)), dmin = h2f((unsigned short)(r.hdr.x >> 16));
         // (scale, min) of sub-blocks 2c and 2c+1 straight from the three 32-bit scale words
         const uint32_t W0 = r.hdr.y, W1 = r.hdr.z, W2 = r.hdr.w;
@@ -167,7 +173,10 @@ FQ_DEV float dot_frag(const Raw& r, int u, const XFrag<FMT>& x, const float* xsu
             mn0 = ((a >> 4) & 15u) | ((b1 >> 2) & 48u); mn1 = ((a >> 12) & 15u) | ((b1 >> 10) & 48u);
         }
         float d1 = d * (float)sc0, m1 = dmin * (float)mn0, d2 = d * (float)sc1, m2 = dmin * (float)mn1;
-        return d1 * slo - m1 * xsum16[e_lo >> 4] + d2 * shi - m2 * xsum16[(e_lo + 32) >> 4];
+        // xsum16 holds per-16 sums; sub-blocks 2c and 2c+1 span two entries each
+        const float s_lo = xsum16[e0 >> 4] + xsum16[(e0 >> 4) + 1];
+        const float s_hi = xsum16[(e0 >> 4) + 2] + xsum16[(e0 >> 4) + 3];
+        return d1 * slo - m1 * s_lo + d2 * shi - m2 * s_hi;
     } else {
         return __uint_as_float(r.q.x) * x.v[0] + __uint_as_float(r.q.y) * x.v[1] + __uint_as_float(r.q.z) * x.v[2] +
                __uint_as_float(r.q.w) * x.v[3];
