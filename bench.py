@@ -119,16 +119,19 @@ class ClockSampler:
         return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def dist_setup(n_gpus: int):
+def dist_setup(n_gpus: int, backend: str = "nccl"):
+    """One process per GPU (torchrun env).  Replicas only: the process group carries the
+    start/stop barriers and the max-over-ranks timing, never the data path."""
     import torch
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if world > 1:
         import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl")
-    else:
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    elif backend == "nccl":
         torch.cuda.set_device(0)
     return rank, world, local
 
@@ -139,14 +142,30 @@ def barrier(world: int):
         dist.barrier()
 
 
-def max_over_ranks(v: float, world: int) -> float:
+def _reduce(v: float, world: int, op: str) -> float:
     if world == 1:
         return v
     import torch
     import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX if op == "max" else dist.ReduceOp.SUM)
     return float(t.item())
+
+
+def max_over_ranks(v: float, world: int) -> float:
+    return _reduce(v, world, "max")
+
+
+def sum_over_ranks(v: float, world: int) -> float:
+    return _reduce(v, world, "sum")
+
+
+def aggregate(units: float, seconds: float, world: int) -> tuple:
+    """Whole-job throughput: units processed by all ranks / the slowest rank's time."""
+    total = sum_over_ranks(units, world)
+    dt = max_over_ranks(seconds, world)
+    return total / dt, dt
 
 
 # ---------------------------------------------------------------- CPU oracle (reference arm / baseline)
@@ -336,8 +355,8 @@ def run_fq(args):
         torch.cuda.nvtx.range_pop()
         torch.cuda.synchronize()
         barrier(world)
-    dt = max_over_ranks(ev0.elapsed_time(ev1) / 1e3, world)
-    value = world * n * args.steps / dt
+    value, dt = aggregate(n * args.steps, ev0.elapsed_time(ev1) / 1e3, world)
+    kernels_per_step = fq.fq_step_kernels(model, stream)
 
     # ---- end to end through the public API with host buffers: per step the tokens go in
     # from pinned host memory (by value through the call) and the chosen tokens come back
@@ -359,8 +378,7 @@ def run_fq(args):
             cur = host_tok.tolist()
         done += s_
     rewind()
-    e2e_dt = max_over_ranks(time.perf_counter() - t0, world)
-    e2e_value = world * n * e2e_steps / e2e_dt
+    e2e_value, e2e_dt = aggregate(n * e2e_steps, time.perf_counter() - t0, world)
 
     # ---- experts touched per layer (MoE): from one traced step
     experts = None
@@ -397,8 +415,8 @@ def run_fq(args):
     kv_write = n * 2 * d.num_layers * d.kv_dim * 2
     total = wb["layers"] + wb["lm_head"] + wb["embedding_rows"] + kv_read + kv_write
     step_gbs = total / (dt / args.steps) / 1e9
-    per_layer = 5 if not d.is_moe else 8
-    launches_per_step = 1 + d.num_layers * per_layer + 2
+    # kernels inside the timed region: each step replays one captured graph; each chain adds
+    # the one state-setup launch made before its replays
     n_chains = (args.steps + chain - 1) // chain
 
     if rank == 0:
@@ -412,7 +430,8 @@ def run_fq(args):
             "config": config_dict(w),
             "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": 4 * n,
                     "d2h_bytes_per_step": 4 * n, "steps": e2e_steps},
-            "gpu_launches": args.steps * launches_per_step + n_chains,
+            "gpu_launches": args.steps * kernels_per_step + n_chains,
+            "kernels_per_step": kernels_per_step,
             "roofline": {"bound": "hbm", "kernel": f"dequant GEMV ({w.weight_dtype}), LM head launch "
                                                    f"{d.vocab_size}x{d.hidden_size}",
                          "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
@@ -438,8 +457,9 @@ def run_fq(args):
 
 
 def run_kernel(args):
-    """Kernel-level timing for profiling: the LM-head GEMV alone (--kernel lm_head) or one
-    decoder layer step at the workload's context (--kernel layer), `--steps` launches after
+    """Kernel-level timing for profiling: the LM-head GEMV alone (--kernel lm_head), one
+    decoder layer step at the workload's context (--kernel layer), or the layer's dense
+    projections at the workload's batch (--kernel proj), `--steps` repetitions after
     `--warmup`, on one layer of the chosen workload's weights."""
     import dataclasses
     import torch
@@ -463,11 +483,26 @@ def run_kernel(args):
     model = fq.fq_load_weights(desc, src, stream)
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     bpw = 34 / 32 if w.weight_dtype == "q8_0" else 144 / 256
+    flops = None
     if args.kernel == "lm_head":
         x = torch.randn(d.hidden_size, device=dev)
         y = torch.empty(d.vocab_size, device=dev)
         call = lambda: fq.fq_gemv(model, 0, fq.W_OUTPUT, 1, x.data_ptr(), y.data_ptr(), stream)  # noqa: E731
         nbytes = d.vocab_size * d.hidden_size * bpw
+    elif args.kernel == "proj":
+        # every dense projection of one layer at the workload's batch (tensor-core GEMM for
+        # batches of 8 or more); bytes = weights once + activations in and out
+        n = w.batch
+        mats = [(fq.W_Q, d.q_dim + 2 * d.kv_dim, d.hidden_size), (fq.W_O, d.hidden_size, d.q_dim)]
+        if not d.is_moe:
+            mats += [(fq.W_GATE, 2 * d.intermediate_size, d.hidden_size),
+                     (fq.W_DOWN, d.hidden_size, d.intermediate_size)]
+        bufs = [(wh, torch.randn(n, cols, device=dev), torch.empty(n, rows, device=dev)) for wh, rows, cols in mats]
+        def call():
+            for wh, xb, yb in bufs:
+                fq.fq_gemv(model, 0, wh, n, xb.data_ptr(), yb.data_ptr(), stream)
+        nbytes = sum(r * c * bpw + 4 * n * (r + c) for _, r, c in mats)
+        flops = 2 * n * sum(r * c for _, r, c in mats)
     else:
         kv = fq.fq_kv_init(model, ctx + 1, "bf16")
         k, v = wl.make_kv_prior(w1, 0, 0, ctx)
@@ -492,19 +527,15 @@ def run_kernel(args):
     peak, kind = measured_peaks()
     print(json.dumps({"kernel": args.kernel, "workload": w.name, "launches": len(t), "us_mean": mean * 1e6,
                       "us_min": min(t) * 1e6, "bytes": nbytes, "gbs": nbytes / mean / 1e9,
-                      "frac": nbytes / mean / 1e9 / peak, "peak": peak, "peak_kind": kind}))
+                      "frac": nbytes / mean / 1e9 / peak, "peak": peak, "peak_kind": kind,
+                      "tflops": (flops / mean / 1e12) if flops else None}))
     fq.fq_model_free(model)
     return 0
 
 
-def dataclasses_replace_layers(d):
-    import dataclasses
-    return dataclasses.replace(d, num_layers=1)
-
-
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("--kernel", choices=["lm_head", "layer"], default=None,
+    ap.add_argument("--kernel", choices=["lm_head", "layer", "proj"], default=None,
                     help="time one kernel family instead of the decode loop (profiling)")
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--workload", default=WORKLOAD,

@@ -221,11 +221,17 @@ fq_status fq_gemv(const fq_model* m, uint32_t layer, fq_weight_id which, uint32_
  * 2 MiB array built into the library, which every GPU that loads the library holds until
  * the process exits.  A model + cache capacity whose layer scratch does not fit is rejected
  * with FQ_ERR_INVALID_ARGUMENT and a message giving the size (a 0.6B- or 8B-shaped dense layer
- * fits at any capacity up to 16K positions).  The first call on a device looks up the
+ * fits at any capacity up to 40960 positions).  The first call on a device looks up the
  * array's device address (once, with that device current), so make that first call before
  * any stream capture.  Every call shares the array: calls whose GPU work overlaps (other
  * streams, other threads) race and give wrong results; serialise them. */
 fq_status fq_layer_step_noalloc(const fq_model* m, uint32_t layer, fq_kv* kv, uint32_t pos, float* x, void* stream);
+
+/* Number of kernels one step launches: the kernel nodes of the CUDA graph most recently
+ * replayed by fq_decode_step / fq_decode_step_batch / fq_decode_greedy on `stream` (0 when
+ * no step has been replayed there, or the steps ran without a graph).  Host-only; for
+ * accounting by benchmarks. */
+fq_status fq_step_kernels(const fq_model* m, void* stream, uint32_t* kernels);
 
 /* Synchronise `stream` and report device-side failures recorded since the last check:
  * FQ_ERR_DEVICE_TIMEOUT when a kernel's bounded wait on its own copy pipeline gave up

@@ -102,6 +102,8 @@ struct Workspace {
     float *x = nullptr, *qkv = nullptr, *attn = nullptr, *h = nullptr, *part = nullptr, *logits = nullptr;
     float *xn = nullptr, *rlogits = nullptr, *he = nullptr, *ye = nullptr;
     void* xh = nullptr;        // f16 hi/lo activations for the tensor-core GEMM (batches >= 8)
+    float* tc_part = nullptr;  // its split-K partial sums
+    uint32_t* tc_tickets = nullptr;
     uint32_t* counters = nullptr;
     MoeRoute* route = nullptr;
     std::vector<void*> allocs;
@@ -109,8 +111,10 @@ struct Workspace {
         int mode, n, chunk, splits, kv_bf16;
         float* logits;
         cudaGraphExec_t exec;
+        uint32_t kernels;      // kernel nodes in the captured step
     };
     std::vector<Graph> graphs;
+    uint32_t last_kernels = 0; // kernels of the step most recently replayed on this stream
     void drop_graphs() {
         for (auto& g : graphs) cudaGraphExecDestroy(g.exec);
         graphs.clear();
@@ -197,6 +201,9 @@ fq_status ensure_ws(const fq_model* mc, cudaStream_t stream, int n, uint32_t cap
             uint16_t* xh;
             TRY(dalloc(A, &xh, gemm_tc_xh_elems(kmax)));
             w->xh = xh;
+            TRY(dalloc(A, &w->tc_part, TC_PART_FLOATS));
+            TRY(dalloc(A, &w->tc_tickets, (size_t)TC_TICKETS));
+            CK(cudaMemsetAsync(w->tc_tickets, 0, sizeof(uint32_t) * TC_TICKETS, stream));
         }
         CK(cudaMemsetAsync(w->st, 0, sizeof(StepState), stream));
         if (m->moe()) {
@@ -248,7 +255,7 @@ fq_status enqueue_step(const Body& b, cudaStream_t s, int kv_bf16, float* x_over
         g.err = m->err;
         if (!no_tc && w->xh && gemm_tc_applicable(g)) {
             const bool p0 = pdl();
-            launch_gemm_tc(g, w->xh, s, p0, use_pdl);
+            launch_gemm_tc(g, w->xh, w->tc_part, TC_PART_FLOATS, w->tc_tickets, s, p0, use_pdl);
         } else {
             launch_gemv(g, s, pdl());
         }
@@ -371,8 +378,10 @@ fq_status run_body(const Body& b, cudaStream_t s, int kv_bf16, int reps) {
     cudaGraphExec_t exec = nullptr;
     for (auto& g : w->graphs)
         if (g.mode == mode && g.n == b.n && g.chunk == b.chunk && g.splits == b.splits && g.kv_bf16 == kv_bf16 &&
-            g.logits == b.logits)
+            g.logits == b.logits) {
             exec = g.exec;
+            w->last_kernels = g.kernels;
+        }
     if (!exec) {
         cudaStream_t cs;
         CK(cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking));
@@ -387,10 +396,21 @@ fq_status run_body(const Body& b, cudaStream_t s, int kv_bf16, int reps) {
         cudaStreamDestroy(cs);
         if (st != FQ_OK) return st;
         if (e != cudaSuccess) return fail(FQ_ERR_CUDA, "cudaStreamEndCapture: %s", cudaGetErrorString(e));
+        uint32_t kernels = 0;
+        size_t n_nodes = 0;
+        if (cudaGraphGetNodes(graph, nullptr, &n_nodes) == cudaSuccess && n_nodes) {
+            std::vector<cudaGraphNode_t> nodes(n_nodes);
+            if (cudaGraphGetNodes(graph, nodes.data(), &n_nodes) == cudaSuccess)
+                for (auto nd : nodes) {
+                    cudaGraphNodeType t;
+                    if (cudaGraphNodeGetType(nd, &t) == cudaSuccess && t == cudaGraphNodeTypeKernel) ++kernels;
+                }
+        }
         e = cudaGraphInstantiate(&exec, graph, 0);
         cudaGraphDestroy(graph);
         if (e != cudaSuccess) return fail(FQ_ERR_CUDA, "cudaGraphInstantiate: %s", cudaGetErrorString(e));
-        w->graphs.push_back({mode, b.n, b.chunk, b.splits, kv_bf16, b.logits, exec});
+        w->graphs.push_back({mode, b.n, b.chunk, b.splits, kv_bf16, b.logits, exec, kernels});
+        w->last_kernels = kernels;
     }
     for (int r = 0; r < reps; ++r) CK(cudaGraphLaunch(exec, s));
     return FQ_OK;
@@ -922,9 +942,18 @@ fq_status fq_gemv(const fq_model* m, uint32_t layer, fq_weight_id which, uint32_
     cudaStream_t s = (cudaStream_t)stream;
     Workspace* w = nullptr;
     if (n >= (uint32_t)TC_MIN_BATCH) TRY(ensure_ws(m, s, (int)n, 1, &w));
-    if (w && w->xh && gemm_tc_applicable(g) && !env_flag("FQ_NO_TC")) launch_gemm_tc(g, w->xh, s, false, false);
+    if (w && w->xh && gemm_tc_applicable(g) && !env_flag("FQ_NO_TC"))
+        launch_gemm_tc(g, w->xh, w->tc_part, TC_PART_FLOATS, w->tc_tickets, s, false, false);
     else launch_gemv(g, s, false);
     CK(cudaGetLastError());
+    return FQ_OK;
+}
+
+fq_status fq_step_kernels(const fq_model* m, void* stream, uint32_t* kernels) {
+    if (!m || !kernels) return fail(FQ_ERR_INVALID_ARGUMENT, "null argument");
+    std::lock_guard<std::mutex> lk(const_cast<fq_model*>(m)->ws_mu);
+    auto it = m->ws.find((cudaStream_t)stream);
+    *kernels = it == m->ws.end() ? 0u : it->second->last_kernels;
     return FQ_OK;
 }
 

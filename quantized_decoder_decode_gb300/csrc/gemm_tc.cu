@@ -20,6 +20,10 @@
 //              accumulator to the epilogue;
 //   warps 4-7  epilogue: tcgen05.ld of the 128 x N accumulator (one row per thread), hi+lo,
 //              then store / residual add / SwiGLU (gate, up rows adjacent) / logits+argmax.
+// Work is split into (row tile, K slice) units so that narrow matrices still cover every
+// SM: with several K slices each unit writes its partial sums to scratch and the last unit
+// of a tile to finish (atomic ticket, no waiting) adds them up and applies the epilogue.
+// Converter threads keep two chunks of codes in flight ahead of the one they decode.
 // Every mbarrier wait is bounded; a stuck pipeline sets the error word and unwinds.
 
 #include <cuda_fp16.h>
@@ -52,10 +56,13 @@ struct TcArgs {
     int epi;
     StepState* st;
     uint32_t* err;
+    int ks;              // K slices per tile (divides K / 64)
+    float* part;         // [ks][B][N] partial sums (ks > 1)
+    uint32_t* tickets;   // [4 * tiles] arrival counters per (tile, epilogue warp), zero between uses
 };
 
 template <int BP>
-__global__ void __launch_bounds__(TC_THREADS) gemm_tc_kernel(const TcArgs a) {
+__global__ void __launch_bounds__(TC_THREADS, 2) gemm_tc_kernel(const TcArgs a) {
     constexpr int NCOL = 2 * BP;         // MMA N
     extern __shared__ __align__(1024) uint8_t smem[];
     uint8_t* As = smem;
@@ -71,7 +78,9 @@ __global__ void __launch_bounds__(TC_THREADS) gemm_tc_kernel(const TcArgs a) {
     const int N = W.N, K = W.K;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int n_tiles = (N + TM - 1) / TM, n_chunks = K / KCH;
-    const int my_tiles = (int)blockIdx.x < n_tiles ? (n_tiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+    const int KS = a.ks, cpk = n_chunks / KS;            // K slices per tile, chunks per slice
+    const int n_units = n_tiles * KS;
+    const int my_units = (int)blockIdx.x < n_units ? (n_units - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
 
     if (tid == 0) {
         for (int s = 0; s < TSTAGES; ++s) {
@@ -94,33 +103,46 @@ __global__ void __launch_bounds__(TC_THREADS) gemm_tc_kernel(const TcArgs a) {
     pdl_wait();
 
     if (warp < CONV_WARPS) {
-        // ---------------- converters: one weight row per thread
+        // ---------------- converters: one weight row per thread, two chunks of codes in flight
         const int r = tid;
-        for (int it = 0; it < my_tiles * n_chunks; ++it) {
-            const int tile = blockIdx.x + (it / n_chunks) * gridDim.x, chunk = it % n_chunks;
-            const int stage = it % TSTAGES;
-            const uint32_t ph = (uint32_t)(it / TSTAGES) & 1u;
-            const int row = tile * TM + r;
+        const int n_iters = my_units * cpk;
+        struct Codes {
             uint4 c[4];
-            uint32_t sc2 = 0;
-            if (row < N) {
+            uint32_t sc2;
+        };
+        auto fetch = [&](int it, Codes& cd) {
+            const int unit = blockIdx.x + (it / cpk) * gridDim.x;
+            const int tile = unit / KS, chunk = (unit % KS) * cpk + it % cpk;
+            const int row = tile * TM + r;
+            if (it < n_iters && row < N) {
                 const uint8_t* src = W.q + (size_t)row * K + (size_t)chunk * KCH;
 #pragma unroll
-                for (int i = 0; i < 4; ++i) c[i] = ld_stream16(src + 16 * i);
-                sc2 = ld_stream4(W.s + (size_t)row * (K / 32) + (size_t)chunk * 2);
+                for (int i = 0; i < 4; ++i) cd.c[i] = ld_stream16(src + 16 * i);
+                cd.sc2 = ld_stream4(W.s + (size_t)row * (K / 32) + (size_t)chunk * 2);
             } else {
 #pragma unroll
-                for (int i = 0; i < 4; ++i) c[i] = make_uint4(0u, 0u, 0u, 0u);
+                for (int i = 0; i < 4; ++i) cd.c[i] = make_uint4(0u, 0u, 0u, 0u);
+                cd.sc2 = 0u;
             }
+        };
+        Codes c0, c1, c2;
+        fetch(0, c0);
+        fetch(1, c1);
+        for (int it = 0; it < n_iters; ++it) {
+            fetch(it + 2, c2);
+            const int unit = blockIdx.x + (it / cpk) * gridDim.x;
+            const int chunk = (unit % KS) * cpk + it % cpk;
+            const int stage = it % TSTAGES;
+            const uint32_t ph = (uint32_t)(it / TSTAGES) & 1u;
             if (!mbar_wait(&freeb[stage], ph ^ 1u)) {
                 if (a.err && lane == 0) atomicOr(a.err, 4u);
                 break;
             }
             uint8_t* Ast = As + (size_t)stage * A_STAGE;
-            const float d0 = h2f((unsigned short)(sc2 & 0xFFFFu)), d1 = h2f((unsigned short)(sc2 >> 16));
+            const float d0 = h2f((unsigned short)(c0.sc2 & 0xFFFFu)), d1 = h2f((unsigned short)(c0.sc2 >> 16));
 #pragma unroll
             for (int j = 0; j < 8; ++j) {          // 16-byte chunk j = K elements 8j..8j+7
-                const uint4 w4 = c[j >> 1];
+                const uint4 w4 = c0.c[j >> 1];
                 const uint32_t w0 = (j & 1) ? w4.z : w4.x, w1 = (j & 1) ? w4.w : w4.y;
                 float f[8];
                 s8x4_to_f32(w0, f);
@@ -140,6 +162,8 @@ __global__ void __launch_bounds__(TC_THREADS) gemm_tc_kernel(const TcArgs a) {
             fence_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(&full[stage]);
+            c0 = c1;
+            c1 = c2;
         }
     } else if (warp == MMA_WARP) {
         // ---------------- MMA issue: one thread
@@ -147,7 +171,7 @@ __global__ void __launch_bounds__(TC_THREADS) gemm_tc_kernel(const TcArgs a) {
             const uint32_t idesc = idesc_f16_f32(TM, NCOL);
             int it = 0;
             bool ok = true;
-            for (int t = 0; t < my_tiles && ok; ++t) {
+            for (int t = 0; t < my_units && ok; ++t) {
                 if (t > 0) {
                     if (!mbar_wait(acc_free, (uint32_t)(t - 1) & 1u)) {
                         if (a.err) atomicOr(a.err, 8u);
@@ -155,7 +179,7 @@ __global__ void __launch_bounds__(TC_THREADS) gemm_tc_kernel(const TcArgs a) {
                     }
                     tc_fence_after();
                 }
-                for (int chunk = 0; chunk < n_chunks; ++chunk, ++it) {
+                for (int chunk = 0; chunk < cpk; ++chunk, ++it) {
                     const int stage = it % TSTAGES;
                     const uint32_t ph = (uint32_t)(it / TSTAGES) & 1u;
                     if (!mbar_wait(&full[stage], ph)) {
@@ -179,7 +203,7 @@ __global__ void __launch_bounds__(TC_THREADS) gemm_tc_kernel(const TcArgs a) {
         // ---------------- epilogue: TMEM lanes 32q..32q+31 <-> tile rows
         const int q = warp - EPI_WARP0;
         const int rin = 32 * q + lane;
-        for (int t = 0; t < my_tiles; ++t) {
+        for (int t = 0; t < my_units; ++t) {
             if (!mbar_wait(acc_full, (uint32_t)t & 1u)) {
                 if (a.err && lane == 0) atomicOr(a.err, 32u);
                 break;
@@ -192,23 +216,51 @@ __global__ void __launch_bounds__(TC_THREADS) gemm_tc_kernel(const TcArgs a) {
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(acc_free);
-            const int tile = blockIdx.x + t * gridDim.x;
+            const int unit = blockIdx.x + t * gridDim.x;
+            const int tile = unit / KS, ksl = unit % KS;
             const int row = tile * TM + rin;
             const bool ok_row = row < N;
+            float val[BP];
+#pragma unroll
+            for (int b = 0; b < BP; ++b) val[b] = __uint_as_float(v[b]) + __uint_as_float(v[BP + b]);
+            if (KS > 1) {
+                // partial of this K slice -> scratch; the tile's last slice adds them up
+                if (ok_row)
+#pragma unroll
+                    for (int b = 0; b < BP; ++b)
+                        if (b < a.B) a.part[((size_t)ksl * a.B + b) * N + row] = val[b];
+                // each epilogue warp owns 32 rows of the tile and its own ticket
+                __threadfence();
+                __syncwarp();
+                uint32_t prev = 0u;
+                if (lane == 0) {
+                    prev = atomicAdd(&a.tickets[4 * tile + q], 1u);
+                    if (prev == (uint32_t)(KS - 1)) a.tickets[4 * tile + q] = 0u;
+                }
+                prev = __shfl_sync(0xFFFFFFFFu, prev, 0);
+                if (prev != (uint32_t)(KS - 1)) continue;
+                __threadfence();
+#pragma unroll
+                for (int b = 0; b < BP; ++b) {
+                    float acc = 0.f;
+                    if (b < a.B && ok_row)
+                        for (int k2 = 0; k2 < KS; ++k2) acc += __ldcg(&a.part[((size_t)k2 * a.B + b) * N + row]);
+                    val[b] = acc;
+                }
+            }
             unsigned long long kb[BP];
 #pragma unroll
             for (int b = 0; b < BP; ++b) {
-                const float val = __uint_as_float(v[b]) + __uint_as_float(v[BP + b]);
                 kb[b] = 0ull;
                 if (a.epi == EPI_SWIGLU) {
-                    const float up = __shfl_xor_sync(0xFFFFFFFFu, val, 1);
+                    const float up = __shfl_xor_sync(0xFFFFFFFFu, val[b], 1);
                     if (b < a.B && ok_row && (rin & 1) == 0 && row + 1 < N)
-                        a.y[(size_t)b * a.y_stride + (row >> 1)] = silu(val) * up;
+                        a.y[(size_t)b * a.y_stride + (row >> 1)] = silu(val[b]) * up;
                 } else if (b < a.B && ok_row) {
                     float* yp = a.y + (size_t)b * a.y_stride + row;
-                    if (a.epi == EPI_ADD) *yp += val;
-                    else *yp = val;
-                    if (a.epi == EPI_LOGITS) kb[b] = argmax_key(val, (uint32_t)row);
+                    if (a.epi == EPI_ADD) *yp += val[b];
+                    else *yp = val[b];
+                    if (a.epi == EPI_LOGITS) kb[b] = argmax_key(val[b], (uint32_t)row);
                 }
             }
             if (a.epi == EPI_LOGITS) {
@@ -272,7 +324,7 @@ template <int BP>
 void launch_bp(const TcArgs& t, cudaStream_t s, bool pdl) {
     const int tiles = (t.W.N + TM - 1) / TM;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(std::min(tiles, 2 * g_sms_tc));
+    cfg.gridDim = dim3(std::min(tiles * t.ks, 2 * g_sms_tc));
     cfg.blockDim = dim3(TC_THREADS);
     cfg.dynamicSmemBytes = TC_SMEM;
     cfg.stream = s;
@@ -302,7 +354,8 @@ bool gemm_tc_applicable(const GemvArgs& a) {
 
 size_t gemm_tc_xh_elems(int K) { return (size_t)64 * K; }
 
-void launch_gemm_tc(const GemvArgs& a, void* xh_v, cudaStream_t s, bool pdl_prep, bool pdl) {
+void launch_gemm_tc(const GemvArgs& a, void* xh_v, float* part, size_t part_cap, uint32_t* tickets, cudaStream_t s,
+                    bool pdl_prep, bool pdl) {
     __half* xh = static_cast<__half*>(xh_v);
     const int BP = a.B <= 8 ? 8 : a.B <= 16 ? 16 : 32;
     cudaLaunchConfig_t cfg = {};
@@ -324,6 +377,15 @@ void launch_gemm_tc(const GemvArgs& a, void* xh_v, cudaStream_t s, bool pdl_prep
     t.epi = a.epi;
     t.st = a.st;
     t.err = a.err;
+    // K slices: enough (row tile, K slice) units for two CTAs per SM, at least 4 chunks each
+    const int tiles = (a.W.N + TM - 1) / TM, n_chunks = a.W.K / KCH;
+    int ks = 1;
+    while (tiles * ks < 2 * g_sms_tc && n_chunks % (2 * ks) == 0 && n_chunks / (2 * ks) >= 4 &&
+           (size_t)(2 * ks) * a.B * a.W.N <= part_cap && 4 * tiles <= TC_TICKETS)
+        ks *= 2;
+    t.ks = ks;
+    t.part = part;
+    t.tickets = tickets;
     if (BP == 8) launch_bp<8>(t, s, pdl);
     else if (BP == 16) launch_bp<16>(t, s, pdl);
     else launch_bp<32>(t, s, pdl);

@@ -112,7 +112,11 @@ constexpr int TC_MIN_BATCH = 8;
 void gemm_tc_prepare();
 bool gemm_tc_applicable(const GemvArgs& a);
 size_t gemm_tc_xh_elems(int K);
-void launch_gemm_tc(const GemvArgs& a, void* xh, cudaStream_t s, bool pdl_prep, bool pdl);
+// part: split-K scratch of part_cap floats; tickets: TC_TICKETS zeroed counters
+void launch_gemm_tc(const GemvArgs& a, void* xh, float* part, size_t part_cap, uint32_t* tickets, cudaStream_t s,
+                    bool pdl_prep, bool pdl);
+constexpr size_t TC_PART_FLOATS = (size_t)4 << 20;
+constexpr int TC_TICKETS = 8192;
 
 // Attention with fused QK-norm + rope + KV append (one query row per sequence).
 struct AttnArgs {

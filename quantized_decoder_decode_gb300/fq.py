@@ -89,6 +89,7 @@ def lib():
                 "fq_layer_step_trace": [vp, u32, vp, u32, vp, vp, vp, vp, vp],
                 "fq_gemv": [vp, u32, ctypes.c_int, u32, vp, vp, vp],
                 "fq_check_device": [vp, vp],
+                "fq_step_kernels": [vp, vp, ctypes.POINTER(ctypes.c_uint32)],
                 "fq_layer_step_noalloc": [vp, u32, vp, u32, vp, vp],
             }
             for name, args in sig.items():
@@ -114,7 +115,7 @@ def lib():
 EXPORTED = ("fq_desc_init", "fq_load_weights", "fq_model_free", "fq_kv_init", "fq_kv_free", "fq_kv_len",
             "fq_kv_capacity", "fq_kv_append", "fq_kv_commit", "fq_kv_rewind", "fq_kv_read", "fq_layer_step", "fq_decode_step",
             "fq_decode_step_batch", "fq_decode_greedy", "fq_decode_step_trace", "fq_dequant_rows", "fq_layer_step_trace",
-            "fq_gemv", "fq_check_device", "fq_layer_step_noalloc", "fq_last_error",
+            "fq_gemv", "fq_step_kernels", "fq_check_device", "fq_layer_step_noalloc", "fq_last_error",
             "fq_status_str")
 
 
@@ -270,6 +271,13 @@ def fq_layer_step_trace(model: int, layer: int, kv: int, pos: int, x_ptr: int, q
 
 def fq_gemv(model: int, layer: int, which: int, n: int, x_ptr: int, y_ptr: int, stream: int = 0) -> None:
     _check(lib().fq_gemv(model, layer, which, n, x_ptr, y_ptr, stream), "fq_gemv")
+
+
+def fq_step_kernels(model: int, stream: int = 0) -> int:
+    """Kernels per step of the CUDA graph last replayed on `stream` (0 if none)."""
+    out = ctypes.c_uint32(0)
+    _check(lib().fq_step_kernels(model, stream, ctypes.byref(out)), "fq_step_kernels")
+    return int(out.value)
 
 
 def fq_check_device(model: int, stream: int = 0) -> None:
