@@ -227,10 +227,11 @@ fq_status fq_gemv(const fq_model* m, uint32_t layer, fq_weight_id which, uint32_
  * streams, other threads) race and give wrong results; serialise them. */
 fq_status fq_layer_step_noalloc(const fq_model* m, uint32_t layer, fq_kv* kv, uint32_t pos, float* x, void* stream);
 
-/* Number of kernels one step launches: the kernel nodes of the CUDA graph most recently
- * replayed by fq_decode_step / fq_decode_step_batch / fq_decode_greedy on `stream` (0 when
- * no step has been replayed there, or the steps ran without a graph).  Host-only; for
- * accounting by benchmarks. */
+/* Number of kernels one step launches on `stream`: the kernel nodes of the CUDA graph most
+ * recently replayed there by fq_decode_step / fq_decode_step_batch / fq_decode_greedy, or 1
+ * when the step ran as the single persistent kernel (batch 1, dense model); 0 when nothing
+ * has run there or the steps ran as direct launches.  Host-only; for accounting by
+ * benchmarks. */
 fq_status fq_step_kernels(const fq_model* m, void* stream, uint32_t* kernels);
 
 /* Synchronise `stream` and report device-side failures recorded since the last check:

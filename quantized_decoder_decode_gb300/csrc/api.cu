@@ -78,6 +78,7 @@ struct fq_model {
     int max_pos = 0;
     uint32_t* err = nullptr;       // device error word (bounded waits that gave up)
     std::deque<TmaMaps> tmaps;     // tensor maps of the dense weights (stable addresses)
+    PersistLayer* players = nullptr;   // device copy of the layer table for the persistent step
     std::vector<void*> allocs;
     std::mutex ws_mu;
     std::map<cudaStream_t, Workspace*> ws;
@@ -105,6 +106,7 @@ struct Workspace {
     float* tc_part = nullptr;  // its split-K partial sums
     uint32_t* tc_tickets = nullptr;
     uint32_t* counters = nullptr;
+    uint32_t* pbar = nullptr;  // persistent step: grid barrier [2] + LM-head ticket
     MoeRoute* route = nullptr;
     std::vector<void*> allocs;
     struct Graph {
@@ -194,7 +196,9 @@ fq_status ensure_ws(const fq_model* mc, cudaStream_t stream, int n, uint32_t cap
         TRY(dalloc(A, &w->part, pc));
         TRY(dalloc(A, &w->counters, (size_t)nn * p.num_key_value_heads));
         TRY(dalloc(A, &w->logits, (size_t)nn * p.vocab_size));
+        TRY(dalloc(A, &w->pbar, 4));
         CK(cudaMemsetAsync(w->counters, 0, sizeof(uint32_t) * nn * p.num_key_value_heads, stream));
+        CK(cudaMemsetAsync(w->pbar, 0, sizeof(uint32_t) * 4, stream));
         if (nn >= TC_MIN_BATCH) {
             const int kmax = (int)std::max<size_t>({H, (size_t)p.num_attention_heads * HEAD_DIM,
                                                      (size_t)std::max<uint32_t>(p.intermediate_size, 1)});
@@ -237,6 +241,14 @@ struct Body {
     float* route_w = nullptr;
 };
 
+// Batch 1 of a dense model can run as one persistent kernel (FQ_PERSIST=1).  Off by default:
+// measured on GB300 its grid barriers (about 2.4 us each, 5 per layer) cost more than the
+// launches of the captured kernel sequence they replace.
+bool persist_eligible(const Body& b) {
+    static const bool persist = env_flag("FQ_PERSIST");
+    return b.n == 1 && !b.m->moe() && b.m->players && !b.layer_out && !b.route_idx && persist;
+}
+
 // The kernels of one decode step, in order.  The first launch follows the set-up kernel
 // with ordinary stream order; every later one uses programmatic dependent launch.
 fq_status enqueue_step(const Body& b, cudaStream_t s, int kv_bf16, float* x_override, int layer_only) {
@@ -261,6 +273,41 @@ fq_status enqueue_step(const Body& b, cudaStream_t s, int kv_bf16, float* x_over
         }
     };
     float* x = x_override ? x_override : w->x;
+
+    // batch 1 of a dense model: the whole step as one persistent kernel
+    if (layer_only < 0 && persist_eligible(b)) {
+        PersistArgs pa;
+        pa.layers = m->players;
+        pa.n_layers = (int)p.num_layers;
+        pa.H = H;
+        pa.F = (int)p.intermediate_size;
+        pa.Hq = Hq;
+        pa.Hkv = Hkv;
+        pa.V = (int)p.vocab_size;
+        pa.eps = p.rms_norm_eps;
+        pa.emb = m->tok_embd;
+        pa.out = m->output;
+        pa.out_norm = m->output_norm;
+        AttnArgs& a = pa.at;
+        a.qkv = w->qkv; a.qkv_stride = m->qkv_rows(); a.q_norm = nullptr; a.k_norm = nullptr;
+        a.rope = m->rope; a.eps = p.rms_norm_eps; a.Hq = Hq; a.Hkv = Hkv; a.layer = 0; a.kv_bf16 = kv_bf16;
+        a.chunk = b.chunk; a.splits = b.splits; a.st = w->st; a.part = w->part; a.counters = w->counters;
+        a.out = w->attn; a.n = 1;
+        pa.x = x;
+        pa.qkv = w->qkv;
+        pa.attn = w->attn;
+        pa.h = w->h;
+        pa.logits = b.logits;
+        pa.greedy = b.greedy ? 1 : 0;
+        pa.bar = w->pbar;
+        pa.lm_ticket = w->pbar + 2;
+        pa.err = m->err;
+        if (launch_persist(pa, s)) {
+            CK(cudaGetLastError());
+            return FQ_OK;
+        }
+        cudaGetLastError();   // a refused launch: fall through to the kernel sequence
+    }
 
     if (layer_only < 0) launch_embed(m->tok_embd, w->st, n, x, s, pdl());
     int L0 = layer_only < 0 ? 0 : layer_only, L1 = layer_only < 0 ? (int)p.num_layers : layer_only + 1;
@@ -371,8 +418,10 @@ fq_status setup_state(Workspace* w, fq_kv* const* caches, const int32_t* tokens,
 fq_status run_body(const Body& b, cudaStream_t s, int kv_bf16, int reps) {
     Workspace* w = b.w;
     const int mode = b.greedy ? MODE_GREEDY : MODE_DECODE;
-    if (env_flag("FQ_NO_GRAPH") || b.layer_out || b.route_idx) {
+    // one persistent kernel per step needs no graph (and a cooperative launch is not captured)
+    if (env_flag("FQ_NO_GRAPH") || b.layer_out || b.route_idx || persist_eligible(b)) {
         for (int r = 0; r < reps; ++r) TRY(enqueue_step(b, s, kv_bf16, nullptr, -1));
+        w->last_kernels = persist_eligible(b) ? 1u : 0u;
         return FQ_OK;
     }
     cudaGraphExec_t exec = nullptr;
@@ -647,6 +696,7 @@ fq_status fq_load_weights(const fq_desc* d, const fq_weight_src* src, void* stre
     CK(cudaGetDevice(&dev));
     gemv_prepare();
     gemm_tc_prepare();
+    persist_prepare();
     CK(cudaGetLastError());
     fq_model* m = new fq_model();
     m->d = *d;
@@ -707,13 +757,30 @@ fq_status fq_load_weights(const fq_desc* d, const fq_weight_src* src, void* stre
         auto attach = [&](QMat& q) {
             if (!q.q) return;
             m->tmaps.emplace_back();
-            if (make_tma_maps(q, &m->tmaps.back())) q.tm = &m->tmaps.back();
+            const bool gemv_ok = make_tma_maps(q, &m->tmaps.back());
+            if (gemv_ok || m->tmaps.back().tc_ok) q.tm = &m->tmaps.back();
         };
         attach(m->tok_embd);
         if (m->output.q != m->tok_embd.q) attach(m->output);
         else m->output.tm = m->tok_embd.tm;
         for (auto& lw : m->layers) {
             attach(lw.qkv); attach(lw.o); attach(lw.gate_up); attach(lw.down); attach(lw.router);
+        }
+        // layer table of the persistent batch-1 step (dense models, quantised projections)
+        auto quant = [](const QMat& q) { return q.q && (q.fmt == FMT_Q8_0 || q.fmt == FMT_Q4_K); };
+        const uint32_t G = p.num_attention_heads / p.num_key_value_heads;
+        bool persist_ok = !m->moe() && m->tok_embd.q && quant(m->output) && (G == 1 || G == 2 || G == 4 || G == 8);
+        std::vector<PersistLayer> pl(p.num_layers);
+        for (uint32_t L = 0; L < p.num_layers && persist_ok; ++L) {
+            const LayerW& lw = m->layers[L];
+            persist_ok = quant(lw.qkv) && quant(lw.o) && quant(lw.gate_up) && quant(lw.down);
+            pl[L] = PersistLayer{lw.qkv, lw.o, lw.gate_up, lw.down, lw.attn_norm, lw.ffn_norm, lw.q_norm, lw.k_norm};
+        }
+        if (persist_ok) {
+            PersistLayer* dpl;
+            TRY(dalloc(m->allocs, &dpl, pl.size()));
+            CK(cudaMemcpyAsync(dpl, pl.data(), sizeof(PersistLayer) * pl.size(), cudaMemcpyHostToDevice, s));
+            m->players = dpl;
         }
         m->max_pos = (int)p.max_positions;
         float2* rope;

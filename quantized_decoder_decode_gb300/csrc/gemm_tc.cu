@@ -4,28 +4,33 @@
 // so that every weight is read once for all streams.  With n = 8..32 rows the contraction
 // y[b][r] = sum_k W[r][k] x[b][k] is dense enough for tensor cores, so it runs "swap-AB":
 //   D[r, c] = sum_k A[r, k] B[c, k],  A = dequantised weight tile (M = 128 rows, f16),
-//                                     B = activations, N = 2 * BP columns (f16),
-// where activation row b is split into a high part hi = f16(x) (column b) and a low part
-// lo = f16(x - hi) (column BP + b): hi + lo carries ~22 bits, so only the weights are
-// rounded to f16 (relative 2^-12), and y = D[:, b] + D[:, BP + b] with f32 accumulation in
-// tensor memory.
+//                                     B = activations, N = 2 * BP columns (f16).
+// Nothing is rounded beyond f32 accuracy:
+//   * activation row b is split into a high part hi = f16(x) (column b) and a low part
+//     lo = f16(x - hi) (column BP + b), about 22 significant bits together;
+//   * a Q8_0 weight d * q (int8 q, fp16 d) has at most 18 significant bits and is carried as
+//     two f16 tiles, Wh = f16(q d) and Wl = q d - Wh (exact: one fused multiply-add in f16),
+//   * D = Wh [hi lo] + Wl [hi lo] accumulates in f32 in tensor memory, y = D[:, b] + D[:, BP+b].
 //
-// Roles in a CTA (288 threads):
-//   warps 0-3  converters: per stage of 64 K-elements, each thread streams one weight row's
-//              64 Q8_0 codes + 2 scales from global memory, dequantises to exact products
-//              d*q and rounds them once to f16 into the 128-byte-swizzled K-major layout,
-//              and copies the stage's activation slice (prepared f16 hi/lo rows);
-//   warp 8     one thread issues 4 tcgen05.mma (K = 16 each) per stage and commits the
-//              stage back to the converters; after the tile's last stage it commits the
-//              accumulator to the epilogue;
-//   warps 4-7  epilogue: tcgen05.ld of the 128 x N accumulator (one row per thread), hi+lo,
-//              then store / residual add / SwiGLU (gate, up rows adjacent) / logits+argmax.
-// Work is split into (row tile, K slice) units so that narrow matrices still cover every
-// SM: with several K slices each unit writes its partial sums to scratch and the last unit
-// of a tile to finish (atomic ticket, no waiting) adds them up and applies the epilogue.
-// Converter threads keep two chunks of codes in flight ahead of the one they decode.
+// Work split (stream-K): the (row tile, 64-element K chunk) iterations of the matrix are
+// cut into one contiguous, equal range per CTA (one CTA per SM).  A tile whose chunks all
+// fall to one CTA is finished in place; a tile split between CTAs is finished by the last of
+// them to arrive (atomic ticket per tile and epilogue warp, no waiting), which adds the
+// partial sums in CTA order, so results do not depend on timing.
+//
+// Roles in a CTA (448 threads):
+//   warp 13     TMA producer: per chunk, the 128 x 64 code box (64-byte swizzle) and the
+//               activation box (2BP x 64 halves, 128-byte swizzle = the MMA's K-major layout)
+//               into a 6-slot ring;
+//   warps 0-7   converters: thread (row, half) turns 32 codes into exact Wh / Wl halves and
+//               writes them into the 128-byte swizzled A tiles (3-slot ring);
+//   warp 12     one thread issues 2 x 4 tcgen05.mma (K = 16) per chunk into one of two
+//               tensor-memory accumulators and commits the slots back;
+//   warps 8-11  epilogue: tcgen05.ld of the accumulator (one row per thread), hi + lo, then
+//               store / residual add / SwiGLU (gate, up rows adjacent) / logits + argmax.
 // Every mbarrier wait is bounded; a stuck pipeline sets the error word and unwinds.
 
+#include <cuda.h>
 #include <cuda_fp16.h>
 
 #include <algorithm>
@@ -39,60 +44,84 @@ namespace fq {
 namespace {
 
 constexpr int TM = 128;                  // MMA M: weight rows per tile
-constexpr int KCH = 64;                  // K elements per stage: one 128-byte f16 swizzle atom
-constexpr int TSTAGES = 4;
-constexpr int A_STAGE = TM * KCH * 2;    // 16 KB
-constexpr int B_STAGE = 64 * KCH * 2;    // 8 KB (N <= 64)
-constexpr int TC_THREADS = 9 * 32;
-constexpr int CONV_WARPS = 4, EPI_WARP0 = 4, MMA_WARP = 8;
-constexpr size_t TC_SMEM = (size_t)TSTAGES * (A_STAGE + B_STAGE) + 256;
+constexpr int KCH = 64;                  // K elements per chunk: one 128-byte f16 swizzle atom
+constexpr int RS = 6;                    // raw slots: codes + activations
+constexpr int AS = 3;                    // converted weight slots: Wh + Wl
+constexpr int CODE_BYTES = TM * KCH;     // 8 KB
+constexpr int XB_BYTES = 64 * KCH * 2;   // 8 KB (N <= 64)
+constexpr int RAW_BYTES = CODE_BYTES + XB_BYTES;
+constexpr int A_TILE = TM * KCH * 2;     // 16 KB per f16 tile
+constexpr int CONV_WARPS = 8, EPI_WARP0 = 8, MMA_WARP = 12, TMA_WARP = 13;
+constexpr int TC_THREADS = 14 * 32;
+constexpr uint32_t TMEM_COLS = 128;      // two accumulators of up to 64 columns
+constexpr size_t TC_SMEM = (size_t)RS * RAW_BYTES + (size_t)AS * 2 * A_TILE + 1024 + 256;
 
 struct TcArgs {
+    alignas(64) unsigned long long mapq[16];   // codes [N][K] u8, box 64 x 128, 64-byte swizzle
+    alignas(64) unsigned long long mapx[16];   // activations [2BP][K] f16, box 64 x 2BP, 128-byte swizzle
     QMat W;              // Q8_0 [N][K], K % 64 == 0
-    const __half* xh;    // [2 * BP][K] f16: rows 0..BP-1 high parts, BP..2BP-1 low parts
     int B;               // activation rows (<= BP)
     float* y;
     int y_stride;
     int epi;
     StepState* st;
     uint32_t* err;
-    int ks;              // K slices per tile (divides K / 64)
-    float* part;         // [ks][B][N] partial sums (ks > 1)
-    uint32_t* tickets;   // [4 * tiles] arrival counters per (tile, epilogue warp), zero between uses
+    float* part;         // [grid][2][128][BP] partial sums of split tiles
+    uint32_t* tickets;   // [4 * tiles] arrivals per (tile, epilogue warp), zero between uses
 };
 
+FQ_DEV long long iter_begin(int c, long long total, int G) { return (long long)c * total / G; }
+// the CTA whose range holds iteration i
+FQ_DEV int cta_of(long long i, long long total, int G) { return (int)(((i + 1) * G + total - 1) / total) - 1; }
+
+// two int8 codes (bytes 2p, 2p+1 of w, already offset by +128) -> exact f16 pair
+FQ_DEV __half2 codes_to_h2(uint32_t w_biased, int p) {
+    const uint32_t u = __byte_perm(w_biased, 0x64u, p == 0 ? 0x4140u : 0x4342u);   // 0x64XX: 1024 + q + 128
+    return __hsub2(*reinterpret_cast<const __half2*>(&u), __floats2half2_rn(1152.f, 1152.f));
+}
+
 template <int BP>
-__global__ void __launch_bounds__(TC_THREADS, 2) gemm_tc_kernel(const TcArgs a) {
+__global__ void __launch_bounds__(TC_THREADS, 1) gemm_tc_kernel(const __grid_constant__ TcArgs a) {
     constexpr int NCOL = 2 * BP;         // MMA N
-    extern __shared__ __align__(1024) uint8_t smem[];
-    uint8_t* As = smem;
-    uint8_t* Bs = As + (size_t)TSTAGES * A_STAGE;
-    uint64_t* full = reinterpret_cast<uint64_t*>(Bs + (size_t)TSTAGES * B_STAGE);
-    uint64_t* freeb = full + TSTAGES;
-    uint64_t* acc_full = freeb + TSTAGES;
-    uint64_t* acc_free = acc_full + 1;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_free + 1);
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    uint8_t* raw = smem;                                        // [RS][codes 8 KB | activations 8 KB]
+    uint8_t* At = raw + (size_t)RS * RAW_BYTES;                 // [AS][Wh 16 KB | Wl 16 KB]
+    uint64_t* raw_full = reinterpret_cast<uint64_t*>(At + (size_t)AS * 2 * A_TILE);
+    uint64_t* raw_empty = raw_full + RS;
+    uint64_t* a_full = raw_empty + RS;
+    uint64_t* a_empty = a_full + AS;
+    uint64_t* acc_full = a_empty + AS;   // [2]
+    uint64_t* acc_free = acc_full + 2;   // [2]
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_free + 2);
     __shared__ unsigned long long best[32];
 
     const QMat& W = a.W;
     const int N = W.N, K = W.K;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int n_tiles = (N + TM - 1) / TM, n_chunks = K / KCH;
-    const int KS = a.ks, cpk = n_chunks / KS;            // K slices per tile, chunks per slice
-    const int n_units = n_tiles * KS;
-    const int my_units = (int)blockIdx.x < n_units ? (n_units - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+    const int G = gridDim.x, c = blockIdx.x;
+    const int nch = K / KCH, n_tiles = (N + TM - 1) / TM;
+    const long long total = (long long)n_tiles * nch;
+    const long long beg = iter_begin(c, total, G), end = iter_begin(c + 1, total, G);
+    const int n_it = (int)(end - beg);
 
     if (tid == 0) {
-        for (int s = 0; s < TSTAGES; ++s) {
-            mbar_init(&full[s], CONV_WARPS);
-            mbar_init(&freeb[s], 1);
+        for (int s = 0; s < RS; ++s) {
+            mbar_init(&raw_full[s], 1);
+            mbar_init(&raw_empty[s], 1);
         }
-        mbar_init(acc_full, 1);
-        mbar_init(acc_free, 4);
+        for (int s = 0; s < AS; ++s) {
+            mbar_init(&a_full[s], CONV_WARPS);
+            mbar_init(&a_empty[s], 1);
+        }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&acc_full[s], 1);
+            mbar_init(&acc_free[s], 4);
+        }
         mbar_fence_init();
     }
     if (warp == MMA_WARP) {
-        tmem_alloc(tmem_slot, 64);
+        tmem_alloc(tmem_slot, TMEM_COLS);
         tmem_relinquish();
     }
     if (tid < 32) best[tid] = 0ull;
@@ -102,150 +131,189 @@ __global__ void __launch_bounds__(TC_THREADS, 2) gemm_tc_kernel(const TcArgs a) 
     pdl_trigger();
     pdl_wait();
 
-    if (warp < CONV_WARPS) {
-        // ---------------- converters: one weight row per thread, two chunks of codes in flight
-        const int r = tid;
-        const int n_iters = my_units * cpk;
-        struct Codes {
-            uint4 c[4];
-            uint32_t sc2;
-        };
-        auto fetch = [&](int it, Codes& cd) {
-            const int unit = blockIdx.x + (it / cpk) * gridDim.x;
-            const int tile = unit / KS, chunk = (unit % KS) * cpk + it % cpk;
-            const int row = tile * TM + r;
-            if (it < n_iters && row < N) {
-                const uint8_t* src = W.q + (size_t)row * K + (size_t)chunk * KCH;
-#pragma unroll
-                for (int i = 0; i < 4; ++i) cd.c[i] = ld_stream16(src + 16 * i);
-                cd.sc2 = ld_stream4(W.s + (size_t)row * (K / 32) + (size_t)chunk * 2);
-            } else {
-#pragma unroll
-                for (int i = 0; i < 4; ++i) cd.c[i] = make_uint4(0u, 0u, 0u, 0u);
-                cd.sc2 = 0u;
+    if (warp == TMA_WARP) {
+        // ---------------- producer
+        int issued = 0;
+        for (int i = 0; i < n_it; ++i) {
+            const long long g = beg + i;
+            const int tile = (int)(g / nch), chunk = (int)(g % nch);
+            const int s = i % RS;
+            if (!mbar_wait(&raw_empty[s], ((uint32_t)(i / RS) & 1u) ^ 1u)) {
+                if (a.err && lane == 0) atomicOr(a.err, 2u);
+                break;
             }
+            if (lane == 0) {
+                uint8_t* slot = raw + (size_t)s * RAW_BYTES;
+                mbar_arrive_expect_tx(&raw_full[s], (uint32_t)(CODE_BYTES + NCOL * KCH * 2));
+                tma_load_2d(slot, a.mapq, chunk * KCH, tile * TM, &raw_full[s]);
+                tma_load_2d(slot + CODE_BYTES, a.mapx, chunk * KCH, 0, &raw_full[s]);
+            }
+            __syncwarp();
+            issued = i + 1;
+        }
+        // no copy may still be landing when the CTA exits (only possible after a timeout)
+        for (int i = issued > RS ? issued - RS : 0; i < issued; ++i) mbar_wait(&raw_full[i % RS], (uint32_t)(i / RS) & 1u);
+    } else if (warp < CONV_WARPS) {
+        // ---------------- converters: thread (row rr, half h) owns K elements 32h..32h+31
+        const int rr = (warp & 3) * 32 + lane, h = warp >> 2;
+        // fp16 scale of (row, 32-element block) for iteration i, fetched four chunks ahead
+        auto scale_of = [&](int i) -> uint32_t {
+            if (i >= n_it) return 0u;
+            const long long g = beg + i;
+            const int row = (int)(g / nch) * TM + rr;
+            if (row >= N) return 0u;
+            return (uint32_t)__ldg(W.s + (size_t)row * (K / 32) + (size_t)(g % nch) * 2 + h);
         };
-        Codes c0, c1, c2;
-        fetch(0, c0);
-        fetch(1, c1);
-        for (int it = 0; it < n_iters; ++it) {
-            fetch(it + 2, c2);
-            const int unit = blockIdx.x + (it / cpk) * gridDim.x;
-            const int chunk = (unit % KS) * cpk + it % cpk;
-            const int stage = it % TSTAGES;
-            const uint32_t ph = (uint32_t)(it / TSTAGES) & 1u;
-            if (!mbar_wait(&freeb[stage], ph ^ 1u)) {
+        uint32_t sc0 = scale_of(0), sc1 = scale_of(1), sc2 = scale_of(2), sc3 = scale_of(3);
+        for (int i = 0; i < n_it; ++i) {
+            const uint32_t sc4 = scale_of(i + 4);
+            const int s = i % RS, as = i % AS;
+            if (!mbar_wait(&raw_full[s], (uint32_t)(i / RS) & 1u) ||
+                !mbar_wait(&a_empty[as], ((uint32_t)(i / AS) & 1u) ^ 1u)) {
                 if (a.err && lane == 0) atomicOr(a.err, 4u);
                 break;
             }
-            uint8_t* Ast = As + (size_t)stage * A_STAGE;
-            const float d0 = h2f((unsigned short)(c0.sc2 & 0xFFFFu)), d1 = h2f((unsigned short)(c0.sc2 >> 16));
+            // codes of row rr, logical 16-byte chunks 2h, 2h+1 (64-byte swizzle: chunk ^ bits 1-2 of the row)
+            const uint8_t* crow = raw + (size_t)s * RAW_BYTES + rr * 64;
+            const int sw = (rr >> 1) & 3;
+            uint4 q[2];
+            q[0] = *reinterpret_cast<const uint4*>(crow + (((2 * h) ^ sw) << 4));
+            q[1] = *reinterpret_cast<const uint4*>(crow + (((2 * h + 1) ^ sw) << 4));
+            const unsigned short dbits = (unsigned short)sc0;
+            const __half dh = *reinterpret_cast<const __half*>(&dbits);
+            const __half2 d2 = __halves2half2(dh, dh);
+            uint8_t* Ah = At + (size_t)as * 2 * A_TILE;
+            uint8_t* Al = Ah + A_TILE;
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {          // 16-byte chunk j = K elements 8j..8j+7
-                const uint4 w4 = c0.c[j >> 1];
-                const uint32_t w0 = (j & 1) ? w4.z : w4.x, w1 = (j & 1) ? w4.w : w4.y;
-                float f[8];
-                s8x4_to_f32(w0, f);
-                s8x4_to_f32(w1, f + 4);
-                const float d = j < 4 ? d0 : d1;
-                __half2 h[4];
+            for (int j = 0; j < 4; ++j) {        // 16-byte output chunk 4h + j: K elements 32h + 8j ..
+                const uint4 qv = q[j >> 1];
+                const uint32_t w0 = ((j & 1) ? qv.z : qv.x) ^ 0x80808080u;
+                const uint32_t w1 = ((j & 1) ? qv.w : qv.y) ^ 0x80808080u;
+                __half2 qh[4] = {codes_to_h2(w0, 0), codes_to_h2(w0, 1), codes_to_h2(w1, 0), codes_to_h2(w1, 1)};
+                __half2 hi[4], lo[4];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) h[e] = __floats2half2_rn(f[2 * e] * d, f[2 * e + 1] * d);
-                *reinterpret_cast<uint4*>(Ast + sw128_offset(r, j)) = *reinterpret_cast<uint4*>(h);
-            }
-            uint8_t* Bst = Bs + (size_t)stage * B_STAGE;
-            for (int q = r; q < NCOL * 8; q += CONV_WARPS * 32) {
-                const int nrow = q >> 3, j = q & 7;
-                const uint4 v = *reinterpret_cast<const uint4*>(a.xh + (size_t)nrow * K + (size_t)chunk * KCH + 8 * j);
-                *reinterpret_cast<uint4*>(Bst + sw128_offset(nrow, j)) = v;
+                for (int e = 0; e < 4; ++e) {
+                    hi[e] = __hmul2(qh[e], d2);
+                    lo[e] = __hfma2(qh[e], d2, __hneg2(hi[e]));
+                }
+                const uint32_t off = sw128_offset(rr, 4 * h + j);
+                *reinterpret_cast<uint4*>(Ah + off) = *reinterpret_cast<const uint4*>(hi);
+                *reinterpret_cast<uint4*>(Al + off) = *reinterpret_cast<const uint4*>(lo);
             }
             fence_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&full[stage]);
-            c0 = c1;
-            c1 = c2;
+            if (lane == 0) mbar_arrive(&a_full[as]);
+            sc0 = sc1;
+            sc1 = sc2;
+            sc2 = sc3;
+            sc3 = sc4;
         }
     } else if (warp == MMA_WARP) {
         // ---------------- MMA issue: one thread
         if (lane == 0) {
             const uint32_t idesc = idesc_f16_f32(TM, NCOL);
-            int it = 0;
+            int t = 0;   // segment (tile) counter
+            int last = -1;   // last iteration whose MMAs were issued
             bool ok = true;
-            for (int t = 0; t < my_units && ok; ++t) {
-                if (t > 0) {
-                    if (!mbar_wait(acc_free, (uint32_t)(t - 1) & 1u)) {
-                        if (a.err) atomicOr(a.err, 8u);
-                        break;
-                    }
-                    tc_fence_after();
+            for (int i = 0; i < n_it && ok;) {
+                const long long g0 = beg + i;
+                const int chunk0 = (int)(g0 % nch);
+                const int len = (int)((long long)(nch - chunk0) < end - g0 ? (long long)(nch - chunk0) : end - g0);
+                const int slot = t & 1;
+                if (!mbar_wait(&acc_free[slot], ((uint32_t)(t >> 1) & 1u) ^ 1u)) {
+                    if (a.err) atomicOr(a.err, 8u);
+                    break;
                 }
-                for (int chunk = 0; chunk < cpk; ++chunk, ++it) {
-                    const int stage = it % TSTAGES;
-                    const uint32_t ph = (uint32_t)(it / TSTAGES) & 1u;
-                    if (!mbar_wait(&full[stage], ph)) {
+                tc_fence_after();
+                const uint32_t dacc = tbase + (uint32_t)(slot * 64);
+                for (int j = 0; j < len; ++j, ++i) {
+                    const int s = i % RS, as = i % AS;
+                    if (!mbar_wait(&a_full[as], (uint32_t)(i / AS) & 1u) ||
+                        !mbar_wait(&raw_full[s], (uint32_t)(i / RS) & 1u)) {
                         if (a.err) atomicOr(a.err, 16u);
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint64_t ad = sdesc_sw128(smem_u32(As + (size_t)stage * A_STAGE));
-                    const uint64_t bd = sdesc_sw128(smem_u32(Bs + (size_t)stage * B_STAGE));
+                    const uint32_t ah = smem_u32(At + (size_t)as * 2 * A_TILE);
+                    const uint64_t dh = sdesc_sw128(ah), dl = sdesc_sw128(ah + A_TILE);
+                    const uint64_t bd = sdesc_sw128(smem_u32(raw + (size_t)s * RAW_BYTES + CODE_BYTES));
 #pragma unroll
                     for (int k = 0; k < KCH / 16; ++k)   // 32 bytes of K per MMA: start address + 2 (x16 B)
-                        mma_f16(tbase, ad + 2 * k, bd + 2 * k, idesc, (chunk > 0 || k > 0) ? 1u : 0u);
-                    mma_commit(&freeb[stage]);
+                        mma_f16(dacc, dh + 2 * k, bd + 2 * k, idesc, (j > 0 || k > 0) ? 1u : 0u);
+#pragma unroll
+                    for (int k = 0; k < KCH / 16; ++k) mma_f16(dacc, dl + 2 * k, bd + 2 * k, idesc, 1u);
+                    mma_commit(&a_empty[as]);
+                    mma_commit(&raw_empty[s]);
+                    last = i;
                 }
-                if (ok) mma_commit(acc_full);
+                if (ok) mma_commit(&acc_full[slot]);
+                ++t;
             }
+            // every issued MMA has finished before the accumulators are released
+            if (last >= 0) mbar_wait(&raw_empty[last % RS], (uint32_t)(last / RS) & 1u);
         }
         __syncwarp();
     } else {
         // ---------------- epilogue: TMEM lanes 32q..32q+31 <-> tile rows
         const int q = warp - EPI_WARP0;
         const int rin = 32 * q + lane;
-        for (int t = 0; t < my_units; ++t) {
-            if (!mbar_wait(acc_full, (uint32_t)t & 1u)) {
+        int t = 0;
+        for (int i = 0; i < n_it; ++t) {
+            const long long g0 = beg + i;
+            const int tile = (int)(g0 / nch), chunk0 = (int)(g0 % nch);
+            const int len = (int)((long long)(nch - chunk0) < end - g0 ? (long long)(nch - chunk0) : end - g0);
+            i += len;
+            const int slot = t & 1;
+            if (!mbar_wait(&acc_full[slot], (uint32_t)(t >> 1) & 1u)) {
                 if (a.err && lane == 0) atomicOr(a.err, 32u);
                 break;
             }
             tc_fence_after();
             uint32_t v[NCOL];
 #pragma unroll
-            for (int c4 = 0; c4 < NCOL / 16; ++c4) tmem_ld16(tbase + ((uint32_t)(32 * q) << 16) + 16 * c4, v + 16 * c4);
+            for (int c4 = 0; c4 < NCOL / 16; ++c4)
+                tmem_ld16(tbase + ((uint32_t)(32 * q) << 16) + (uint32_t)(slot * 64 + 16 * c4), v + 16 * c4);
             tmem_wait_ld();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(acc_free);
-            const int unit = blockIdx.x + t * gridDim.x;
-            const int tile = unit / KS, ksl = unit % KS;
+            if (lane == 0) mbar_arrive(&acc_free[slot]);
             const int row = tile * TM + rin;
             const bool ok_row = row < N;
             float val[BP];
 #pragma unroll
             for (int b = 0; b < BP; ++b) val[b] = __uint_as_float(v[b]) + __uint_as_float(v[BP + b]);
-            if (KS > 1) {
-                // partial of this K slice -> scratch; the tile's last slice adds them up
-                if (ok_row)
+            const long long tb = (long long)tile * nch;
+            const int c_first = cta_of(tb, total, G), c_last = cta_of(tb + nch - 1, total, G);
+            if (c_first != c_last) {
+                // split tile: partial -> scratch; the last contributor adds them up in CTA order
+                const int which = (g0 == beg) ? 0 : 1;
+                float4* pp = reinterpret_cast<float4*>(a.part + (((size_t)c * 2 + which) * TM + rin) * BP);
 #pragma unroll
-                    for (int b = 0; b < BP; ++b)
-                        if (b < a.B) a.part[((size_t)ksl * a.B + b) * N + row] = val[b];
-                // each epilogue warp owns 32 rows of the tile and its own ticket
+                for (int b = 0; b < BP; b += 4) pp[b / 4] = make_float4(val[b], val[b + 1], val[b + 2], val[b + 3]);
                 __threadfence();
                 __syncwarp();
                 uint32_t prev = 0u;
                 if (lane == 0) {
                     prev = atomicAdd(&a.tickets[4 * tile + q], 1u);
-                    if (prev == (uint32_t)(KS - 1)) a.tickets[4 * tile + q] = 0u;
+                    if (prev == (uint32_t)(c_last - c_first)) a.tickets[4 * tile + q] = 0u;
                 }
                 prev = __shfl_sync(0xFFFFFFFFu, prev, 0);
-                if (prev != (uint32_t)(KS - 1)) continue;
+                if (prev != (uint32_t)(c_last - c_first)) continue;
                 __threadfence();
 #pragma unroll
-                for (int b = 0; b < BP; ++b) {
-                    float acc = 0.f;
-                    if (b < a.B && ok_row)
-                        for (int k2 = 0; k2 < KS; ++k2) acc += __ldcg(&a.part[((size_t)k2 * a.B + b) * N + row]);
-                    val[b] = acc;
+                for (int b = 0; b < BP; ++b) val[b] = 0.f;
+                for (int cc = c_first; cc <= c_last; ++cc) {
+                    const int wh = (iter_begin(cc, total, G) >= tb) ? 0 : 1;   // cc starts inside this tile
+                    const float4* src = reinterpret_cast<const float4*>(a.part + (((size_t)cc * 2 + wh) * TM + rin) * BP);
+#pragma unroll
+                    for (int b = 0; b < BP; b += 4) {
+                        const float4 f = __ldcg(src + b / 4);
+                        val[b] += f.x;
+                        val[b + 1] += f.y;
+                        val[b + 2] += f.z;
+                        val[b + 3] += f.w;
+                    }
                 }
             }
             unsigned long long kb[BP];
@@ -281,7 +349,7 @@ __global__ void __launch_bounds__(TC_THREADS, 2) gemm_tc_kernel(const TcArgs a) 
     if (a.epi == EPI_LOGITS && tid < a.B) atomicMax(&a.st->keys[tid], best[tid]);
     if (warp == MMA_WARP) {
         tc_fence_after();
-        tmem_dealloc(tbase, 64);
+        tmem_dealloc(tbase, TMEM_COLS);
     }
 }
 
@@ -322,9 +390,9 @@ int g_sms_tc = 0;
 
 template <int BP>
 void launch_bp(const TcArgs& t, cudaStream_t s, bool pdl) {
-    const int tiles = (t.W.N + TM - 1) / TM;
+    const long long total = (long long)((t.W.N + TM - 1) / TM) * (t.W.K / KCH);
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(std::min(tiles * t.ks, 2 * g_sms_tc));
+    cfg.gridDim = dim3((unsigned)std::min<long long>(total, g_sms_tc));
     cfg.blockDim = dim3(TC_THREADS);
     cfg.dynamicSmemBytes = TC_SMEM;
     cfg.stream = s;
@@ -349,7 +417,8 @@ void gemm_tc_prepare() {
 
 bool gemm_tc_applicable(const GemvArgs& a) {
     return g_sms_tc > 0 && !a.route && a.W.fmt == FMT_Q8_0 && a.W.K % KCH == 0 && a.B >= TC_MIN_BATCH &&
-           a.B <= 32 && !a.xn_out;
+           a.B <= 32 && !a.xn_out && a.W.tm && a.W.tm->tc_ok &&
+           (size_t)4 * ((a.W.N + TM - 1) / TM) <= (size_t)TC_TICKETS;
 }
 
 size_t gemm_tc_xh_elems(int K) { return (size_t)64 * K; }
@@ -369,23 +438,24 @@ void launch_gemm_tc(const GemvArgs& a, void* xh_v, float* part, size_t part_cap,
     cfg.numAttrs = pdl_prep ? 1 : 0;
     cudaLaunchKernelEx(&cfg, prep_xh_kernel, a.x, a.x_stride, a.B, BP, a.W.K, a.norm_g, a.eps, xh);
     TcArgs t;
+    std::copy(a.W.tm->tcq, a.W.tm->tcq + 16, t.mapq);
+    if (!encode_f16_rows_sw128(t.mapx, xh, (uint64_t)a.W.K, (uint64_t)(2 * BP), (uint32_t)(2 * BP))) {
+        if (a.err) cudaMemsetAsync(a.err, 0xFF, sizeof(uint32_t), s);   // reported by fq_check_device
+        return;
+    }
     t.W = a.W;
-    t.xh = xh;
     t.B = a.B;
     t.y = a.y;
     t.y_stride = a.y_stride;
     t.epi = a.epi;
     t.st = a.st;
     t.err = a.err;
-    // K slices: enough (row tile, K slice) units for two CTAs per SM, at least 4 chunks each
-    const int tiles = (a.W.N + TM - 1) / TM, n_chunks = a.W.K / KCH;
-    int ks = 1;
-    while (tiles * ks < 2 * g_sms_tc && n_chunks % (2 * ks) == 0 && n_chunks / (2 * ks) >= 4 &&
-           (size_t)(2 * ks) * a.B * a.W.N <= part_cap && 4 * tiles <= TC_TICKETS)
-        ks *= 2;
-    t.ks = ks;
     t.part = part;
     t.tickets = tickets;
+    if ((size_t)g_sms_tc * 2 * TM * BP > part_cap) {
+        if (a.err) cudaMemsetAsync(a.err, 0xFF, sizeof(uint32_t), s);
+        return;
+    }
     if (BP == 8) launch_bp<8>(t, s, pdl);
     else if (BP == 16) launch_bp<16>(t, s, pdl);
     else launch_bp<32>(t, s, pdl);

@@ -315,15 +315,26 @@ bool launch_t(const GemvArgs& a, cudaStream_t s, bool pdl) {
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 bool encode(void* map, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t rows, uint64_t row_bytes,
-            uint32_t box_inner, uint32_t box_rows) {
+            uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_NONE) {
     cuuint64_t dims[2] = {inner, rows};
     cuuint64_t strides[1] = {row_bytes};
     cuuint32_t box[2] = {box_inner, box_rows};
     cuuint32_t es[2] = {1, 1};
     CUresult r = g_encode(reinterpret_cast<CUtensorMap*>(map), dt, 2, const_cast<void*>(base), dims, strides, box, es,
-                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
+}
+
+bool load_encoder() {
+    if (g_encode) return true;
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult qr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &qr) != cudaSuccess ||
+        qr != cudaDriverEntryPointSuccess || !fn)
+        return false;
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    return true;
 }
 
 template <int FMT, int NBG>
@@ -355,15 +366,14 @@ void gemv_tma_prepare() {
 
 bool make_tma_maps(const QMat& W, TmaMaps* out) {
     out->ok = 0;
-    if (!g_encode) {
-        void* fn = nullptr;
-        cudaDriverEntryPointQueryResult qr;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &qr) !=
-                cudaSuccess ||
-            qr != cudaDriverEntryPointSuccess || !fn)
-            return false;
-        g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-    }
+    out->tc_ok = 0;
+    if (!load_encoder()) return false;
+    if (W.fmt == FMT_Q8_0 && W.K % 64 == 0 && W.N > 0)
+        // tensor-core GEMM: 64 codes x 128 rows per box, 64-byte swizzle (conflict-free row reads)
+        out->tc_ok = encode(out->tcq, CU_TENSOR_MAP_DATA_TYPE_UINT8, W.q, (uint64_t)W.K, W.N, (uint64_t)W.K, 64, 128,
+                            CU_TENSOR_MAP_SWIZZLE_64B)
+                         ? 1
+                         : 0;
     if (W.K % 256 != 0 || W.N <= 0) return false;
     const uint64_t rb = W.row_bytes();
     bool ok = false;
@@ -381,6 +391,12 @@ bool make_tma_maps(const QMat& W, TmaMaps* out) {
     }
     out->ok = ok ? 1 : 0;
     return ok;
+}
+
+bool encode_f16_rows_sw128(void* map, const void* base, uint64_t K, uint64_t rows, uint32_t box_rows) {
+    if (!load_encoder()) return false;
+    return encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, base, K, rows, K * 2, 64, box_rows,
+                  CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 bool launch_gemv_tma(const GemvArgs& a, cudaStream_t s, bool pdl) {

@@ -23,7 +23,9 @@ enum Fmt : int { FMT_F32 = 0, FMT_BF16 = 1, FMT_Q8_0 = 8, FMT_Q4_K = 12 };
 struct TmaMaps {
     alignas(64) unsigned long long q[16];
     alignas(64) unsigned long long s[16];
+    alignas(64) unsigned long long tcq[16];   // Q8_0 codes for the tensor-core GEMM
     int ok = 0;
+    int tc_ok = 0;
 };
 
 // One device-resident weight matrix [N rows, K cols].
@@ -103,8 +105,11 @@ void gemv_prepare();
 // the bulk-copy fed variant; returns false when the shape is not covered (caller falls back)
 bool launch_gemv_tma(const GemvArgs& a, cudaStream_t s, bool pdl);
 void gemv_tma_prepare();
-// build the tensor maps of W's planes for the bulk-copy GEMV (false: not applicable)
+// build the tensor maps of W's planes for the bulk-copy GEMV and the tensor-core GEMM
+// (false: the GEMV maps are not applicable; tc_ok tells about the GEMM's)
 bool make_tma_maps(const QMat& W, TmaMaps* out);
+// tensor map over f16 rows [rows][K], box 64 halves x box_rows, 128-byte swizzle
+bool encode_f16_rows_sw128(void* map, const void* base, uint64_t K, uint64_t rows, uint32_t box_rows);
 
 // tcgen05 GEMM for lockstep batches of TC_MIN_BATCH..32 rows over Q8_0 weights: a prep
 // kernel (RMSNorm + f16 hi/lo split into xh, 64 x K halves) and the GEMM
@@ -139,6 +144,30 @@ struct AttnArgs {
 };
 
 void launch_attention(const AttnArgs& a, cudaStream_t s, bool pdl);
+
+// The whole batch-1 step of a dense model as one cooperative persistent kernel (persist.cu).
+struct PersistLayer {
+    QMat qkv, o, gate_up, down;
+    const float *attn_norm, *ffn_norm, *q_norm, *k_norm;
+};
+struct PersistArgs {
+    const PersistLayer* layers;   // device array [n_layers]
+    int n_layers, H, F, Hq, Hkv, V;
+    float eps;
+    QMat emb, out;
+    const float* out_norm;
+    AttnArgs at;                  // attention template: state, scratch, chunking (layer set per layer)
+    float *x, *qkv, *attn, *h;
+    float* logits;                // null: no LM head
+    int greedy;                   // argmax hand-off after the LM head
+    uint32_t* bar;                // grid barrier [2], zero between launches
+    uint32_t* lm_ticket;          // zero between launches
+    uint32_t* err;
+};
+void persist_prepare();
+int persist_ctas();
+// false when the shapes are not covered or the launch was refused (caller uses the kernels)
+bool launch_persist(const PersistArgs& a, cudaStream_t s);
 
 // Embedding rows -> x [n][H]
 void launch_embed(const QMat& emb, const StepState* st, int n, float* x, cudaStream_t s, bool pdl);
