@@ -323,7 +323,7 @@ fq_status enqueue_step(const Body& b, cudaStream_t s, int kv_bf16, float* x_over
         a.qkv = w->qkv; a.qkv_stride = m->qkv_rows(); a.q_norm = lw.q_norm; a.k_norm = lw.k_norm;
         a.rope = m->rope; a.eps = p.rms_norm_eps; a.Hq = Hq; a.Hkv = Hkv; a.layer = L; a.kv_bf16 = kv_bf16;
         a.chunk = b.chunk; a.splits = b.splits; a.st = w->st; a.part = w->part; a.counters = w->counters;
-        a.out = w->attn; a.n = n;
+        a.out = w->attn; a.n = n; a.err = m->err;
         launch_attention(a, s, pdl());
 
         GemvArgs o;
@@ -696,6 +696,7 @@ fq_status fq_load_weights(const fq_desc* d, const fq_weight_src* src, void* stre
     CK(cudaGetDevice(&dev));
     gemv_prepare();
     gemm_tc_prepare();
+    attention_prepare();
     persist_prepare();
     CK(cudaGetLastError());
     fq_model* m = new fq_model();

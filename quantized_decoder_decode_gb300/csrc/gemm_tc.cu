@@ -70,9 +70,22 @@ struct TcArgs {
     uint32_t* tickets;   // [4 * tiles] arrivals per (tile, epilogue warp), zero between uses
 };
 
-FQ_DEV long long iter_begin(int c, long long total, int G) { return (long long)c * total / G; }
+// iterations are (tile, chunk) pairs in tile-major order; total < 2^31 / G is checked on launch
+FQ_DEV int iter_begin(int c, int total, int G) { return (int)((unsigned)(c * total) / (unsigned)G); }
 // the CTA whose range holds iteration i
-FQ_DEV int cta_of(long long i, long long total, int G) { return (int)(((i + 1) * G + total - 1) / total) - 1; }
+FQ_DEV int cta_of(int i, int total, int G) { return (int)((unsigned)((i + 1) * G + total - 1) / (unsigned)total) - 1; }
+
+// (tile, chunk) of consecutive iterations without divisions in the loop
+struct Cursor {
+    int tile, chunk, nch;
+    FQ_DEV Cursor(int it, int n) : tile(it / n), chunk(it % n), nch(n) {}
+    FQ_DEV void next() {
+        if (++chunk == nch) {
+            chunk = 0;
+            ++tile;
+        }
+    }
+};
 
 // two int8 codes (bytes 2p, 2p+1 of w, already offset by +128) -> exact f16 pair
 FQ_DEV __half2 codes_to_h2(uint32_t w_biased, int p) {
@@ -101,9 +114,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gemm_tc_kernel(const __grid_con
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int G = gridDim.x, c = blockIdx.x;
     const int nch = K / KCH, n_tiles = (N + TM - 1) / TM;
-    const long long total = (long long)n_tiles * nch;
-    const long long beg = iter_begin(c, total, G), end = iter_begin(c + 1, total, G);
-    const int n_it = (int)(end - beg);
+    const int total = n_tiles * nch;
+    const int beg = iter_begin(c, total, G), end = iter_begin(c + 1, total, G);
+    const int n_it = end - beg;
 
     if (tid == 0) {
         for (int s = 0; s < RS; ++s) {
@@ -134,9 +147,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gemm_tc_kernel(const __grid_con
     if (warp == TMA_WARP) {
         // ---------------- producer
         int issued = 0;
-        for (int i = 0; i < n_it; ++i) {
-            const long long g = beg + i;
-            const int tile = (int)(g / nch), chunk = (int)(g % nch);
+        Cursor cur(beg, nch);
+        for (int i = 0; i < n_it; ++i, cur.next()) {
+            const int tile = cur.tile, chunk = cur.chunk;
             const int s = i % RS;
             if (!mbar_wait(&raw_empty[s], ((uint32_t)(i / RS) & 1u) ^ 1u)) {
                 if (a.err && lane == 0) atomicOr(a.err, 2u);
@@ -157,16 +170,19 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gemm_tc_kernel(const __grid_con
         // ---------------- converters: thread (row rr, half h) owns K elements 32h..32h+31
         const int rr = (warp & 3) * 32 + lane, h = warp >> 2;
         // fp16 scale of (row, 32-element block) for iteration i, fetched four chunks ahead
-        auto scale_of = [&](int i) -> uint32_t {
-            if (i >= n_it) return 0u;
-            const long long g = beg + i;
-            const int row = (int)(g / nch) * TM + rr;
-            if (row >= N) return 0u;
-            return (uint32_t)__ldg(W.s + (size_t)row * (K / 32) + (size_t)(g % nch) * 2 + h);
+        Cursor ahead(beg, nch);   // the iteration whose scale is fetched next
+        int ia = 0;
+        auto next_scale = [&]() -> uint32_t {
+            uint32_t v = 0u;
+            const int row = ahead.tile * TM + rr;
+            if (ia < n_it && row < N) v = (uint32_t)__ldg(W.s + (size_t)row * (K / 32) + ahead.chunk * 2 + h);
+            ++ia;
+            ahead.next();
+            return v;
         };
-        uint32_t sc0 = scale_of(0), sc1 = scale_of(1), sc2 = scale_of(2), sc3 = scale_of(3);
+        uint32_t sc0 = next_scale(), sc1 = next_scale(), sc2 = next_scale(), sc3 = next_scale();
         for (int i = 0; i < n_it; ++i) {
-            const uint32_t sc4 = scale_of(i + 4);
+            const uint32_t sc4 = next_scale();
             const int s = i % RS, as = i % AS;
             if (!mbar_wait(&raw_full[s], (uint32_t)(i / RS) & 1u) ||
                 !mbar_wait(&a_empty[as], ((uint32_t)(i / AS) & 1u) ^ 1u)) {
@@ -215,10 +231,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gemm_tc_kernel(const __grid_con
             int t = 0;   // segment (tile) counter
             int last = -1;   // last iteration whose MMAs were issued
             bool ok = true;
-            for (int i = 0; i < n_it && ok;) {
-                const long long g0 = beg + i;
-                const int chunk0 = (int)(g0 % nch);
-                const int len = (int)((long long)(nch - chunk0) < end - g0 ? (long long)(nch - chunk0) : end - g0);
+            int chunk0 = beg % nch;
+            for (int i = 0; i < n_it && ok; chunk0 = 0) {
+                const int len = min(nch - chunk0, n_it - i);
                 const int slot = t & 1;
                 if (!mbar_wait(&acc_free[slot], ((uint32_t)(t >> 1) & 1u) ^ 1u)) {
                     if (a.err) atomicOr(a.err, 8u);
@@ -259,10 +274,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gemm_tc_kernel(const __grid_con
         const int q = warp - EPI_WARP0;
         const int rin = 32 * q + lane;
         int t = 0;
-        for (int i = 0; i < n_it; ++t) {
-            const long long g0 = beg + i;
-            const int tile = (int)(g0 / nch), chunk0 = (int)(g0 % nch);
-            const int len = (int)((long long)(nch - chunk0) < end - g0 ? (long long)(nch - chunk0) : end - g0);
+        int tile = beg / nch, chunk0 = beg % nch;
+        for (int i = 0; i < n_it; ++t, ++tile, chunk0 = 0) {
+            const int g0 = beg + i;
+            const int len = min(nch - chunk0, n_it - i);
             i += len;
             const int slot = t & 1;
             if (!mbar_wait(&acc_full[slot], (uint32_t)(t >> 1) & 1u)) {
@@ -283,7 +298,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gemm_tc_kernel(const __grid_con
             float val[BP];
 #pragma unroll
             for (int b = 0; b < BP; ++b) val[b] = __uint_as_float(v[b]) + __uint_as_float(v[BP + b]);
-            const long long tb = (long long)tile * nch;
+            const int tb = tile * nch;
             const int c_first = cta_of(tb, total, G), c_last = cta_of(tb + nch - 1, total, G);
             if (c_first != c_last) {
                 // split tile: partial -> scratch; the last contributor adds them up in CTA order
@@ -392,7 +407,7 @@ template <int BP>
 void launch_bp(const TcArgs& t, cudaStream_t s, bool pdl) {
     const long long total = (long long)((t.W.N + TM - 1) / TM) * (t.W.K / KCH);
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)std::min<long long>(total, g_sms_tc));
+    cfg.gridDim = dim3((unsigned)std::min<long long>(total, g_sms_tc));   // total * grid < 2^31: see applicable
     cfg.blockDim = dim3(TC_THREADS);
     cfg.dynamicSmemBytes = TC_SMEM;
     cfg.stream = s;
@@ -418,7 +433,8 @@ void gemm_tc_prepare() {
 bool gemm_tc_applicable(const GemvArgs& a) {
     return g_sms_tc > 0 && !a.route && a.W.fmt == FMT_Q8_0 && a.W.K % KCH == 0 && a.B >= TC_MIN_BATCH &&
            a.B <= 32 && !a.xn_out && a.W.tm && a.W.tm->tc_ok &&
-           (size_t)4 * ((a.W.N + TM - 1) / TM) <= (size_t)TC_TICKETS;
+           (size_t)4 * ((a.W.N + TM - 1) / TM) <= (size_t)TC_TICKETS &&
+           (long long)((a.W.N + TM - 1) / TM) * (a.W.K / KCH) * (g_sms_tc + 1) < (1ll << 31);
 }
 
 size_t gemm_tc_xh_elems(int K) { return (size_t)64 * K; }

@@ -141,9 +141,12 @@ struct AttnArgs {
     uint32_t* counters;           // [n][Hkv]
     float* out;                   // [n][Hq * 128]
     int n;
+    uint32_t* err = nullptr;      // device error word (a staged copy that never landed)
 };
 
 void launch_attention(const AttnArgs& a, cudaStream_t s, bool pdl);
+// one-time kernel attributes of the attention kernels; call before any graph capture
+void attention_prepare();
 
 // The whole batch-1 step of a dense model as one cooperative persistent kernel (persist.cu).
 struct PersistLayer {
