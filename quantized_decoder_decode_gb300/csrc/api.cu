@@ -194,10 +194,10 @@ fq_status ensure_ws(const fq_model* mc, cudaStream_t stream, int n, uint32_t cap
         TRY(dalloc(A, &w->attn, (size_t)nn * p.num_attention_heads * HEAD_DIM));
         TRY(dalloc(A, &w->h, (size_t)nn * std::max<size_t>(p.intermediate_size, 1)));
         TRY(dalloc(A, &w->part, pc));
-        TRY(dalloc(A, &w->counters, (size_t)nn * p.num_key_value_heads));
+        TRY(dalloc(A, &w->counters, (size_t)nn * p.num_attention_heads));   // one per (row, CTA head group) at most
         TRY(dalloc(A, &w->logits, (size_t)nn * p.vocab_size));
         TRY(dalloc(A, &w->pbar, 4));
-        CK(cudaMemsetAsync(w->counters, 0, sizeof(uint32_t) * nn * p.num_key_value_heads, stream));
+        CK(cudaMemsetAsync(w->counters, 0, sizeof(uint32_t) * nn * p.num_attention_heads, stream));
         CK(cudaMemsetAsync(w->pbar, 0, sizeof(uint32_t) * 4, stream));
         if (nn >= TC_MIN_BATCH) {
             const int kmax = (int)std::max<size_t>({H, (size_t)p.num_attention_heads * HEAD_DIM,
@@ -1145,7 +1145,7 @@ extern "C" fq_status fq_layer_step_noalloc(const fq_model* m, uint32_t layer, fq
     const size_t o_qkv = take(sizeof(float) * m->qkv_rows());
     const size_t o_attn = take(sizeof(float) * p.num_attention_heads * HEAD_DIM);
     const size_t o_part = take(sizeof(float) * p.num_attention_heads * splits * (HEAD_DIM + 2));
-    const size_t o_ctr = take(sizeof(uint32_t) * p.num_key_value_heads);
+    const size_t o_ctr = take(sizeof(uint32_t) * p.num_attention_heads);
     size_t o_h = 0, o_xn = 0, o_rl = 0, o_he = 0, o_ye = 0, o_route = 0;
     if (!m->moe()) {
         o_h = take(sizeof(float) * p.intermediate_size);
@@ -1182,7 +1182,7 @@ extern "C" fq_status fq_layer_step_noalloc(const fq_model* m, uint32_t layer, fq
     }
     cudaStream_t s = (cudaStream_t)stream;
     // the arrival counters must start at zero; the array keeps whatever the last call left
-    CK(cudaMemsetAsync(w.counters, 0, sizeof(uint32_t) * p.num_key_value_heads, s));
+    CK(cudaMemsetAsync(w.counters, 0, sizeof(uint32_t) * p.num_attention_heads, s));
     fq_kv* caches[1] = {kv};
     TRY(setup_state(&w, caches, nullptr, 1, false, nullptr, nullptr, s));
     Body body{m, &w, 1, chunk, splits, nullptr, false};

@@ -12,10 +12,14 @@
 //     (cos/sin table), scaled by log2(e)/sqrt(128) for a base-2 softmax.  The CTA whose
 //     chunk holds pos does the same for k, rounds k and v to the cache dtype, writes them
 //     at pos and uses the rounded values for that position itself.
-//   * Scores: 8 lanes per position, each with 16 of the 128 dimensions (two 16-byte reads
-//     that tile a 128-byte row segment: conflict-free), 3 shuffles to reduce.
-//   * Online softmax per head (one warp per head) over each tile, then V accumulation with
-//     threads over (pair of dimensions, one of 4 position groups).
+//   * Each warp owns 8 positions of every tile and keeps its own online-softmax state and
+//     V accumulators (flash-decode with the warps as splits), so a tile needs no barrier but
+//     the one that frees its ring slot.  Scores: 8 lanes per position, each with 16 of the
+//     128 dimensions (two 16-byte reads that tile a 128-byte row segment: conflict-free),
+//     q in registers, 3 shuffles to reduce.  V: lanes over dimensions (4 per lane).  The 8
+//     warps merge at the end.  Groups of 8 query heads are split over two CTAs of 4 heads
+//     (they read the same tiles, the second mostly from L2) so that every CTA fits the
+//     registers of two CTAs per SM.
 //   * Partial (m, l, o) per chunk; the last CTA of a (sequence, kv head) to finish (atomic
 //     ticket, no waiting) merges the chunks and writes the head outputs.
 // The ring's waits are bounded: a copy that never lands sets the error word instead of
@@ -46,15 +50,14 @@ struct ASmem {
     static constexpr int TILE = KvT<KVT>::TILE;
     static constexpr int ROW = HEAD_DIM * (int)sizeof(T);        // bytes per cached row
     static constexpr int SLOT = 2 * TILE * ROW;                   // K tile | V tile
-    // ring first (16-byte aligned slots); the final reduction reuses it
-    static constexpr int OFF_Q = A_STAGES * SLOT;                 // float q[G][128]
-    static constexpr int OFF_S = OFF_Q + G * HEAD_DIM * 4;        // float s[G][TILE]
-    static constexpr int OFF_KN = OFF_S + G * TILE * 4;           // float kn[128], vn[128]
-    static constexpr int OFF_ML = OFF_KN + 2 * HEAD_DIM * 4;      // float m[G], l[G], corr[G]
-    static constexpr int OFF_BAR = (OFF_ML + 3 * G * 4 + 15) & ~15;   // uint64 full[A_STAGES]
+    // ring first (16-byte aligned slots); the warps' final merge reuses it
+    static constexpr int OFF_Q = A_STAGES * SLOT;                 // float4 q[G][4][8] (piece, lane group)
+    static constexpr int OFF_KN = OFF_Q + G * HEAD_DIM * 4;       // float kn[128], vn[128]
+    static constexpr int OFF_ML = OFF_KN + 2 * HEAD_DIM * 4;      // float mw[8][G], lw[8][G]
+    static constexpr int OFF_BAR = (OFF_ML + 2 * A_WARPS * G * 4 + 15) & ~15;   // uint64 full[A_STAGES]
     static constexpr int OFF_MISC = OFF_BAR + A_STAGES * 8;       // int is_last; float hM[G], hL[G]
     static constexpr int BYTES = OFF_MISC + 16 + 2 * G * 4;
-    static_assert(4 * G * HEAD_DIM * 4 <= A_STAGES * SLOT, "reduction must fit in the ring");
+    static_assert(A_WARPS * G * HEAD_DIM * 4 <= A_STAGES * SLOT, "warp merge must fit in the ring");
 };
 
 FQ_DEV float bf_lo_f(uint32_t w) { return __uint_as_float(w << 16); }
@@ -76,25 +79,26 @@ FQ_DEV void norm_rope4(float v[4], const float* gain, const float2* rope_row, fl
     }
 }
 
+// G query heads per CTA (<= 4); hsplit CTAs share one kv head (G * hsplit = Hq / Hkv)
 template <int KVT, int G>
-__global__ void __launch_bounds__(A_THREADS, 2) attn_kernel(const AttnArgs a) {
+__global__ void __launch_bounds__(A_THREADS, 2) attn_kernel(const AttnArgs a, int hsplit) {
     using S = ASmem<KVT, G>;
     using T = typename S::T;
     constexpr int TILE = S::TILE;
+    constexpr int PW = TILE / A_WARPS;                 // positions per warp per tile (8 or 4)
     extern __shared__ __align__(128) uint8_t sm[];
-    float* qs = reinterpret_cast<float*>(sm + S::OFF_Q);
-    float* sc = reinterpret_cast<float*>(sm + S::OFF_S);
+    float4* qp = reinterpret_cast<float4*>(sm + S::OFF_Q);   // [G][4 pieces][8 lane groups]
     float* kn = reinterpret_cast<float*>(sm + S::OFF_KN);
     float* vn = kn + HEAD_DIM;
-    float* mh = reinterpret_cast<float*>(sm + S::OFF_ML);
-    float* lh = mh + G;
-    float* corr = lh + G;
+    float* mw = reinterpret_cast<float*>(sm + S::OFF_ML);    // [8 warps][G]
+    float* lw = mw + A_WARPS * G;
     uint64_t* full = reinterpret_cast<uint64_t*>(sm + S::OFF_BAR);
     int* is_last = reinterpret_cast<int*>(sm + S::OFF_MISC);
     float* hM = reinterpret_cast<float*>(sm + S::OFF_MISC + 16);
     float* hL = hM + G;
 
-    const int s = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+    const int s = blockIdx.x, g = blockIdx.y / hsplit, sub = blockIdx.y % hsplit, b = blockIdx.z;
+    const int hq0 = (g * hsplit + sub) * G;            // first query head of this CTA
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const SeqState ss = a.st->seq[b];
     const int pos = ss.pos, T_len = pos + 1;
@@ -132,12 +136,13 @@ __global__ void __launch_bounds__(A_THREADS, 2) attn_kernel(const AttnArgs a) {
     const bool owns_new = (s == n_act - 1);
     for (int w = warp; w < G + (owns_new ? 2 : 0); w += A_WARPS) {
         if (w < G) {
-            const int h = g * G + w;
+            const int h = hq0 + w;
             const float4 raw = __ldcg(reinterpret_cast<const float4*>(qkv + (size_t)h * HEAD_DIM + 4 * lane));
             float v[4] = {raw.x, raw.y, raw.z, raw.w};
             norm_rope4(v, a.q_norm, rope_row, a.eps, lane);
-            *reinterpret_cast<float4*>(qs + w * HEAD_DIM + 4 * lane) =
-                make_float4(v[0] * qscale, v[1] * qscale, v[2] * qscale, v[3] * qscale);
+            // dims 4 lane..4 lane+3 = piece ((lane / 2) >= 8 ? 2 : 0) + (lane & 1) of lane group (lane / 2) % 8
+            const int dim0 = 4 * lane, half = dim0 >= 64, grp8 = (dim0 % 64) / 8, piece = 2 * half + ((dim0 / 4) & 1);
+            qp[(w * 4 + piece) * 8 + grp8] = make_float4(v[0] * qscale, v[1] * qscale, v[2] * qscale, v[3] * qscale);
         } else {
             const bool isk = w == G;
             T* dst = const_cast<T*>(isk ? Kc : Vc) + (size_t)pos * HEAD_DIM;
@@ -147,30 +152,35 @@ __global__ void __launch_bounds__(A_THREADS, 2) attn_kernel(const AttnArgs a) {
             if (isk) norm_rope4(v, a.k_norm, rope_row, a.eps, lane);
             float* keep = isk ? kn : vn;
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
+            for (int j = 0; j < 4; ++j) {   // the first CTA of the kv head stores, every one keeps
                 if constexpr (KVT == 1) {
                     const __nv_bfloat16 hb = __float2bfloat16_rn(v[j]);
-                    dst[4 * lane + j] = __bfloat16_as_ushort(hb);
+                    if (sub == 0) dst[4 * lane + j] = __bfloat16_as_ushort(hb);
                     keep[4 * lane + j] = __bfloat162float(hb);
                 } else {
-                    dst[4 * lane + j] = v[j];
+                    if (sub == 0) dst[4 * lane + j] = v[j];
                     keep[4 * lane + j] = v[j];
                 }
             }
         }
     }
-    if (tid < G) {
-        mh[tid] = -INFINITY;
-        lh[tid] = 0.f;
-    }
     __syncthreads();
 
-    // thread roles for V: dims 2dp, 2dp+1 over positions j = 4 jj + pg
-    const int dp = tid & 63, pg = tid >> 6;
-    float acc[G][2];
-#pragma unroll
-    for (int h = 0; h < G; ++h) acc[h][0] = acc[h][1] = 0.f;
     const int l8 = lane & 7, grp = lane >> 3;
+    float4 qr[G][4];
+#pragma unroll
+    for (int h = 0; h < G; ++h)
+#pragma unroll
+        for (int pc = 0; pc < 4; ++pc) qr[h][pc] = qp[(h * 4 + pc) * 8 + l8];
+    // per-warp online softmax state and V accumulators (dims 4 lane..4 lane+3)
+    float m_run[G], l_run[G], acc[G][4];
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+        m_run[h] = -INFINITY;
+        l_run[h] = 0.f;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[h][e] = 0.f;
+    }
 
     for (int i = 0; i < nt; ++i) {
         const int st = i % A_STAGES;
@@ -179,16 +189,16 @@ __global__ void __launch_bounds__(A_THREADS, 2) attn_kernel(const AttnArgs a) {
         const uint8_t* Vt = Kt + TILE * S::ROW;
         const int tb = t0 + i * TILE;
         const int nv = min(TILE, t1 - tb);
+        const int jw = warp * PW;                      // this warp's positions jw..jw+PW-1
 
-        // ---- scores: position j = 32 r + 4 warp + grp (r < TILE / 32), lane l8 holds dims
-        // 8 l8..8 l8+7 and 64 + 8 l8..
-#pragma unroll 1
-        for (int r = 0; r < TILE / 32; ++r) {
-            const int j = 32 * r + 4 * warp + grp;
+        // ---- scores of the warp's positions: round r covers jw + 4 r + grp
+        float sc[PW / 4][G];
+#pragma unroll
+        for (int r = 0; r < PW / 4; ++r) {
+            const int j = jw + 4 * r + grp;
             const bool valid = j < nv;
-            const bool fresh = tb + j == pos;
             float kf[16];
-            if (fresh) {
+            if (tb + j == pos) {
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
                     kf[e] = kn[8 * l8 + e];
@@ -219,110 +229,104 @@ __global__ void __launch_bounds__(A_THREADS, 2) attn_kernel(const AttnArgs a) {
             }
 #pragma unroll
             for (int h = 0; h < G; ++h) {
-                const float4* q0 = reinterpret_cast<const float4*>(qs + h * HEAD_DIM + 8 * l8);
-                const float4* q1 = reinterpret_cast<const float4*>(qs + h * HEAD_DIM + 64 + 8 * l8);
-                const float4 a0 = q0[0], a1 = q0[1], b0 = q1[0], b1 = q1[1];
-                float d0 = a0.x * kf[0], d1 = a0.y * kf[1];
-                d0 = fmaf(a0.z, kf[2], d0); d1 = fmaf(a0.w, kf[3], d1);
-                d0 = fmaf(a1.x, kf[4], d0); d1 = fmaf(a1.y, kf[5], d1);
-                d0 = fmaf(a1.z, kf[6], d0); d1 = fmaf(a1.w, kf[7], d1);
-                d0 = fmaf(b0.x, kf[8], d0); d1 = fmaf(b0.y, kf[9], d1);
-                d0 = fmaf(b0.z, kf[10], d0); d1 = fmaf(b0.w, kf[11], d1);
-                d0 = fmaf(b1.x, kf[12], d0); d1 = fmaf(b1.y, kf[13], d1);
-                d0 = fmaf(b1.z, kf[14], d0); d1 = fmaf(b1.w, kf[15], d1);
+                const float4* q4 = qr[h];
+                float d0 = q4[0].x * kf[0], d1 = q4[0].y * kf[1];
+                d0 = fmaf(q4[0].z, kf[2], d0); d1 = fmaf(q4[0].w, kf[3], d1);
+                d0 = fmaf(q4[1].x, kf[4], d0); d1 = fmaf(q4[1].y, kf[5], d1);
+                d0 = fmaf(q4[1].z, kf[6], d0); d1 = fmaf(q4[1].w, kf[7], d1);
+                d0 = fmaf(q4[2].x, kf[8], d0); d1 = fmaf(q4[2].y, kf[9], d1);
+                d0 = fmaf(q4[2].z, kf[10], d0); d1 = fmaf(q4[2].w, kf[11], d1);
+                d0 = fmaf(q4[3].x, kf[12], d0); d1 = fmaf(q4[3].y, kf[13], d1);
+                d0 = fmaf(q4[3].z, kf[14], d0); d1 = fmaf(q4[3].w, kf[15], d1);
                 float d = d0 + d1;
                 d += __shfl_xor_sync(0xFFFFFFFFu, d, 1);
                 d += __shfl_xor_sync(0xFFFFFFFFu, d, 2);
                 d += __shfl_xor_sync(0xFFFFFFFFu, d, 4);
-                if (l8 == 0) sc[h * TILE + j] = valid ? d : -INFINITY;
+                sc[r][h] = valid ? d : -INFINITY;        // every lane of the group holds it
             }
         }
-        __syncthreads();
 
-        // ---- online softmax over the tile, one warp per head
-        if (warp < G) {
-            const int h = warp;
-            float v[TILE / 32];
-            float mt = -INFINITY;
-#pragma unroll
-            for (int r = 0; r < TILE / 32; ++r) {
-                v[r] = sc[h * TILE + 32 * r + lane];
-                mt = fmaxf(mt, v[r]);
-            }
-            mt = warp_max(mt);
-            const float mold = mh[h];
-            const float mnew = fmaxf(mold, mt);
-            const float c = mnew == -INFINITY ? 1.f : exp2f(mold - mnew);
-            float psum = 0.f;
-#pragma unroll
-            for (int r = 0; r < TILE / 32; ++r) {
-                const float p = v[r] == -INFINITY ? 0.f : exp2f(v[r] - mnew);
-                sc[h * TILE + 32 * r + lane] = p;
-                psum += p;
-            }
-            psum = warp_sum(psum);
-            if (lane == 0) {
-                lh[h] = lh[h] * c + psum;
-                mh[h] = mnew;
-                corr[h] = c;
-            }
-        }
-        __syncthreads();
-
-        // ---- V: acc = corr * acc + sum_j p_j v_j
+        // ---- per-warp online softmax over its PW positions, then V (lanes over dimensions)
 #pragma unroll
         for (int h = 0; h < G; ++h) {
-            const float c = corr[h];
-            acc[h][0] *= c;
-            acc[h][1] *= c;
-        }
-#pragma unroll 4
-        for (int jj = 0; jj < TILE / 4; ++jj) {
-            const int j = 4 * jj + pg;
-            if (j >= nv) break;
-            float v0, v1;
-            if (tb + j == pos) {
-                v0 = vn[2 * dp];
-                v1 = vn[2 * dp + 1];
-            } else if constexpr (KVT == 1) {
-                const uint32_t w = *reinterpret_cast<const uint32_t*>(Vt + j * S::ROW + 4 * dp);
-                v0 = bf_lo_f(w);
-                v1 = bf_hi_f(w);
-            } else {
-                const float2 w = *reinterpret_cast<const float2*>(Vt + j * S::ROW + 8 * dp);
-                v0 = w.x;
-                v1 = w.y;
-            }
+            float p[PW];
+            float mt = -INFINITY;
 #pragma unroll
-            for (int h = 0; h < G; ++h) {
-                const float p = sc[h * TILE + j];
-                acc[h][0] = fmaf(p, v0, acc[h][0]);
-                acc[h][1] = fmaf(p, v1, acc[h][1]);
+            for (int r = 0; r < PW / 4; ++r)
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    p[4 * r + q] = __shfl_sync(0xFFFFFFFFu, sc[r][h], 8 * q);
+                    mt = fmaxf(mt, p[4 * r + q]);
+                }
+            const float mnew = fmaxf(m_run[h], mt);
+            const float c = mnew == -INFINITY ? 1.f : exp2f(m_run[h] - mnew);
+            float psum = 0.f;
+#pragma unroll
+            for (int e = 0; e < PW; ++e) {
+                p[e] = p[e] == -INFINITY ? 0.f : exp2f(p[e] - mnew);
+                psum += p[e];
+            }
+            l_run[h] = l_run[h] * c + psum;
+            m_run[h] = mnew;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[h][e] *= c;
+            // position jw + 4 r + q  <->  p[4 r + q]
+#pragma unroll
+            for (int e = 0; e < PW; ++e) {
+                const int j = jw + e;
+                if (p[e] == 0.f) continue;             // masked (or underflowed) position
+                float v4[4];
+                if (tb + j == pos) {
+                    const float4 x = *reinterpret_cast<const float4*>(vn + 4 * lane);
+                    v4[0] = x.x; v4[1] = x.y; v4[2] = x.z; v4[3] = x.w;
+                } else if constexpr (KVT == 1) {
+                    const uint2 w = *reinterpret_cast<const uint2*>(Vt + j * S::ROW + 8 * lane);
+                    v4[0] = bf_lo_f(w.x); v4[1] = bf_hi_f(w.x); v4[2] = bf_lo_f(w.y); v4[3] = bf_hi_f(w.y);
+                } else {
+                    const float4 x = *reinterpret_cast<const float4*>(Vt + j * S::ROW + 16 * lane);
+                    v4[0] = x.x; v4[1] = x.y; v4[2] = x.z; v4[3] = x.w;
+                }
+#pragma unroll
+                for (int d = 0; d < 4; ++d) acc[h][d] = fmaf(p[e], v4[d], acc[h][d]);
             }
         }
-        __syncthreads();   // the slot and the probabilities are free again
+        __syncthreads();   // every warp is done with the slot
         if (tid == 0 && i + A_STAGES < nt) issue(i + A_STAGES);
     }
 
-    // ---- the 4 position groups into o[h][d] (the ring is free: all copies were consumed)
-    float* red = reinterpret_cast<float*>(sm);   // [4][G][128]
+    // ---- merge the 8 warps (the ring is free: all copies were consumed)
+    float* ow = reinterpret_cast<float*>(sm);   // [8][G][128]
 #pragma unroll
-    for (int h = 0; h < G; ++h)
-        *reinterpret_cast<float2*>(red + ((size_t)pg * G + h) * HEAD_DIM + 2 * dp) = make_float2(acc[h][0], acc[h][1]);
+    for (int h = 0; h < G; ++h) {
+        if (lane == 0) {
+            mw[warp * G + h] = m_run[h];
+            lw[warp * G + h] = l_run[h];
+        }
+        *reinterpret_cast<float4*>(ow + ((size_t)warp * G + h) * HEAD_DIM + 4 * lane) =
+            make_float4(acc[h][0], acc[h][1], acc[h][2], acc[h][3]);
+    }
     __syncthreads();
     float* outb = a.out + (size_t)b * a.Hq * HEAD_DIM;
     for (int i = tid; i < G * HEAD_DIM; i += A_THREADS) {
         const int h = i / HEAD_DIM, d = i % HEAD_DIM;
-        const float O = red[(0 * G + h) * HEAD_DIM + d] + red[(1 * G + h) * HEAD_DIM + d] +
-                        red[(2 * G + h) * HEAD_DIM + d] + red[(3 * G + h) * HEAD_DIM + d];
-        const int hq = g * G + h;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < A_WARPS; ++w) M = fmaxf(M, mw[w * G + h]);
+        float L = 0.f, O = 0.f;
+#pragma unroll
+        for (int w = 0; w < A_WARPS; ++w) {
+            const float c = mw[w * G + h] == -INFINITY ? 0.f : exp2f(mw[w * G + h] - M);
+            L += lw[w * G + h] * c;
+            O += ow[((size_t)w * G + h) * HEAD_DIM + d] * c;
+        }
+        const int hq = hq0 + h;
         if (n_act == 1) {
-            outb[(size_t)hq * HEAD_DIM + d] = O / lh[h];
+            outb[(size_t)hq * HEAD_DIM + d] = O / L;
         } else {
             float* p = a.part + (((size_t)b * a.Hq + hq) * a.splits + s) * (HEAD_DIM + 2);
             if (d == 0) {
-                p[0] = mh[h];
-                p[1] = lh[h];
+                p[0] = M;
+                p[1] = L;
             }
             p[2 + d] = O;
         }
@@ -333,7 +337,7 @@ __global__ void __launch_bounds__(A_THREADS, 2) attn_kernel(const AttnArgs a) {
     __syncthreads();
     if (tid == 0) {
         __threadfence();                        // release this CTA's partial (written above)
-        uint32_t* ctr = a.counters + (size_t)b * a.Hkv + g;
+        uint32_t* ctr = a.counters + (size_t)b * a.Hq + hq0;   // one counter per CTA group of heads
         const uint32_t prev = atomicAdd(ctr, 1u);
         *is_last = (prev == (uint32_t)(n_act - 1));
         if (*is_last) *ctr = 0u;                // every chunk has arrived: re-arm for the next use
@@ -343,19 +347,19 @@ __global__ void __launch_bounds__(A_THREADS, 2) attn_kernel(const AttnArgs a) {
     __threadfence();
     // per-chunk weights exp2(m - M) / L in shared memory (the ring), then each thread sums
     // the chunks' o[d] for its (head, dimension) with independent loads
-    float* wgt = red;                           // [G][n_act]
+    float* wgt = ow;                            // [G][n_act]
     const bool fits = (size_t)G * n_act * 4 <= (size_t)A_STAGES * S::SLOT;
     if (fits) {
         for (int i = tid; i < G * n_act; i += A_THREADS) {
             const int h = i / n_act, c = i % n_act;
-            wgt[i] = __ldcg(a.part + (((size_t)b * a.Hq + g * G + h) * a.splits + c) * (HEAD_DIM + 2));
+            wgt[i] = __ldcg(a.part + (((size_t)b * a.Hq + hq0 + h) * a.splits + c) * (HEAD_DIM + 2));
         }
         __syncthreads();
         if (tid < G) {
             float M = -INFINITY, L = 0.f;
             for (int c = 0; c < n_act; ++c) M = fmaxf(M, wgt[tid * n_act + c]);
             for (int c = 0; c < n_act; ++c) {
-                const float* p = a.part + (((size_t)b * a.Hq + g * G + tid) * a.splits + c) * (HEAD_DIM + 2);
+                const float* p = a.part + (((size_t)b * a.Hq + hq0 + tid) * a.splits + c) * (HEAD_DIM + 2);
                 L += __ldcg(p + 1) * exp2f(wgt[tid * n_act + c] - M);
             }
             hM[tid] = M;
@@ -367,7 +371,7 @@ __global__ void __launch_bounds__(A_THREADS, 2) attn_kernel(const AttnArgs a) {
     }
     for (int i = tid; i < G * HEAD_DIM; i += A_THREADS) {
         const int h = i / HEAD_DIM, d = i % HEAD_DIM;
-        const int hq = g * G + h;
+        const int hq = hq0 + h;
         const float* base = a.part + ((size_t)b * a.Hq + hq) * a.splits * (HEAD_DIM + 2);
         float O = 0.f;
         if (fits) {
@@ -396,9 +400,9 @@ __global__ void __launch_bounds__(A_THREADS, 2) attn_kernel(const AttnArgs a) {
 }
 
 template <int KVT, int G>
-void launch_t(const AttnArgs& a, cudaStream_t s, bool pdl) {
+void launch_t(const AttnArgs& a, cudaStream_t s, bool pdl, int hsplit) {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(a.splits, a.Hkv, a.n);
+    cfg.gridDim = dim3(a.splits, a.Hkv * hsplit, a.n);
     cfg.blockDim = dim3(A_THREADS);
     cfg.dynamicSmemBytes = ASmem<KVT, G>::BYTES;
     cfg.stream = s;
@@ -407,16 +411,16 @@ void launch_t(const AttnArgs& a, cudaStream_t s, bool pdl) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    cudaLaunchKernelEx(&cfg, attn_kernel<KVT, G>, a);
+    cudaLaunchKernelEx(&cfg, attn_kernel<KVT, G>, a, hsplit);
 }
 
 template <int KVT>
 void launch_kv(const AttnArgs& a, cudaStream_t s, bool pdl) {
     switch (a.Hq / a.Hkv) {
-        case 1: launch_t<KVT, 1>(a, s, pdl); break;
-        case 2: launch_t<KVT, 2>(a, s, pdl); break;
-        case 4: launch_t<KVT, 4>(a, s, pdl); break;
-        case 8: launch_t<KVT, 8>(a, s, pdl); break;
+        case 1: launch_t<KVT, 1>(a, s, pdl, 1); break;
+        case 2: launch_t<KVT, 2>(a, s, pdl, 1); break;
+        case 4: launch_t<KVT, 4>(a, s, pdl, 1); break;
+        case 8: launch_t<KVT, 4>(a, s, pdl, 2); break;
         default: break;   // rejected at descriptor validation
     }
 }
@@ -429,8 +433,8 @@ void prepare_t() {
 }  // namespace
 
 void attention_prepare() {
-    prepare_t<0, 1>(); prepare_t<0, 2>(); prepare_t<0, 4>(); prepare_t<0, 8>();
-    prepare_t<1, 1>(); prepare_t<1, 2>(); prepare_t<1, 4>(); prepare_t<1, 8>();
+    prepare_t<0, 1>(); prepare_t<0, 2>(); prepare_t<0, 4>();
+    prepare_t<1, 1>(); prepare_t<1, 2>(); prepare_t<1, 4>();
 }
 
 void launch_attention(const AttnArgs& a, cudaStream_t s, bool pdl) {

@@ -369,19 +369,22 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gemm_tc_kernel(const __grid_con
 }
 
 // x (optionally RMSNorm-ed with gain g) -> f16 high / low rows for the MMA B operand;
-// rows B..BP-1 are zero.  One CTA per padded row.
+// rows B..BP-1 are zero.  Grid (BP, K slices of XK elements): each CTA converts one slice of
+// one row (the RMS of the whole row is recomputed per CTA, from L2).
+constexpr int XK = 2048;
 __global__ void __launch_bounds__(256) prep_xh_kernel(const float* x, int x_stride, int B, int BP, int K,
                                                       const float* g, float eps, __half* xh) {
     pdl_trigger();
     pdl_wait();
     __shared__ float red[32];
     const int b = blockIdx.x;
+    const int k0 = blockIdx.y * XK, k1 = min(K, k0 + XK);
     __half* hi = xh + (size_t)b * K;
     __half* lo = xh + (size_t)(BP + b) * K;
     if (b >= B) {
-        for (int k = threadIdx.x; k < K; k += blockDim.x) {
-            hi[k] = __float2half_rn(0.f);
-            lo[k] = __float2half_rn(0.f);
+        for (int k = k0 + 4 * threadIdx.x; k < k1; k += 4 * blockDim.x) {
+            *reinterpret_cast<uint2*>(hi + k) = make_uint2(0u, 0u);
+            *reinterpret_cast<uint2*>(lo + k) = make_uint2(0u, 0u);
         }
         return;
     }
@@ -389,15 +392,26 @@ __global__ void __launch_bounds__(256) prep_xh_kernel(const float* x, int x_stri
     float inv = 1.f;
     if (g) {
         float ss = 0.f;
-        for (int k = threadIdx.x; k < K; k += blockDim.x) ss += xr[k] * xr[k];
+        for (int k = 4 * threadIdx.x; k < K; k += 4 * blockDim.x) {
+            const float4 v = *reinterpret_cast<const float4*>(xr + k);
+            ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+        }
         ss = block_sum(ss, red);
         inv = rsqrtf(ss / (float)K + eps);
     }
-    for (int k = threadIdx.x; k < K; k += blockDim.x) {
-        const float v = g ? xr[k] * inv * g[k] : xr[k];
-        const __half h = __float2half_rn(v);
-        hi[k] = h;
-        lo[k] = __float2half_rn(v - __half2float(h));
+    for (int k = k0 + 4 * threadIdx.x; k < k1; k += 4 * blockDim.x) {
+        float4 v = *reinterpret_cast<const float4*>(xr + k);
+        if (g) {
+            const float4 gg = *reinterpret_cast<const float4*>(g + k);
+            v.x = v.x * inv * gg.x; v.y = v.y * inv * gg.y; v.z = v.z * inv * gg.z; v.w = v.w * inv * gg.w;
+        }
+        const __half2 h01 = __floats2half2_rn(v.x, v.y), h23 = __floats2half2_rn(v.z, v.w);
+        const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
+        const __half2 l01 = __floats2half2_rn(v.x - f01.x, v.y - f01.y), l23 = __floats2half2_rn(v.z - f23.x, v.w - f23.y);
+        *reinterpret_cast<uint2*>(hi + k) =
+            make_uint2(*reinterpret_cast<const uint32_t*>(&h01), *reinterpret_cast<const uint32_t*>(&h23));
+        *reinterpret_cast<uint2*>(lo + k) =
+            make_uint2(*reinterpret_cast<const uint32_t*>(&l01), *reinterpret_cast<const uint32_t*>(&l23));
     }
 }
 
@@ -444,7 +458,7 @@ void launch_gemm_tc(const GemvArgs& a, void* xh_v, float* part, size_t part_cap,
     __half* xh = static_cast<__half*>(xh_v);
     const int BP = a.B <= 8 ? 8 : a.B <= 16 ? 16 : 32;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(BP);
+    cfg.gridDim = dim3(BP, (a.W.K + XK - 1) / XK);
     cfg.blockDim = dim3(256);
     cfg.stream = s;
     cudaLaunchAttribute attr[1];

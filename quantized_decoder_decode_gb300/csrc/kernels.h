@@ -138,7 +138,7 @@ struct AttnArgs {
     int splits;                   // grid.x
     const StepState* st;
     float* part;                  // [n][Hq][splits][130] partial (m, l, o[128])
-    uint32_t* counters;           // [n][Hkv]
+    uint32_t* counters;           // [n][Hq]: arrivals per (row, CTA group of query heads)
     float* out;                   // [n][Hq * 128]
     int n;
     uint32_t* err = nullptr;      // device error word (a staged copy that never landed)

@@ -228,17 +228,19 @@ FQ_DEV float dot_unit(const Raw& r, int u, const float* xs, const float* xsum16)
         const float4* plo = reinterpret_cast<const float4*>(xs + xpad<FMT>(e0));
         const float4* phi = reinterpret_cast<const float4*>(xs + xpad<FMT>(e0 + 32));
         const uint32_t w[8] = {r.q.x, r.q.y, r.q.z, r.q.w, r.q2.x, r.q2.y, r.q2.z, r.q2.w};
+        // codes as 1 + q/128 (one byte permute each); sum q x recovered from the per-16 sums
         float slo = 0.f, shi = 0.f;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            float lo[4], hi[4];
-            u8x4_to_f32(w[i] & 0x0F0F0F0Fu, lo);
-            u8x4_to_f32((w[i] >> 4) & 0x0F0F0F0Fu, hi);
+            const uint32_t lw = (w[i] & 0x0F0F0F0Fu) | 0x80808080u;
+            const uint32_t hw = ((w[i] >> 4) & 0x0F0F0F0Fu) | 0x80808080u;
             const float4 xl = plo[i], xh = phi[i];
-            slo = fmaf(lo[0], xl.x, slo); slo = fmaf(lo[1], xl.y, slo);
-            slo = fmaf(lo[2], xl.z, slo); slo = fmaf(lo[3], xl.w, slo);
-            shi = fmaf(hi[0], xh.x, shi); shi = fmaf(hi[1], xh.y, shi);
-            shi = fmaf(hi[2], xh.z, shi); shi = fmaf(hi[3], xh.w, shi);
+            const float xla[4] = {xl.x, xl.y, xl.z, xl.w}, xha[4] = {xh.x, xh.y, xh.z, xh.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                slo = fmaf(__uint_as_float(__byte_perm(lw, 0x3F000000u, 0x7044u | (j << 8))), xla[j], slo);
+                shi = fmaf(__uint_as_float(__byte_perm(hw, 0x3F000000u, 0x7044u | (j << 8))), xha[j], shi);
+            }
         }
         const float d = h2f((unsigned short)(r.hdr.x & 0xFFFFu)), dmin = h2f((unsigned short)(r.hdr.x >> 16));
         const uint32_t W0 = r.hdr.y, W1 = r.hdr.z, W2 = r.hdr.w;
@@ -255,7 +257,8 @@ FQ_DEV float dot_unit(const Raw& r, int u, const float* xs, const float* xsum16)
         }
         const float s_lo = xsum16[e0 >> 4] + xsum16[(e0 >> 4) + 1];
         const float s_hi = xsum16[(e0 >> 4) + 2] + xsum16[(e0 >> 4) + 3];
-        return d * (float)sc0 * slo - dmin * (float)mn0 * s_lo + d * (float)sc1 * shi - dmin * (float)mn1 * s_hi;
+        return d * (float)sc0 * 128.f * (slo - s_lo) - dmin * (float)mn0 * s_lo + d * (float)sc1 * 128.f * (shi - s_hi) -
+               dmin * (float)mn1 * s_hi;
     }
 }
 

@@ -142,18 +142,20 @@ FQ_DEV float dot_frag(const Raw& r, int u, const XFrag<FMT>& x, const float* xsu
         const int c = u & 3;
         const int e0 = (u >> 2) * 256 + 64 * c;
         const uint32_t w[8] = {r.q.x, r.q.y, r.q.z, r.q.w, r.q2.x, r.q2.y, r.q2.z, r.q2.w};
+        // each 4-bit code q becomes the float 1 + q/128 in one byte permute (byte 2 = 0x80 | q
+        // under the exponent byte 0x3F); sum (1 + q/128) x = sum x + (sum q x) / 128, and the
+        // per-16 sums of x recover sum q x below (about 4 of f32's 24 bits go to the cancellation)
         float slo = 0.f, shi = 0.f, slo2 = 0.f, shi2 = 0.f;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            float lo[4], hi[4];
-            u8x4_to_f32(w[i] & 0x0F0F0F0Fu, lo);
-            u8x4_to_f32((w[i] >> 4) & 0x0F0F0F0Fu, hi);
+            const uint32_t lo = (w[i] & 0x0F0F0F0Fu) | 0x80808080u;
+            const uint32_t hi = ((w[i] >> 4) & 0x0F0F0F0Fu) | 0x80808080u;
             float& al = (i & 1) ? slo2 : slo;
             float& ah = (i & 1) ? shi2 : shi;
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                al = fmaf(lo[j], x.v[4 * i + j], al);
-                ah = fmaf(hi[j], x.v[32 + 4 * i + j], ah);
+                al = fmaf(__uint_as_float(__byte_perm(lo, 0x3F000000u, 0x7044u | (j << 8))), x.v[4 * i + j], al);
+                ah = fmaf(__uint_as_float(__byte_perm(hi, 0x3F000000u, 0x7044u | (j << 8))), x.v[32 + 4 * i + j], ah);
             }
         }
         slo += slo2;
@@ -176,7 +178,7 @@ FQ_DEV float dot_frag(const Raw& r, int u, const XFrag<FMT>& x, const float* xsu
         // xsum16 holds per-16 sums; sub-blocks 2c and 2c+1 span two entries each
         const float s_lo = xsum16[e0 >> 4] + xsum16[(e0 >> 4) + 1];
         const float s_hi = xsum16[(e0 >> 4) + 2] + xsum16[(e0 >> 4) + 3];
-        return d1 * slo - m1 * s_lo + d2 * shi - m2 * s_hi;
+        return d1 * 128.f * (slo - s_lo) - m1 * s_lo + d2 * 128.f * (shi - s_hi) - m2 * s_hi;
     } else {
         return __uint_as_float(r.q.x) * x.v[0] + __uint_as_float(r.q.y) * x.v[1] + __uint_as_float(r.q.z) * x.v[2] +
                __uint_as_float(r.q.w) * x.v[3];
