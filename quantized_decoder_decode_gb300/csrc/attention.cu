@@ -54,7 +54,9 @@ struct ASmem {
     static constexpr int OFF_Q = A_STAGES * SLOT;                 // float4 q[G][4][8] (piece, lane group)
     static constexpr int OFF_KN = OFF_Q + G * HEAD_DIM * 4;       // float kn[128], vn[128]
     static constexpr int OFF_ML = OFF_KN + 2 * HEAD_DIM * 4;      // float mw[8][G], lw[8][G]
-    static constexpr int OFF_BAR = (OFF_ML + 2 * A_WARPS * G * 4 + 15) & ~15;   // uint64 full[A_STAGES]
+    static constexpr int OFF_P = (OFF_ML + 2 * A_WARPS * G * 4 + 15) & ~15;   // float pw[8][G][TILE/8 + 4]
+    static constexpr int PSTRIDE = TILE / A_WARPS + 4;            // probabilities of a head, then its rescale
+    static constexpr int OFF_BAR = (OFF_P + A_WARPS * G * PSTRIDE * 4 + 15) & ~15;   // uint64 full[A_STAGES]
     static constexpr int OFF_MISC = OFF_BAR + A_STAGES * 8;       // int is_last; float hM[G], hL[G]
     static constexpr int BYTES = OFF_MISC + 16 + 2 * G * 4;
     static_assert(A_WARPS * G * HEAD_DIM * 4 <= A_STAGES * SLOT, "warp merge must fit in the ring");
@@ -80,6 +82,41 @@ FQ_DEV void norm_rope4(float v[4], const float* gain, const float2* rope_row, fl
 }
 
 // G query heads per CTA (<= 4); hsplit CTAs share one kv head (G * hsplit = Hq / Hkv)
+// Sum G per-head partials over the 8 lanes of a position group, transposing as it goes: the
+// lane keeps half of its heads at each exchange, so after log2(G) exchanges it holds one
+// head's value and the remaining exchanges are plain sums.  Returns the full sum for head
+// *h of this lane (lanes l8 and l8 ^ (8 / G >> 1).. hold equal copies).
+template <int G>
+FQ_DEV float reduce8(const float (&d)[G], int l8, int& h) {
+    if constexpr (G == 4) {
+        const bool up = l8 & 4, up2 = l8 & 2;
+        float k0 = up ? d[2] : d[0], k1 = up ? d[3] : d[1];
+        const float s0 = up ? d[0] : d[2], s1 = up ? d[1] : d[3];
+        k0 += __shfl_xor_sync(0xFFFFFFFFu, s0, 4);
+        k1 += __shfl_xor_sync(0xFFFFFFFFu, s1, 4);
+        float k = up2 ? k1 : k0;
+        k += __shfl_xor_sync(0xFFFFFFFFu, up2 ? k0 : k1, 2);
+        k += __shfl_xor_sync(0xFFFFFFFFu, k, 1);
+        h = (up ? 2 : 0) + (up2 ? 1 : 0);
+        return k;
+    } else if constexpr (G == 2) {
+        const bool up = l8 & 4;
+        float k = up ? d[1] : d[0];
+        k += __shfl_xor_sync(0xFFFFFFFFu, up ? d[0] : d[1], 4);
+        k += __shfl_xor_sync(0xFFFFFFFFu, k, 2);
+        k += __shfl_xor_sync(0xFFFFFFFFu, k, 1);
+        h = up ? 1 : 0;
+        return k;
+    } else {
+        float k = d[0];
+        k += __shfl_xor_sync(0xFFFFFFFFu, k, 4);
+        k += __shfl_xor_sync(0xFFFFFFFFu, k, 2);
+        k += __shfl_xor_sync(0xFFFFFFFFu, k, 1);
+        h = 0;
+        return k;
+    }
+}
+
 template <int KVT, int G>
 __global__ void __launch_bounds__(A_THREADS, 2) attn_kernel(const AttnArgs a, int hsplit) {
     using S = ASmem<KVT, G>;
@@ -126,6 +163,7 @@ __global__ void __launch_bounds__(A_THREADS, 2) attn_kernel(const AttnArgs a, in
         mbar_fence_init();
         for (int i = 0; i < min(nt, A_STAGES); ++i) issue(i);
     }
+    prefetch_next(a.next, tid, A_THREADS);
     pdl_trigger();
     pdl_wait();
 
@@ -172,15 +210,14 @@ __global__ void __launch_bounds__(A_THREADS, 2) attn_kernel(const AttnArgs a, in
     for (int h = 0; h < G; ++h)
 #pragma unroll
         for (int pc = 0; pc < 4; ++pc) qr[h][pc] = qp[(h * 4 + pc) * 8 + l8];
-    // per-warp online softmax state and V accumulators (dims 4 lane..4 lane+3)
-    float m_run[G], l_run[G], acc[G][4];
+    // online softmax state of the lane's head (all lanes holding a head agree) and the V
+    // accumulators of every head for dims 4 lane..4 lane+3
+    float m_run[1] = {-INFINITY}, l_run[1] = {0.f}, acc[G][4];
 #pragma unroll
-    for (int h = 0; h < G; ++h) {
-        m_run[h] = -INFINITY;
-        l_run[h] = 0.f;
+    for (int h = 0; h < G; ++h)
 #pragma unroll
         for (int e = 0; e < 4; ++e) acc[h][e] = 0.f;
-    }
+    int hl_own = 0;
 
     for (int i = 0; i < nt; ++i) {
         const int st = i % A_STAGES;
@@ -191,8 +228,10 @@ __global__ void __launch_bounds__(A_THREADS, 2) attn_kernel(const AttnArgs a, in
         const int nv = min(TILE, t1 - tb);
         const int jw = warp * PW;                      // this warp's positions jw..jw+PW-1
 
-        // ---- scores of the warp's positions: round r covers jw + 4 r + grp
-        float sc[PW / 4][G];
+        // ---- scores of the warp's positions: round r covers position jw + 4 r + grp; after the
+        // reduction lane (grp, l8) holds the score of head hl for that position
+        float sr[PW / 4];
+        int hl = 0;
 #pragma unroll
         for (int r = 0; r < PW / 4; ++r) {
             const int j = jw + 4 * r + grp;
@@ -227,6 +266,7 @@ __global__ void __launch_bounds__(A_THREADS, 2) attn_kernel(const AttnArgs a, in
 #pragma unroll
                 for (int e = 0; e < 16; ++e) kf[e] = 0.f;
             }
+            float dd[G];
 #pragma unroll
             for (int h = 0; h < G; ++h) {
                 const float4* q4 = qr[h];
@@ -238,43 +278,61 @@ __global__ void __launch_bounds__(A_THREADS, 2) attn_kernel(const AttnArgs a, in
                 d0 = fmaf(q4[2].z, kf[10], d0); d1 = fmaf(q4[2].w, kf[11], d1);
                 d0 = fmaf(q4[3].x, kf[12], d0); d1 = fmaf(q4[3].y, kf[13], d1);
                 d0 = fmaf(q4[3].z, kf[14], d0); d1 = fmaf(q4[3].w, kf[15], d1);
-                float d = d0 + d1;
-                d += __shfl_xor_sync(0xFFFFFFFFu, d, 1);
-                d += __shfl_xor_sync(0xFFFFFFFFu, d, 2);
-                d += __shfl_xor_sync(0xFFFFFFFFu, d, 4);
-                sc[r][h] = valid ? d : -INFINITY;        // every lane of the group holds it
+                dd[h] = d0 + d1;
             }
+            const float sc = reduce8<G>(dd, l8, hl);
+            hl_own = hl;
+            sr[r] = valid ? sc : -INFINITY;
         }
 
-        // ---- per-warp online softmax over its PW positions, then V (lanes over dimensions)
+        // ---- online softmax of head hl over the warp's positions: the other 3 groups hold the
+        // other positions of the same head (xor 8, 16)
+        float mt = sr[0];
 #pragma unroll
-        for (int h = 0; h < G; ++h) {
-            float p[PW];
-            float mt = -INFINITY;
+        for (int r = 1; r < PW / 4; ++r) mt = fmaxf(mt, sr[r]);
+        mt = fmaxf(mt, __shfl_xor_sync(0xFFFFFFFFu, mt, 8));
+        mt = fmaxf(mt, __shfl_xor_sync(0xFFFFFFFFu, mt, 16));
+        const float mold = m_run[0];              // lane-local state of head hl
+        const float mnew = fmaxf(mold, mt);
+        const float c = mnew == -INFINITY ? 1.f : exp2f(mold - mnew);
+        float psum = 0.f;
+        float pr[PW / 4];
 #pragma unroll
-            for (int r = 0; r < PW / 4; ++r)
+        for (int r = 0; r < PW / 4; ++r) {
+            pr[r] = sr[r] == -INFINITY ? 0.f : exp2f(sr[r] - mnew);
+            psum += pr[r];
+        }
+        psum += __shfl_xor_sync(0xFFFFFFFFu, psum, 8);
+        psum += __shfl_xor_sync(0xFFFFFFFFu, psum, 16);
+        m_run[0] = mnew;
+        l_run[0] = l_run[0] * c + psum;
+        // probabilities [head][position] and the rescale of each head, per warp
+        float* pw = reinterpret_cast<float*>(sm + S::OFF_P) + (size_t)warp * G * S::PSTRIDE;
+        if ((l8 & (8 / G - 1)) == 0) {           // one writer per (group, head)
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    p[4 * r + q] = __shfl_sync(0xFFFFFFFFu, sc[r][h], 8 * q);
-                    mt = fmaxf(mt, p[4 * r + q]);
+            for (int r = 0; r < PW / 4; ++r) pw[hl * S::PSTRIDE + 4 * r + grp] = pr[r];
+            if (grp == 0) pw[hl * S::PSTRIDE + PW] = c;
+        }
+        __syncwarp();
+
+        // ---- V: acc[h] = c_h acc[h] + sum_e p[h][e] v_e, lanes over dimensions
+        if (__any_sync(0xFFFFFFFFu, mt != -INFINITY)) {
+            float ph[G][PW];
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+#pragma unroll
+                for (int e = 0; e < PW; e += 4) {
+                    const float4 t = *reinterpret_cast<const float4*>(pw + h * S::PSTRIDE + e);
+                    ph[h][e] = t.x; ph[h][e + 1] = t.y; ph[h][e + 2] = t.z; ph[h][e + 3] = t.w;
                 }
-            const float mnew = fmaxf(m_run[h], mt);
-            const float c = mnew == -INFINITY ? 1.f : exp2f(m_run[h] - mnew);
-            float psum = 0.f;
+                const float ch = pw[h * S::PSTRIDE + PW];
 #pragma unroll
-            for (int e = 0; e < PW; ++e) {
-                p[e] = p[e] == -INFINITY ? 0.f : exp2f(p[e] - mnew);
-                psum += p[e];
+                for (int d = 0; d < 4; ++d) acc[h][d] *= ch;
             }
-            l_run[h] = l_run[h] * c + psum;
-            m_run[h] = mnew;
-#pragma unroll
-            for (int e = 0; e < 4; ++e) acc[h][e] *= c;
-            // position jw + 4 r + q  <->  p[4 r + q]
 #pragma unroll
             for (int e = 0; e < PW; ++e) {
                 const int j = jw + e;
-                if (p[e] == 0.f) continue;             // masked (or underflowed) position
+                if (j >= nv) break;
                 float v4[4];
                 if (tb + j == pos) {
                     const float4 x = *reinterpret_cast<const float4*>(vn + 4 * lane);
@@ -287,24 +345,33 @@ __global__ void __launch_bounds__(A_THREADS, 2) attn_kernel(const AttnArgs a, in
                     v4[0] = x.x; v4[1] = x.y; v4[2] = x.z; v4[3] = x.w;
                 }
 #pragma unroll
-                for (int d = 0; d < 4; ++d) acc[h][d] = fmaf(p[e], v4[d], acc[h][d]);
+                for (int h = 0; h < G; ++h)
+#pragma unroll
+                    for (int d = 0; d < 4; ++d) acc[h][d] = fmaf(ph[h][e], v4[d], acc[h][d]);
+            }
+        } else {
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+                const float ch = pw[h * S::PSTRIDE + PW];
+#pragma unroll
+                for (int d = 0; d < 4; ++d) acc[h][d] *= ch;
             }
         }
+        __syncwarp();
         __syncthreads();   // every warp is done with the slot
         if (tid == 0 && i + A_STAGES < nt) issue(i + A_STAGES);
     }
 
     // ---- merge the 8 warps (the ring is free: all copies were consumed)
     float* ow = reinterpret_cast<float*>(sm);   // [8][G][128]
+    if ((l8 & (8 / G - 1)) == 0 && grp == 0) {   // one lane per head
+        mw[warp * G + hl_own] = m_run[0];
+        lw[warp * G + hl_own] = l_run[0];
+    }
 #pragma unroll
-    for (int h = 0; h < G; ++h) {
-        if (lane == 0) {
-            mw[warp * G + h] = m_run[h];
-            lw[warp * G + h] = l_run[h];
-        }
+    for (int h = 0; h < G; ++h)
         *reinterpret_cast<float4*>(ow + ((size_t)warp * G + h) * HEAD_DIM + 4 * lane) =
             make_float4(acc[h][0], acc[h][1], acc[h][2], acc[h][3]);
-    }
     __syncthreads();
     float* outb = a.out + (size_t)b * a.Hq * HEAD_DIM;
     for (int i = tid; i < G * HEAD_DIM; i += A_THREADS) {
