@@ -274,34 +274,6 @@ fq_status enqueue_step(const Body& b, cudaStream_t s, int kv_bf16, float* x_over
     };
     float* x = x_override ? x_override : w->x;
 
-    // what the next kernel streams, asked of L2 by the current one (weights; this layer's
-    // cached K/V when a layer's worth of it fits L2 comfortably)
-    auto nx_mat = [](const QMat& q, size_t cap = ~(size_t)0) {
-        NextPrefetch nx;
-        if (!q.q) return nx;
-        nx.p[0] = q.q;
-        nx.bytes[0] = std::min((size_t)q.N * q.row_bytes(), cap);
-        if (q.fmt == FMT_Q8_0 && q.s) {
-            nx.p[1] = q.s;
-            nx.bytes[1] = std::min((size_t)q.N * (q.K / 32) * 2, cap / 16);
-        }
-        return nx;
-    };
-    uint32_t cap_kv = 0;
-    for (int i = 0; i < n; ++i) cap_kv = std::max<uint32_t>(cap_kv, (uint32_t)b.chunk * (uint32_t)b.splits);
-    const bool kv_fits = (size_t)n * Hkv * cap_kv * 2 * (kv_bf16 ? 2 : 4) <= ((size_t)48 << 20);
-    auto nx_kv = [&](int L) {
-        NextPrefetch nx;
-        if (!kv_fits) return nx;
-        nx.kv_layer = L;
-        nx.kv_heads = Hkv;
-        nx.kv_elem = kv_bf16 ? 2 : 4;
-        nx.n_seq = n;
-        nx.st = w->st;
-        return nx;
-    };
-    constexpr size_t LM_PREFETCH = (size_t)32 << 20;
-
     // batch 1 of a dense model: the whole step as one persistent kernel
     if (layer_only < 0 && persist_eligible(b)) {
         PersistArgs pa;
@@ -345,7 +317,6 @@ fq_status enqueue_step(const Body& b, cudaStream_t s, int kv_bf16, float* x_over
         g.W = lw.qkv; g.B = n; g.x = x; g.x_stride = H; g.norm_g = lw.attn_norm; g.eps = p.rms_norm_eps;
         g.y = w->qkv; g.y_stride = m->qkv_rows(); g.epi = EPI_STORE;
         g.ksplit = choose_ksplit(g.W, rows_per_warp(g.W));
-        g.next = nx_kv(L);
         proj(g);
 
         AttnArgs a;
@@ -353,13 +324,11 @@ fq_status enqueue_step(const Body& b, cudaStream_t s, int kv_bf16, float* x_over
         a.rope = m->rope; a.eps = p.rms_norm_eps; a.Hq = Hq; a.Hkv = Hkv; a.layer = L; a.kv_bf16 = kv_bf16;
         a.chunk = b.chunk; a.splits = b.splits; a.st = w->st; a.part = w->part; a.counters = w->counters;
         a.out = w->attn; a.n = n; a.err = m->err;
-        a.next = nx_mat(lw.o);
         launch_attention(a, s, pdl());
 
         GemvArgs o;
         o.W = lw.o; o.B = n; o.x = w->attn; o.x_stride = Hq * HEAD_DIM; o.y = x; o.y_stride = H; o.epi = EPI_ADD;
         o.ksplit = choose_ksplit(o.W, rows_per_warp(o.W));
-        o.next = m->moe() ? nx_mat(lw.router) : nx_mat(lw.gate_up);
         proj(o);
 
         if (!m->moe()) {
@@ -367,14 +336,11 @@ fq_status enqueue_step(const Body& b, cudaStream_t s, int kv_bf16, float* x_over
             gu.W = lw.gate_up; gu.B = n; gu.x = x; gu.x_stride = H; gu.norm_g = lw.ffn_norm; gu.eps = p.rms_norm_eps;
             gu.y = w->h; gu.y_stride = p.intermediate_size; gu.epi = EPI_SWIGLU;
             gu.ksplit = choose_ksplit(gu.W, rows_per_warp(gu.W));
-            gu.next = nx_mat(lw.down);
             proj(gu);
 
             GemvArgs dn;
             dn.W = lw.down; dn.B = n; dn.x = w->h; dn.x_stride = p.intermediate_size; dn.y = x; dn.y_stride = H;
             dn.epi = EPI_ADD; dn.ksplit = choose_ksplit(dn.W, rows_per_warp(dn.W));
-            if (L + 1 < L1) dn.next = nx_mat(m->layers[L + 1].qkv);
-            else if (b.logits) dn.next = nx_mat(m->output, LM_PREFETCH);
             proj(dn);
         } else {
             const int E = p.num_experts, k = p.num_experts_used, Fe = p.moe_intermediate_size;

@@ -39,35 +39,6 @@ FQ_DEV void prefetch_l2_range(const void* p, uint64_t bytes, int tid, int nthrea
     }
 }
 
-// This CTA's share (blockIdx.x of gridDim.x) of the bytes the next kernel of the step streams:
-// weight ranges, and for kv_layer >= 0 the cached rows [0, pos) of every kv head of that layer
-// of every sequence.  Starts are rounded up and ends down to 16 bytes; a hint only.
-FQ_DEV void prefetch_share(const void* p, size_t bytes, int tid, int nthreads) {
-    const size_t share = (bytes / gridDim.x + 15) & ~(size_t)15;
-    size_t a = share * blockIdx.x, e = a + share;
-    if (e > bytes) e = bytes;
-    a = (a + 15) & ~(size_t)15;
-    e &= ~(size_t)15;
-    if (e > a) prefetch_l2_range(static_cast<const char*>(p) + a, e - a, tid, nthreads);
-}
-
-FQ_DEV void prefetch_next(const NextPrefetch& nx, int tid, int nthreads) {
-    for (int i = 0; i < 2; ++i)
-        if (nx.p[i] && nx.bytes[i]) prefetch_share(nx.p[i], nx.bytes[i], tid, nthreads);
-    if (nx.kv_layer >= 0 && nx.st) {
-        const StepState* st = nx.st;
-        // one (sequence, kv head, K|V) plane per CTA, round robin
-        const int planes = nx.n_seq * nx.kv_heads * 2;
-        for (int pl = blockIdx.x; pl < planes; pl += gridDim.x) {
-            const int b = pl / (nx.kv_heads * 2), g = (pl / 2) % nx.kv_heads, v = pl & 1;
-            const SeqState& q = st->seq[b];
-            const size_t off = (((size_t)nx.kv_layer * nx.kv_heads + g) * (size_t)q.cap) * HEAD_DIM * nx.kv_elem;
-            const size_t n = (size_t)q.pos * HEAD_DIM * nx.kv_elem;
-            prefetch_l2_range(static_cast<const char*>(v ? q.v : q.k) + off, n & ~(size_t)15, tid, nthreads);
-        }
-    }
-}
-
 // ---------------------------------------------------------------- loads
 // Streaming loads of data read exactly once per step (weights, cache): bypass L1.
 FQ_DEV uint4 ld_stream16(const void* p) {

@@ -68,7 +68,6 @@ struct TcArgs {
     uint32_t* err;
     float* part;         // [grid][2][128][BP] partial sums of split tiles
     uint32_t* tickets;   // [4 * tiles] arrivals per (tile, epilogue warp), zero between uses
-    NextPrefetch next;   // what the next kernel of the step streams
 };
 
 // iterations are (tile, chunk) pairs in tile-major order; total < 2^31 / G is checked on launch
@@ -139,7 +138,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gemm_tc_kernel(const __grid_con
         tmem_relinquish();
     }
     if (tid < 32) best[tid] = 0ull;
-    if (warp >= EPI_WARP0 && warp < MMA_WARP) prefetch_next(a.next, tid - 32 * EPI_WARP0, 128);
     __syncthreads();
     tc_fence_after();
     const uint32_t tbase = *tmem_slot;
@@ -484,7 +482,6 @@ void launch_gemm_tc(const GemvArgs& a, void* xh_v, float* part, size_t part_cap,
     t.err = a.err;
     t.part = part;
     t.tickets = tickets;
-    t.next = a.next;
     if ((size_t)g_sms_tc * 2 * TM * BP > part_cap) {
         if (a.err) cudaMemsetAsync(a.err, 0xFF, sizeof(uint32_t), s);
         return;

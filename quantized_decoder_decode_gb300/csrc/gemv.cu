@@ -60,7 +60,6 @@ __global__ void __launch_bounds__(THREADS) gemv_kernel(const GemvArgs a) {
                 prefetch_l2_range(W.s + (size_t)r0 * (K / 32), ((size_t)nrows * (K / 32) * 2) & ~(size_t)15, tid,
                                   THREADS);
         }
-        prefetch_next(a.next, tid, THREADS);
         pdl_trigger();
         pdl_wait();
     } else {

@@ -101,7 +101,6 @@ __global__ void __launch_bounds__(THREADS_T, 2) gemv_tma_kernel(const __grid_con
         mbar_fence_init();
     }
     if (tid < NBG) best[tid] = 0ull;
-    prefetch_next(a.next, tid, THREADS_T);
     __syncthreads();
     pdl_trigger();
 

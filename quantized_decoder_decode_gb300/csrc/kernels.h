@@ -75,18 +75,6 @@ struct StepState {
 // GEMV / small-batch GEMM on CUDA cores:  y[b][r] (op)= sum_k W[r][k] * xin[b][k]
 enum Epi : int { EPI_STORE = 0, EPI_ADD = 1, EPI_SWIGLU = 2, EPI_LOGITS = 3 };
 
-// Bytes the next kernel of the step will stream (weights, or cached K/V of layer `kv_layer`
-// of every sequence of `st`), asked of L2 by the current kernel's CTAs, each its share.
-struct NextPrefetch {
-    const void* p[2] = {nullptr, nullptr};
-    size_t bytes[2] = {0, 0};
-    int kv_layer = -1;            // >= 0: also the cached K/V rows [0, pos) of that layer
-    int kv_heads = 0;
-    int kv_elem = 0;              // bytes per cached element
-    int n_seq = 0;
-    const struct StepState* st = nullptr;
-};
-
 struct GemvArgs {
     QMat W;
     int B = 1;                    // activation rows
@@ -109,7 +97,6 @@ struct GemvArgs {
     int x_by_pair = 0;            // input row = token*moe_k + slot (else token)
     int max_experts = 0;          // grid.y
     uint32_t* err = nullptr;      // device error word: bit set when a bounded wait gave up
-    NextPrefetch next;            // what the next kernel of the step streams
 };
 
 void launch_gemv(const GemvArgs& a, cudaStream_t s, bool pdl);
@@ -155,7 +142,6 @@ struct AttnArgs {
     float* out;                   // [n][Hq * 128]
     int n;
     uint32_t* err = nullptr;      // device error word (a staged copy that never landed)
-    NextPrefetch next;            // what the next kernel of the step streams
 };
 
 void launch_attention(const AttnArgs& a, cudaStream_t s, bool pdl);
