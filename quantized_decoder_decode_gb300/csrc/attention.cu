@@ -163,7 +163,6 @@ __global__ void __launch_bounds__(A_THREADS, 2) attn_kernel(const AttnArgs a, in
         mbar_fence_init();
         for (int i = 0; i < min(nt, A_STAGES); ++i) issue(i);
     }
-    prefetch_next(a.next, tid, A_THREADS);
     pdl_trigger();
     pdl_wait();
 
