@@ -180,14 +180,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gemm_tc_kernel(const __grid_con
             ahead.next();
             return v;
         };
-        uint32_t sc0 = next_scale(), sc1 = next_scale(), sc2 = next_scale(), sc3 = next_scale();
-        for (int i = 0; i < n_it; ++i) {
-            const uint32_t sc4 = next_scale();
+        // one chunk: wait for its codes and a free A slot, write Wh / Wl; false on a timeout
+        auto convert = [&](int i, uint32_t sc) -> bool {
             const int s = i % RS, as = i % AS;
             if (!mbar_wait(&raw_full[s], (uint32_t)(i / RS) & 1u) ||
                 !mbar_wait(&a_empty[as], ((uint32_t)(i / AS) & 1u) ^ 1u)) {
                 if (a.err && lane == 0) atomicOr(a.err, 4u);
-                break;
+                return false;
             }
             // codes of row rr, logical 16-byte chunks 2h, 2h+1 (64-byte swizzle: chunk ^ bits 1-2 of the row)
             const uint8_t* crow = raw + (size_t)s * RAW_BYTES + rr * 64;
@@ -195,7 +194,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gemm_tc_kernel(const __grid_con
             uint4 q[2];
             q[0] = *reinterpret_cast<const uint4*>(crow + (((2 * h) ^ sw) << 4));
             q[1] = *reinterpret_cast<const uint4*>(crow + (((2 * h + 1) ^ sw) << 4));
-            const unsigned short dbits = (unsigned short)sc0;
+            const unsigned short dbits = (unsigned short)sc;
             const __half dh = *reinterpret_cast<const __half*>(&dbits);
             const __half2 d2 = __halves2half2(dh, dh);
             uint8_t* Ah = At + (size_t)as * 2 * A_TILE;
@@ -219,10 +218,20 @@ __global__ void __launch_bounds__(TC_THREADS, 1) gemm_tc_kernel(const __grid_con
             fence_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(&a_full[as]);
-            sc0 = sc1;
-            sc1 = sc2;
-            sc2 = sc3;
-            sc3 = sc4;
+            return true;
+        };
+        // four scale registers in a static rotation: each is refilled right after its use and
+        // read again four chunks later, so a scale load's latency hides behind three chunks
+        uint32_t sc0 = next_scale(), sc1 = next_scale(), sc2 = next_scale(), sc3 = next_scale();
+        for (int i = 0; i < n_it; i += 4) {
+            if (!convert(i, sc0)) break;
+            sc0 = next_scale();
+            if (i + 1 >= n_it || !convert(i + 1, sc1)) break;
+            sc1 = next_scale();
+            if (i + 2 >= n_it || !convert(i + 2, sc2)) break;
+            sc2 = next_scale();
+            if (i + 3 >= n_it || !convert(i + 3, sc3)) break;
+            sc3 = next_scale();
         }
     } else if (warp == MMA_WARP) {
         // ---------------- MMA issue: one thread
