@@ -99,7 +99,9 @@ __global__ void __launch_bounds__(THREADS) gemv_kernel(const GemvArgs a) {
     const int u_begin = kp * upp, u_end = min(n_units, u_begin + upp);
     const int n_tiles = (W.N + rows_per_cta - 1) / rows_per_cta;
 
-    for (int b0 = 0; b0 < B; b0 += NBG) {
+    // activation rows in groups of NBG: outside expert mode grid.y splits the groups
+    const int g0 = a.route ? 0 : (int)blockIdx.y, gstep = a.route ? 1 : (int)gridDim.y;
+    for (int b0 = g0 * NBG; b0 < B; b0 += NBG * gstep) {
         const int nb = min(NBG, B - b0);
         // ---- prologue: x (times the norm gain) into shared memory, partial sums of x^2
         for (int b = 0; b < nb; ++b) {
@@ -275,7 +277,10 @@ void launch_t(const GemvArgs& a, cudaStream_t s, bool pdl) {
     const int rows = a.route ? a.rows_per_expert : a.W.N;
     const int tiles = (rows + rows_per_cta - 1) / rows_per_cta;
     // one wave of resident CTAs; larger matrices loop over tiles inside each CTA
-    dim3 grid(a.route ? tiles : std::min(tiles, Occ<FMT, R, NBG>::ctas_per_sm * g_sms), a.route ? a.max_experts : 1);
+    // one wave of resident CTAs over (row tiles, activation-row groups)
+    const int groups = a.route ? a.max_experts : (a.B + NBG - 1) / NBG;
+    const int per_group = std::max(1, Occ<FMT, R, NBG>::ctas_per_sm * g_sms / groups);
+    dim3 grid(a.route ? tiles : std::min(tiles, per_group), groups);
     size_t smem = (size_t)NBG * xpad_len<FMT>(a.W.K) * 4 + (FMT == FMT_Q4_K ? (size_t)NBG * (a.W.K / 16) * 4 : 0) +
                   (size_t)(WARPS * R * NBG + WARPS * NBG) * 4;
     auto kern = gemv_kernel<FMT, R, NBG>;
@@ -323,6 +328,8 @@ void gemv_prepare() {
 
 void launch_gemv(const GemvArgs& a, cudaStream_t s, bool pdl) {
     if (!getenv("FQ_NO_TMA") && launch_gemv_tma(a, s, pdl)) return;
+    // expert mode runs the one-row variant: measured faster than four rows per pass at the
+    // usual 1-2 tokens per touched expert
     const bool one = a.B == 1;
     switch (a.W.fmt) {
         case FMT_Q8_0:

@@ -26,13 +26,17 @@ cudaLaunchConfig_t make_cfg(dim3 grid, dim3 block, cudaStream_t s, bool pdl, cud
 
 // One warp per token: k rounds of (max logit, lowest index) over the unselected experts.
 // Selecting on logits equals selecting on softmax probabilities (exp is increasing).
-// Weights: exp(l_j - max) over the selected sum (norm_topk) or over all experts.
+// Weights: exp(l_j - max) over the selected sum (norm_topk) or over all experts.  The grouping
+// of (token, slot) pairs by expert is built in shared memory: counts, an exclusive scan in
+// expert order, then each pair's rank among the earlier pairs of its expert.
 __global__ void __launch_bounds__(256) route_kernel(const float* logits, int E, int k, int n, int norm_topk,
                                                     MoeRoute* rt) {
     pdl_trigger();
     pdl_wait();
     __shared__ int sidx[MAX_SEQ * MAX_TOPK];
     __shared__ int cnt[MAX_EXPERTS];
+    __shared__ int pos_of[MAX_EXPERTS];       // first grouped slot of expert e
+    __shared__ int na_s;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     for (int e = tid; e < E; e += blockDim.x) cnt[e] = 0;
     __syncthreads();
@@ -87,44 +91,66 @@ __global__ void __launch_bounds__(256) route_kernel(const float* logits, int E, 
         }
     }
     __syncthreads();
-    // active experts in ascending id order, with their pair ranges
-    if (tid == 0) {
+    // active experts in ascending id order, with their pair ranges (warp 0: ballot scan)
+    if (warp == 0) {
         int na = 0, off = 0;
-        for (int e = 0; e < E; ++e) {
-            if (cnt[e] == 0) continue;
-            rt->expert[na] = e;
-            rt->start[na] = off;
-            off += cnt[e];
-            ++na;
+        for (int e0 = 0; e0 < E; e0 += 32) {
+            const int e = e0 + lane;
+            const int c = e < E ? cnt[e] : 0;
+            const unsigned act = __ballot_sync(0xFFFFFFFFu, c > 0);
+            int pre = c;   // inclusive scan of the counts over the lanes
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int t = __shfl_up_sync(0xFFFFFFFFu, pre, o);
+                if (lane >= o) pre += t;
+            }
+            if (c > 0) {
+                const int a = na + __popc(act & ((1u << lane) - 1u));
+                rt->expert[a] = e;
+                rt->start[a] = off + pre - c;
+                pos_of[e] = off + pre - c;
+            }
+            na += __popc(act);
+            off += __shfl_sync(0xFFFFFFFFu, pre, 31);
         }
-        rt->start[na] = off;
-        rt->n_active = na;
+        if (lane == 0) {
+            rt->start[na] = off;
+            rt->n_active = na;
+            na_s = na;
+        }
     }
     __syncthreads();
-    // pairs of expert e in (token, slot) order; thread e scans the selections
-    for (int e = tid; e < E; e += blockDim.x) {
-        if (cnt[e] == 0) continue;
-        int a = 0;
-        for (int i = 0; i < E && rt->expert[i] != e; ++i) ++a;   // position of e among active
-        int w = rt->start[a];
-        for (int p = 0; p < n * k; ++p)
-            if (sidx[p] == e) {
-                rt->pair_token[w] = p / k;
-                rt->pair_slot[w] = p % k;
-                ++w;
-            }
+    // pair p goes to its expert's range after the earlier pairs of the same expert
+    for (int p = tid; p < n * k; p += blockDim.x) {
+        const int e = sidx[p];
+        int rank = 0;
+        for (int q = 0; q < p; ++q) rank += sidx[q] == e;
+        const int w = pos_of[e] + rank;
+        rt->pair_token[w] = p / k;
+        rt->pair_slot[w] = p % k;
     }
 }
 
+// x[b][i] += sum_j w[b][j] y[b*k + j][i]; grid (n, column slices of 1024)
 __global__ void __launch_bounds__(256) combine_kernel(float* x, const float* y, const MoeRoute* rt, int k, int H) {
     pdl_trigger();
     pdl_wait();
     const int b = blockIdx.x;
-    for (int i = threadIdx.x; i < H; i += blockDim.x) {
-        float acc = 0.f;
-        for (int j = 0; j < k; ++j) acc = fmaf(rt->w[b * k + j], y[((size_t)b * k + j) * H + i], acc);
-        x[(size_t)b * H + i] += acc;
+    const int i = blockIdx.y * 1024 + 4 * threadIdx.x;
+    if (i >= H) return;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j = 0; j < k; ++j) {
+        const float wj = rt->w[b * k + j];
+        const float4 v = *reinterpret_cast<const float4*>(y + ((size_t)b * k + j) * H + i);
+        acc.x = fmaf(wj, v.x, acc.x);
+        acc.y = fmaf(wj, v.y, acc.y);
+        acc.z = fmaf(wj, v.z, acc.z);
+        acc.w = fmaf(wj, v.w, acc.w);
     }
+    float4* xp = reinterpret_cast<float4*>(x + (size_t)b * H + i);
+    float4 xv = *xp;
+    xv.x += acc.x; xv.y += acc.y; xv.z += acc.z; xv.w += acc.w;
+    *xp = xv;
 }
 
 }  // namespace
@@ -139,7 +165,7 @@ void launch_moe_route(const float* logits, int E, int k, int n, int norm_topk, M
 void launch_moe_combine(float* x, const float* y, const MoeRoute* route, int n, int k, int H, cudaStream_t s,
                         bool pdl) {
     cudaLaunchAttribute attr[1];
-    cudaLaunchConfig_t cfg = make_cfg(dim3(n), dim3(256), s, pdl, attr);
+    cudaLaunchConfig_t cfg = make_cfg(dim3(n, (H + 1023) / 1024), dim3(256), s, pdl, attr);
     cudaLaunchKernelEx(&cfg, combine_kernel, x, y, route, k, H);
 }
 
