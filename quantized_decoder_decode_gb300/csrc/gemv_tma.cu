@@ -295,6 +295,9 @@ bool launch_t(const GemvArgs& a, cudaStream_t s, bool pdl) {
     const size_t smem = TLayout<FMT, NBG>::bytes(a.W.K);
     if (smem > 200 * 1024) return false;
     const int tiles = (a.W.N + C::RT - 1) / C::RT;
+    // fewer row tiles than SMs (the 1024-row O and down projections of small models): the
+    // register-fed kernel, which also splits K inside a CTA, keeps more SMs streaming
+    if (tiles < g_sms_t) return false;
     TmaParams prm;
     prm.maps = *a.W.tm;
     prm.a = a;
