@@ -165,6 +165,42 @@ __global__ void __launch_bounds__(THREADS) gemv_kernel(const GemvArgs a) {
             for (int r = 0; r < R; ++r) row_ok[r] = row_base + r < W.N;
 
             int u = u_begin + lane;
+            if constexpr (FMT == FMT_Q8_0 && NBG > 1) {
+                // several activation rows: each unit's codes become floats once per weight row,
+                // then meet every activation row (read from shared memory as they are used)
+                for (; u < u_end; u += 32) {
+                    Raw rq[R];
+#pragma unroll
+                    for (int r = 0; r < R; ++r)
+                        if (row_ok[r]) rq[r] = load_unit<FMT>(W, row_base + r, u);
+#pragma unroll
+                    for (int r = 0; r < R; ++r) {
+                        if (!row_ok[r]) continue;
+                        float f[16];
+                        s8x4_to_f32(rq[r].q.x, f);
+                        s8x4_to_f32(rq[r].q.y, f + 4);
+                        s8x4_to_f32(rq[r].q.z, f + 8);
+                        s8x4_to_f32(rq[r].q.w, f + 12);
+                        const float d = h2f(rq[r].sc);
+#pragma unroll
+                        for (int b = 0; b < NBG; ++b) {
+                            if (b >= nb) break;
+                            const float4* xp = reinterpret_cast<const float4*>(xs + b * KP + xpad<FMT>(u * 16));
+                            float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                const float4 xv = xp[i];
+                                float& sa = (i & 1) ? s1 : s0;
+                                sa = fmaf(f[4 * i], xv.x, sa);
+                                sa = fmaf(f[4 * i + 1], xv.y, sa);
+                                sa = fmaf(f[4 * i + 2], xv.z, sa);
+                                sa = fmaf(f[4 * i + 3], xv.w, sa);
+                            }
+                            acc[r][b] = fmaf(d, s0 + s1, acc[r][b]);
+                        }
+                    }
+                }
+            } else {
             for (; u + 32 < u_end; u += 64) {
                 Raw r0[R], r1[R];
 #pragma unroll
@@ -202,6 +238,7 @@ __global__ void __launch_bounds__(THREADS) gemv_kernel(const GemvArgs a) {
                             if (row_ok[r]) acc[r][b] += dot_frag<FMT>(r0[r], u, x0, xsum16 + b * (K / 16));
                     }
                 }
+            }
             }
 
             // ---- reduce: lanes, then the K parts of a row group
@@ -328,9 +365,9 @@ void gemv_prepare() {
 
 void launch_gemv(const GemvArgs& a, cudaStream_t s, bool pdl) {
     if (!getenv("FQ_NO_TMA") && launch_gemv_tma(a, s, pdl)) return;
-    // expert mode runs the one-row variant: measured faster than four rows per pass at the
-    // usual 1-2 tokens per touched expert
-    const bool one = a.B == 1;
+    // expert mode: an expert's tokens are only known on the device; the four-row variant reads
+    // and converts each weight once for up to four of them
+    const bool one = a.B == 1 && !(a.route && a.W.fmt == FMT_Q8_0);
     switch (a.W.fmt) {
         case FMT_Q8_0:
             if (one) launch_t<FMT_Q8_0, 4, 1>(a, s, pdl);
