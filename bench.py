@@ -37,9 +37,9 @@ CHAIN = 64
 CONTEXT = 2048
 
 # DRAM bytes (read + write) of one LM-head GEMV launch, from the ncu capture summarised in
-# profiles/gemv_tma_q8_0_lm_head_qwen3-0.6b.md.  Reported only while the kernel's sources
+# profiles/gemv_tma_q8_0_lm_head_qwen3-0.6b.md (its metrics-only recapture).  Reported only while the kernel's sources
 # hash to the value they had when the counters were taken.
-LM_HEAD_TRAFFIC = {"qwen3-0.6b": (169257216, "fe32022265e21c50")}
+LM_HEAD_TRAFFIC = {"qwen3-0.6b": (168251392, "ae06facd60aae183")}
 GEMV_SOURCES = ["gemv_tma.cu", "quant.cuh", "tma.cuh", "common.cuh"]
 
 

@@ -151,6 +151,20 @@ def test_batch_ragged_matches_oracle(pair_factory, dims, ctxs):
         toks = ref.argmax(axis=1)
 
 
+def test_moe_experts_shared_by_many_tokens(pair_factory):
+    """Twelve sequences with the same token over the same cache route identically, so every
+    chosen expert serves all twelve (three four-row passes of the expert GEMV each)."""
+    p = pair_factory(workload(SMALL_MOE, "q8_0", "bf16", seed=34), max_positions=512)
+    kvs, ocs = [], []
+    for _ in range(12):
+        kvc, oc = p.new_seq(capacity=128, ctx=40, seq=0)
+        kvs.append(kvc)
+        ocs.append(oc)
+    got, ref = _compare_step(p, kvs, ocs, [123] * 12, "shared experts")
+    for s in range(1, 12):
+        assert np.array_equal(got[s], got[0]), f"sequence {s} differs from sequence 0"
+
+
 def test_graph_replay_equals_direct_launches(pair_factory):
     p = pair_factory(workload(SMALL_G4, "q8_0", "bf16"), max_positions=512, with_oracle=False)
     a, _ = p.new_seq(capacity=256, ctx=150, seq=0, oracle_cache=False)

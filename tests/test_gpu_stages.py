@@ -69,6 +69,23 @@ def test_weight_gemv_matches_oracle(pair_factory, wtype, n):
             assert_layer_close(got[b], ref, f"gemv which={which} row {b}")
 
 
+@pytest.mark.parametrize("wtype,n", [("q8_0", 1), ("q8_0", 3), ("q4_k", 1), ("q4_k", 3)])
+def test_tma_gemv_many_rows_matches_oracle(pair_factory, wtype, n):
+    """8192 output rows give every SM a row tile, so the TMA-fed kernel serves this matrix
+    (smaller ones go to the register-fed kernel, covered above)."""
+    d = dataclasses.replace(SMALL, vocab_size=8192, hidden_size=512, intermediate_size=1024)
+    p = pair_factory(wl.Workload("gt", d, wtype, "bf16", seed=73), with_oracle=False)
+    x = synth.normal_f32(6, 7, n * d.hidden_size).reshape(n, d.hidden_size)
+    y = torch.empty((n, d.vocab_size), dtype=torch.float32, device=DEV)
+    xt = torch.from_numpy(x).to(DEV)
+    fq.fq_gemv(p.model, 0, fq.W_OUTPUT, n, xt.data_ptr(), y.data_ptr(), stream())
+    torch.cuda.synchronize()
+    got = y.cpu().numpy()
+    for b in range(n):
+        ref = _gemv_ref(wtype, p.W["output"], d.vocab_size, d.hidden_size, x[b].astype(np.float64))
+        assert_layer_close(got[b], ref, f"LM-head rows, activation row {b}")
+
+
 @pytest.mark.parametrize("kv", ["bf16", "f32"])
 def test_layer_stages_match_oracle(pair_factory, kv):
     d = SMALL
