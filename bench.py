@@ -554,6 +554,73 @@ def run_kernel(args):
     return 0
 
 
+def run_verify(args):
+    """forwardStepAllLogits economics, as the qwen3 app page's verify benchmark measures them: one
+    batched k-token pass that scores every position against k single-token steps, for k in
+    {2, 4, 8, 16}, on the chosen workload's model at its context (seeded KV prior)."""
+    import torch
+    import synth.workloads as wl
+    from quantized_decoder_decode_gb300 import fq
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    st = torch.cuda.current_stream(dev)
+    stream = st.cuda_stream
+    w = wl.WORKLOADS[args.workload]
+    d = w.dims
+    ctx = CONTEXT if w.prefill_from_model else int(w.contexts().max())
+    W = wl.make_weights(w)
+    desc = fq.fq_desc_init(vocab_size=d.vocab_size, hidden_size=d.hidden_size, intermediate_size=d.intermediate_size,
+                           num_layers=d.num_layers, num_attention_heads=d.num_attention_heads,
+                           num_key_value_heads=d.num_key_value_heads, head_dim=d.head_dim,
+                           num_experts=d.num_experts, num_experts_used=d.num_experts_used,
+                           moe_intermediate_size=d.moe_intermediate_size, max_positions=ctx + 64)
+    src, keep = fq.weight_src(desc, W, w.weight_dtype)
+    model = fq.fq_load_weights(desc, src, stream)
+    del src, keep
+    kv = fq.fq_kv_init(model, ctx + 32, "bf16")
+    for L in range(d.num_layers):
+        k, v = wl.make_kv_prior(w, 0, L, ctx)
+        kt = torch.from_numpy(k.view(np.int16)).to(dev)
+        vt = torch.from_numpy(v.view(np.int16)).to(dev)
+        fq.fq_kv_append(kv, L, 0, ctx, kt.data_ptr(), vt.data_ptr(), stream)
+    fq.fq_kv_commit(kv, ctx)
+    logits = torch.empty((16, d.vocab_size), dtype=torch.float32, device=dev)
+    ids = [int(t) for t in wl.first_ids(wl.scaled(w, batch=16))] if not w.prefill_from_model else \
+        [int(t) for t in wl.prefill_ids(w)[:16]]
+    reps = max(args.steps, 3)
+
+    def timed(fn):
+        for _ in range(max(args.warmup, 3)):
+            fq.fq_kv_rewind(kv, ctx)
+            fn()
+        torch.cuda.synchronize()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        for a_, b_ in evs:
+            fq.fq_kv_rewind(kv, ctx)
+            a_.record(st)
+            fn()
+            b_.record(st)
+        torch.cuda.synchronize()
+        t = sorted(a_.elapsed_time(b_) * 1e3 for a_, b_ in evs)
+        return t[len(t) // 2], t[0]
+
+    for k in (2, 4, 8, 16):
+        toks = ids[:k]
+        v_med, v_best = timed(lambda: fq.fq_decode_step_all_logits(model, kv, toks, ctx, logits.data_ptr(), stream))
+
+        def singles():
+            for i, t in enumerate(toks):
+                fq.fq_decode_step(model, kv, t, ctx + i, logits[i].data_ptr(), stream)
+        s_med, s_best = timed(singles)
+        print(json.dumps({"kernel": "verify", "workload": w.name, "k": k, "context": ctx,
+                          "verify_us_median": v_med, "verify_us_best": v_best,
+                          "single_steps_us_median": s_med, "single_steps_us_best": s_best,
+                          "speedup_median": s_med / v_med, "verify_tokens_per_s": k / (v_med * 1e-6)}))
+    fq.fq_kv_free(kv)
+    fq.fq_model_free(model)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--kernel", choices=["lm_head", "layer", "proj"], default=None,
@@ -567,7 +634,11 @@ def main():
     ap.add_argument("--impl", default="fq", choices=["fq", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--verify", action="store_true",
+                    help="all-logits verify pass of k tokens against k single steps, k in 2/4/8/16")
     args = ap.parse_args()
+    if args.verify:
+        return run_verify(args)
     if args.kernel:
         return run_kernel(args)
     if args.impl == "reference":

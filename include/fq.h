@@ -168,6 +168,17 @@ fq_status fq_decode_step(const fq_model* m, fq_kv* kv, int32_t token, uint32_t p
 fq_status fq_decode_step_batch(const fq_model* m, fq_kv* const* caches, uint32_t n, const int32_t* tokens,
                                float* logits, void* stream);
 
+/* Section 14.1 forwardStepAllLogits, the verify pass of speculative decoding: the len
+ * tokens (host [len], 1 <= len <= 64) of ONE sequence at positions pos0 .. pos0+len-1 in a
+ * single pass, each attending causally to the cache and to the rows before it; logits of
+ * every row -> device f32 [len][vocab] (caller-owned).  The same KV semantics as forwardStep:
+ * pos0 == len (else INVALID_SEQUENCE_LENGTH, also for len outside 1..64), len + n <=
+ * capacity (else KV_CACHE_OVERFLOW); advances len by len.  The dense trunk reads each weight
+ * once for all rows (the tcgen05 GEMM from 8 rows on).  Equal, up to rounding, to len
+ * consecutive fq_decode_step calls. */
+fq_status fq_decode_step_all_logits(const fq_model* m, fq_kv* kv, const int32_t* tokens, uint32_t len, uint32_t pos0,
+                                    float* logits, void* stream);
+
 /* Greedy generation (section 14.1 generate, without the reset): n_steps decode steps on
  * the device, each feeding back the argmax (ties -> lowest id) of its own logits.
  * Stream s starts from first_tokens[s] (host [n]) at its cache len; tokens_out is device

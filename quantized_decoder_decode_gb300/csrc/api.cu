@@ -239,6 +239,9 @@ struct Body {
     float* layer_out = nullptr;
     int32_t* route_idx = nullptr;
     float* route_w = nullptr;
+    // rows are consecutive positions of one sequence (the all-logits step): every row's new
+    // k/v is appended before any row attends
+    bool block = false;
 };
 
 // Batch 1 of a dense model can run as one persistent kernel (FQ_PERSIST=1).  Off by default:
@@ -324,6 +327,12 @@ fq_status enqueue_step(const Body& b, cudaStream_t s, int kv_bf16, float* x_over
         a.rope = m->rope; a.eps = p.rms_norm_eps; a.Hq = Hq; a.Hkv = Hkv; a.layer = L; a.kv_bf16 = kv_bf16;
         a.chunk = b.chunk; a.splits = b.splits; a.st = w->st; a.part = w->part; a.counters = w->counters;
         a.out = w->attn; a.n = n; a.err = m->err;
+        if (b.block) {
+            AttnArgs ap = a;
+            ap.append_only = 1;
+            launch_attention(ap, s, pdl());
+            a.kv_store = 0;
+        }
         launch_attention(a, s, pdl());
 
         GemvArgs o;
@@ -394,8 +403,9 @@ fq_status enqueue_step(const Body& b, cudaStream_t s, int kv_bf16, float* x_over
     return FQ_OK;
 }
 
+// pos_step = 1: row b sits at position len + b (consecutive positions of one sequence)
 fq_status setup_state(Workspace* w, fq_kv* const* caches, const int32_t* tokens, int n, bool greedy,
-                      int32_t* tokens_out, float* logits, cudaStream_t s) {
+                      int32_t* tokens_out, float* logits, cudaStream_t s, int pos_step = 0) {
     SetupArgs a;
     memset(&a, 0, sizeof a);
     a.n = n;
@@ -404,7 +414,7 @@ fq_status setup_state(Workspace* w, fq_kv* const* caches, const int32_t* tokens,
     a.logits = logits;
     for (int b = 0; b < n; ++b) {
         a.token[b] = tokens ? tokens[b] : 0;
-        a.pos[b] = (int32_t)caches[b]->len;
+        a.pos[b] = (int32_t)caches[b]->len + b * pos_step;
         a.cap[b] = (int32_t)caches[b]->cap;
         a.k[b] = caches[b]->k;
         a.v[b] = caches[b]->v;
@@ -927,6 +937,30 @@ fq_status fq_decode_step_batch(const fq_model* m, fq_kv* const* caches, uint32_t
     attn_split((int)n, m->d.p.num_key_value_heads, cap, b.chunk, b.splits);
     TRY(run_body(b, s, caches[0]->bf16, 1));
     for (uint32_t i = 0; i < n; ++i) caches[i]->len += 1;
+    return FQ_OK;
+}
+
+fq_status fq_decode_step_all_logits(const fq_model* m, fq_kv* kv, const int32_t* tokens, uint32_t len, uint32_t pos0,
+                                    float* logits, void* stream) {
+    if (!m || !kv || !logits) return fail(FQ_ERR_INVALID_ARGUMENT, "null argument");
+    if (kv->m != m) return fail(FQ_ERR_MISMATCHED_KV_CACHES, "cache belongs to another model");
+    if (!m->tok_embd.q || !m->output.q) return fail(FQ_ERR_INVALID_ARGUMENT, "model has no embedding or LM head");
+    if (len == 0 || len > (uint32_t)MAX_SEQ)
+        return fail(FQ_ERR_INVALID_SEQUENCE_LENGTH, "len %u outside 1..%d", len, MAX_SEQ);
+    if (pos0 != kv->len) return fail(FQ_ERR_INVALID_SEQUENCE_LENGTH, "pos0 %u != len %u", pos0, kv->len);
+    if ((uint64_t)kv->len + len > kv->cap)
+        return fail(FQ_ERR_KV_CACHE_OVERFLOW, "len %u + %u > capacity %u", kv->len, len, kv->cap);
+    TRY(check_tokens(m, tokens, len));
+    cudaStream_t s = (cudaStream_t)stream;
+    Workspace* w;
+    TRY(ensure_ws(m, s, (int)len, kv->cap, &w));
+    std::vector<fq_kv*> rows(len, kv);
+    TRY(setup_state(w, rows.data(), tokens, (int)len, false, nullptr, logits, s, 1));
+    Body b{m, w, (int)len, 0, 0, logits, false};
+    b.block = true;
+    attn_split((int)len, m->d.p.num_key_value_heads, kv->cap, b.chunk, b.splits);
+    TRY(enqueue_step(b, s, kv->bf16, nullptr, -1));
+    kv->len += len;
     return FQ_OK;
 }
 

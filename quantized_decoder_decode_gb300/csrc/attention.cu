@@ -22,6 +22,9 @@
 //     registers of two CTAs per SM.
 //   * Partial (m, l, o) per chunk; the last CTA of a (sequence, kv head) to finish (atomic
 //     ticket, no waiting) merges the chunks and writes the head outputs.
+// A step over several positions of one sequence (the all-logits step) runs the kernel twice:
+// an append-only pass writes every row's new k/v, then the full pass reads them as cached rows
+// (no store), so each row sees the rows before it.
 // The ring's waits are bounded: a copy that never lands sets the error word instead of
 // hanging the kernel.
 
@@ -158,7 +161,10 @@ __global__ void __launch_bounds__(A_THREADS, 2) attn_kernel(const AttnArgs a, in
             bulk_g2s(slot + TILE * S::ROW, Vc + (size_t)tb * HEAD_DIM, (uint32_t)(nr * S::ROW), &full[i % A_STAGES]);
         }
     };
-    if (tid == 0) {
+    // append-only pass (rows of one sequence in one step): just the new k/v of the chunk's owner
+    const bool append_only = a.append_only != 0;
+    if (append_only && s != n_act - 1) return;
+    if (tid == 0 && !append_only) {
         for (int i = 0; i < A_STAGES; ++i) mbar_init(&full[i], 1);
         mbar_fence_init();
         for (int i = 0; i < min(nt, A_STAGES); ++i) issue(i);
@@ -171,7 +177,9 @@ __global__ void __launch_bounds__(A_THREADS, 2) attn_kernel(const AttnArgs a, in
     const float2* rope_row = a.rope + (size_t)pos * (HEAD_DIM / 2);
     const float qscale = LOG2E_A * rsqrtf((float)HEAD_DIM);
     const bool owns_new = (s == n_act - 1);
-    for (int w = warp; w < G + (owns_new ? 2 : 0); w += A_WARPS) {
+    const bool store = a.kv_store != 0 && sub == 0;   // the first CTA of the kv head stores, every one keeps
+    for (int w = append_only ? G : warp; w < G + (owns_new ? 2 : 0); w += append_only ? 1 : A_WARPS) {
+        if (append_only && w - G != warp) continue;     // warps 0 and 1: k and v
         if (w < G) {
             const int h = hq0 + w;
             const float4 raw = __ldcg(reinterpret_cast<const float4*>(qkv + (size_t)h * HEAD_DIM + 4 * lane));
@@ -189,18 +197,19 @@ __global__ void __launch_bounds__(A_THREADS, 2) attn_kernel(const AttnArgs a, in
             if (isk) norm_rope4(v, a.k_norm, rope_row, a.eps, lane);
             float* keep = isk ? kn : vn;
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {   // the first CTA of the kv head stores, every one keeps
+            for (int j = 0; j < 4; ++j) {
                 if constexpr (KVT == 1) {
                     const __nv_bfloat16 hb = __float2bfloat16_rn(v[j]);
-                    if (sub == 0) dst[4 * lane + j] = __bfloat16_as_ushort(hb);
+                    if (store) dst[4 * lane + j] = __bfloat16_as_ushort(hb);
                     keep[4 * lane + j] = __bfloat162float(hb);
                 } else {
-                    if (sub == 0) dst[4 * lane + j] = v[j];
+                    if (store) dst[4 * lane + j] = v[j];
                     keep[4 * lane + j] = v[j];
                 }
             }
         }
     }
+    if (append_only) return;
     __syncthreads();
 
     const int l8 = lane & 7, grp = lane >> 3;

@@ -142,6 +142,8 @@ struct AttnArgs {
     float* out;                   // [n][Hq * 128]
     int n;
     uint32_t* err = nullptr;      // device error word (a staged copy that never landed)
+    int append_only = 0;          // 1: only write the new k/v of each row, no attention
+    int kv_store = 1;             // 0: the new k/v are already in the cache (kept, not stored)
 };
 
 void launch_attention(const AttnArgs& a, cudaStream_t s, bool pdl);

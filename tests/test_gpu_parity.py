@@ -165,6 +165,48 @@ def test_moe_experts_shared_by_many_tokens(pair_factory):
         assert np.array_equal(got[s], got[0]), f"sequence {s} differs from sequence 0"
 
 
+@pytest.mark.parametrize("dims,wtype,rows", [(SMALL, "q8_0", 1), (SMALL, "q8_0", 3), (SMALL, "q8_0", 9),
+                                             (SMALL_G4, "q4_k", 5), (SMALL_MOE, "q8_0", 4), (SMALL_MOE, "q8_0", 12)])
+def test_all_logits_step_matches_sequential_oracle(pair_factory, dims, wtype, rows):
+    """forwardStepAllLogits (section 14.1): the rows' logits equal the oracle's consecutive
+    single-token steps; the cache ends where those steps leave it."""
+    p = pair_factory(workload(dims, wtype, "bf16", seed=35), max_positions=512)
+    ctx = 70                                        # rows cross the 64-position tile boundary
+    kvc, oc = p.new_seq(capacity=128, ctx=ctx, seq=0)
+    toks = [int(t) for t in synth.uniform_i32(35, 5, rows, 0, dims.vocab_size)]
+    logits = torch.empty((rows, dims.vocab_size), dtype=torch.float32, device=DEV)
+    fq.fq_decode_step_all_logits(p.model, kvc, toks, ctx, logits.data_ptr(), stream())
+    torch.cuda.synchronize()
+    assert fq.fq_kv_len(kvc) == ctx + rows
+    got = logits.cpu().numpy()
+    for i, t in enumerate(toks):
+        ref = p.om.decode_step(oc, t, ctx + i)
+        assert_logits_close(got[i], ref, f"row {i}")
+    for L in range(dims.num_layers):
+        k, v = p.read_kv(kvc, L, ctx, rows)
+        kr, vr = oc.read(L, ctx, rows)
+        for got_c, ref_c, name in ((k, kr, "k"), (v, vr, "v")):
+            # stored bf16: a value on a rounding boundary may land one ulp (2^-7 of it) away
+            # on top of the per-layer tolerance of the f32 arithmetic that produced it
+            tol = 2.0 ** -7 * np.abs(ref_c) + 1e-3 * float(np.abs(ref_c).max()) + 1e-4
+            assert np.all(np.abs(got_c - ref_c) <= tol), f"layer {L} appended {name}"
+
+
+def test_all_logits_step_contract(pair_factory):
+    p = pair_factory(workload(SMALL, "q8_0", "bf16", seed=36), max_positions=512, with_oracle=False)
+    kvc, _ = p.new_seq(capacity=16, ctx=10, seq=0, oracle_cache=False)
+    out = torch.empty((70, SMALL.vocab_size), dtype=torch.float32, device=DEV)
+    for toks, pos0, status in [([1, 2], 9, fq.INVALID_SEQUENCE_LENGTH), ([], 10, fq.INVALID_SEQUENCE_LENGTH),
+                               ([1] * 65, 10, fq.INVALID_SEQUENCE_LENGTH), ([1] * 7, 10, fq.KV_CACHE_OVERFLOW),
+                               ([1, SMALL.vocab_size], 10, fq.INVALID_ARGUMENT)]:
+        with pytest.raises(fq.FqError) as e:
+            fq.fq_decode_step_all_logits(p.model, kvc, toks, pos0, out.data_ptr(), stream())
+        assert e.value.status == status, (len(toks), pos0)
+        assert fq.fq_kv_len(kvc) == 10             # a refused step leaves the cache as it was
+    fq.fq_decode_step_all_logits(p.model, kvc, [1] * 6, 10, out.data_ptr(), stream())   # exactly fills it
+    assert fq.fq_kv_len(kvc) == 16
+
+
 def test_graph_replay_equals_direct_launches(pair_factory):
     p = pair_factory(workload(SMALL_G4, "q8_0", "bf16"), max_positions=512, with_oracle=False)
     a, _ = p.new_seq(capacity=256, ctx=150, seq=0, oracle_cache=False)
