@@ -165,7 +165,18 @@ __global__ void __launch_bounds__(THREADS) gemv_kernel(const GemvArgs a) {
             for (int r = 0; r < R; ++r) row_ok[r] = row_base + r < W.N;
 
             int u = u_begin + lane;
-            if constexpr (FMT == FMT_Q8_0 && NBG > 1) {
+            if constexpr (FMT == FMT_Q4_K && NBG > 1) {
+                // several activation rows: each code is turned into a float once per weight row
+                for (; u < u_end; u += 32) {
+                    Raw rq[R];
+#pragma unroll
+                    for (int r = 0; r < R; ++r)
+                        if (row_ok[r]) rq[r] = load_unit<FMT>(W, row_base + r, u);
+#pragma unroll
+                    for (int r = 0; r < R; ++r)
+                        if (row_ok[r]) dot_q4k_rows<NBG>(rq[r], u, xs, KP, xsum16, K / 16, nb, acc[r]);
+                }
+            } else if constexpr (FMT == FMT_Q8_0 && NBG > 1) {
                 // several activation rows: each unit's codes become floats once per weight row,
                 // then meet every activation row (read from shared memory as they are used)
                 for (; u < u_end; u += 32) {

@@ -224,14 +224,23 @@ __global__ void __launch_bounds__(THREADS_T, 2) gemv_tma_kernel(const __grid_con
                             raw[r].q = *reinterpret_cast<const uint4*>(srow + 16 * ul);
                         }
                     }
+                    if constexpr (FMT == FMT_Q4_K && NBG > 1) {
+                        // several activation rows: each code is turned into a float once
 #pragma unroll
-                    for (int b = 0; b < NBG; ++b) {
-                        if (b < a.B) {
-                            XFrag<FMT> xf;
-                            load_x<FMT>(xs + (size_t)b * KP, u, xf);
+                        for (int r = 0; r < C::R; ++r) dot_q4k_rows<NBG>(raw[r], u, xs, KP, xsum16, K / 16, a.B, acc[r]);
+                    } else if constexpr (FMT == FMT_Q8_0 && NBG > 1) {
 #pragma unroll
-                            for (int r = 0; r < C::R; ++r)
-                                acc[r][b] += dot_frag<FMT>(raw[r], u, xf, xsum16 + (size_t)b * (K / 16));
+                        for (int r = 0; r < C::R; ++r) dot_q8_rows<NBG>(raw[r], u, xs, KP, a.B, acc[r]);
+                    } else {
+#pragma unroll
+                        for (int b = 0; b < NBG; ++b) {
+                            if (b < a.B) {
+                                XFrag<FMT> xf;
+                                load_x<FMT>(xs + (size_t)b * KP, u, xf);
+#pragma unroll
+                                for (int r = 0; r < C::R; ++r)
+                                    acc[r][b] += dot_frag<FMT>(raw[r], u, xf, xsum16 + (size_t)b * (K / 16));
+                            }
                         }
                     }
                 }

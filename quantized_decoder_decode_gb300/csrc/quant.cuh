@@ -185,4 +185,89 @@ FQ_DEV float dot_frag(const Raw& r, int u, const XFrag<FMT>& x, const float* xsu
     }
 }
 
+// One Q8_0 unit (16 codes, one scale) against up to NB activation rows: the codes become
+// floats once and meet every row, read from shared memory as it is used.
+template <int NB>
+FQ_DEV void dot_q8_rows(const Raw& r, int u, const float* xs, int KP, int nb, float (&acc)[NB]) {
+    float f[16];
+    s8x4_to_f32(r.q.x, f);
+    s8x4_to_f32(r.q.y, f + 4);
+    s8x4_to_f32(r.q.z, f + 8);
+    s8x4_to_f32(r.q.w, f + 12);
+    const float d = h2f(r.sc);
+#pragma unroll
+    for (int b = 0; b < NB; ++b) {
+        if (b >= nb) break;
+        const float4* xp = reinterpret_cast<const float4*>(xs + (size_t)b * KP + xpad<FMT_Q8_0>(u * 16));
+        float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float4 xv = xp[i];
+            float& sa = (i & 1) ? s1 : s0;
+            sa = fmaf(f[4 * i], xv.x, sa);
+            sa = fmaf(f[4 * i + 1], xv.y, sa);
+            sa = fmaf(f[4 * i + 2], xv.z, sa);
+            sa = fmaf(f[4 * i + 3], xv.w, sa);
+        }
+        acc[b] = fmaf(d, s0 + s1, acc[b]);
+    }
+}
+
+// One Q4_K unit against up to NB activation rows: each code becomes its float (1 + q/128, as
+// in dot_frag) once and meets every row, read from shared memory as it is used.  xs: staged
+// rows with stride KP; xsum16: their per-16 sums with stride K16; adds into acc[0..nb).
+template <int NB>
+FQ_DEV void dot_q4k_rows(const Raw& r, int u, const float* xs, int KP, const float* xsum16, int K16, int nb,
+                         float (&acc)[NB]) {
+    const int c = u & 3;
+    const int e0 = (u >> 2) * 256 + 64 * c;
+    const uint32_t w[8] = {r.q.x, r.q.y, r.q.z, r.q.w, r.q2.x, r.q2.y, r.q2.z, r.q2.w};
+    float slo[NB], shi[NB];
+#pragma unroll
+    for (int b = 0; b < NB; ++b) slo[b] = shi[b] = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const uint32_t lo = (w[i] & 0x0F0F0F0Fu) | 0x80808080u;
+        const uint32_t hi = ((w[i] >> 4) & 0x0F0F0F0Fu) | 0x80808080u;
+        float fl[4], fh[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            fl[j] = __uint_as_float(__byte_perm(lo, 0x3F000000u, 0x7044u | (j << 8)));
+            fh[j] = __uint_as_float(__byte_perm(hi, 0x3F000000u, 0x7044u | (j << 8)));
+        }
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+            if (b >= nb) break;
+            const float4 xl = *reinterpret_cast<const float4*>(xs + (size_t)b * KP + xpad<FMT_Q4_K>(e0 + 4 * i));
+            const float4 xh = *reinterpret_cast<const float4*>(xs + (size_t)b * KP + xpad<FMT_Q4_K>(e0 + 32 + 4 * i));
+            slo[b] = fmaf(fl[0], xl.x, slo[b]); slo[b] = fmaf(fl[1], xl.y, slo[b]);
+            slo[b] = fmaf(fl[2], xl.z, slo[b]); slo[b] = fmaf(fl[3], xl.w, slo[b]);
+            shi[b] = fmaf(fh[0], xh.x, shi[b]); shi[b] = fmaf(fh[1], xh.y, shi[b]);
+            shi[b] = fmaf(fh[2], xh.z, shi[b]); shi[b] = fmaf(fh[3], xh.w, shi[b]);
+        }
+    }
+    const float d = h2f((unsigned short)(r.hdr.x & 0xFFFFu)), dmin = h2f((unsigned short)(r.hdr.x >> 16));
+    const uint32_t W0 = r.hdr.y, W1 = r.hdr.z, W2 = r.hdr.w;
+    uint32_t sc0, mn0, sc1, mn1;
+    if (c < 2) {
+        const uint32_t sh = 16u * c;
+        sc0 = (W0 >> sh) & 63u; sc1 = (W0 >> (sh + 8)) & 63u;
+        mn0 = (W1 >> sh) & 63u; mn1 = (W1 >> (sh + 8)) & 63u;
+    } else {
+        const uint32_t sh = 16u * (c - 2);
+        const uint32_t a = W2 >> sh, b0 = W0 >> sh, b1 = W1 >> sh;
+        sc0 = (a & 15u) | ((b0 >> 2) & 48u); sc1 = ((a >> 8) & 15u) | ((b0 >> 10) & 48u);
+        mn0 = ((a >> 4) & 15u) | ((b1 >> 2) & 48u); mn1 = ((a >> 12) & 15u) | ((b1 >> 10) & 48u);
+    }
+    const float d1 = d * (float)sc0 * 128.f, m1 = dmin * (float)mn0, d2 = d * (float)sc1 * 128.f,
+                m2 = dmin * (float)mn1;
+#pragma unroll
+    for (int b = 0; b < NB; ++b) {
+        if (b >= nb) break;
+        const float* xq = xsum16 + (size_t)b * K16 + (e0 >> 4);
+        const float s_lo = xq[0] + xq[1], s_hi = xq[2] + xq[3];
+        acc[b] += d1 * (slo[b] - s_lo) - m1 * s_lo + d2 * (shi[b] - s_hi) - m2 * s_hi;
+    }
+}
+
 }  // namespace fq
