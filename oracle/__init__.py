@@ -23,6 +23,7 @@ _lib = None
 
 Q8_0, Q4_K, F32 = 0, 1, 2
 WTYPES = {"q8_0": Q8_0, "q4_k": Q4_K}
+KV_TYPES = {"f32": 0, "bf16": 1, "q8_0": 2}
 OK, INVALID_CONFIG, INVALID_SEQUENCE_LENGTH, KV_CACHE_OVERFLOW, MISMATCHED_KV_CACHES, INVALID_ARGUMENT = range(6)
 
 
@@ -45,7 +46,7 @@ def build(force: bool = False) -> str:
 class _Dims(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in ("vocab", "hidden", "ffn", "layers", "n_q", "n_kv", "head_dim")] + \
                [("eps", ctypes.c_double), ("theta", ctypes.c_double)] + \
-               [(n, ctypes.c_int) for n in ("n_exp", "n_used", "moe_ffn", "norm_topk", "wtype", "kv_bf16")]
+               [(n, ctypes.c_int) for n in ("n_exp", "n_used", "moe_ffn", "norm_topk", "wtype", "kv_type")]
 
 
 def lib():
@@ -64,6 +65,8 @@ def lib():
                 "or_dequant_q4_k": ([vp, sz, vp], None), "or_quant_q4_k": ([vp, sz, vp], None),
                 "or_rmsnorm": ([vp, i32, vp, f64, vp], None), "or_rope": ([vp, i32, i32, f64], None),
                 "or_attention": ([vp, vp, vp, i32, i32, sz, vp], None), "or_silu": ([f64], f64),
+                "or_attention_q8": ([vp, vp, vp, i32, i32, sz, vp], None),
+                "or_kv_round_row": ([i32, vp, i32, vp], None),
                 "or_router": ([vp, i32, i32, i32, vp, vp], None), "or_gemv": ([i32, vp, i32, i32, vp, vp], None),
                 "or_validate": ([vp], i32), "or_model_new": ([vp], vp), "or_model_free": ([vp], None),
                 "or_model_set_global": ([vp, vp, vp, vp], None),
@@ -179,6 +182,25 @@ def attention(q: np.ndarray, K: np.ndarray, V: np.ndarray) -> np.ndarray:
     return o
 
 
+def attention_q8(q: np.ndarray, K: np.ndarray, V: np.ndarray) -> np.ndarray:
+    """One head over a q8_0 cache: q [D] f64 (quantised inside), K/V [T, D] dequantised rows."""
+    q = np.ascontiguousarray(q, dtype=np.float64)
+    K = np.ascontiguousarray(K, dtype=np.float32)
+    V = np.ascontiguousarray(V, dtype=np.float32)
+    T, D = K.shape
+    o = np.empty(D, dtype=np.float64)
+    lib().or_attention_q8(_p(q), _p(K), _p(V), T, D, D, _p(o))
+    return o
+
+
+def kv_round_row(kv_dtype: str, x: np.ndarray) -> np.ndarray:
+    """The values a cache of ``kv_dtype`` holds for one row ``x``."""
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    out = np.empty(x.size, dtype=np.float32)
+    lib().or_kv_round_row(KV_TYPES[kv_dtype], _p(x), x.size, _p(out))
+    return out
+
+
 def silu(z: float) -> float:
     return lib().or_silu(z)
 
@@ -212,7 +234,7 @@ def make_dims(dims, wtype: str, kv_dtype: str) -> _Dims:
                  layers=dims.num_layers, n_q=dims.num_attention_heads, n_kv=dims.num_key_value_heads,
                  head_dim=dims.head_dim, eps=dims.rms_norm_eps, theta=dims.rope_theta,
                  n_exp=dims.num_experts, n_used=dims.num_experts_used, moe_ffn=dims.moe_intermediate_size,
-                 norm_topk=int(dims.norm_topk_prob), wtype=WTYPES[wtype], kv_bf16=int(kv_dtype == "bf16"))
+                 norm_topk=int(dims.norm_topk_prob), wtype=WTYPES[wtype], kv_type=KV_TYPES[kv_dtype])
 
 
 def validate(dims, wtype: str = "q8_0", kv_dtype: str = "bf16") -> int:
@@ -311,7 +333,12 @@ class Cache:
             raise OracleError(rc, "or_cache_set_len")
 
     def write(self, layer: int, pos0: int, k: np.ndarray, v: np.ndarray) -> None:
-        """k, v: [n, Hkv, D] float32 values, or uint16 bf16 bit patterns."""
+        """k, v: [n, Hkv, D] float32 values, uint16 bf16 bit patterns, or uint8 ggml Q8_0
+        blocks [n, Hkv, D / 32 * 34] (dequantised here)."""
+        if k.dtype == np.uint8:
+            D = self.model.dims.head_dim
+            k = dequant("q8_0", k, k.size // 34 * 32).reshape(k.shape[0], k.shape[1], D)
+            v = dequant("q8_0", v, v.size // 34 * 32).reshape(v.shape[0], v.shape[1], D)
         k, v = _as_f32(k), _as_f32(v)
         rc = lib().or_cache_write(self._h, layer, pos0, k.shape[0], _p(k), _p(v))
         if rc:

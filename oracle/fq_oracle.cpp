@@ -14,6 +14,10 @@
 //     theta^(-2i/D), angle pos * freq, applied after the per-head q/k RMSNorm;
 //   * attention scale 1/sqrt(D); q head h reads kv head h / (n_q / n_kv);
 //   * the new token's k/v are rounded to the cache dtype before attention reads them;
+//   * a q8_0 cache (runner page, "KV cache"; section 14.2 load specifics) holds each head's
+//     k and v row as ggml Q8_0 blocks of 32 along head_dim, quantised from the f32 values
+//     like weights; its scores use q quantised the same way (the integer q8 x q8 score
+//     path), the 1/sqrt(D) scale applied to the score, and V dequantised;
 //   * SwiGLU h = silu(gate) * up with silu(z) = z / (1 + e^-z);
 //   * MoE: softmax over all router logits, top-k by value with ties to the lower expert
 //     index, selected weights renormalised to sum 1 when norm_topk_prob is set;
@@ -321,6 +325,28 @@ void or_attention(const double* q, const float* K, const float* V, int T, int d,
     for (int i = 0; i < d; ++i) o[i] /= l;
 }
 
+void or_kv_round_row(int kv_type, const double* x, int n, float* out) {
+    if (kv_type == OR_KV_Q8_0) {
+        std::vector<float> f(n);
+        std::vector<uint8_t> blk((size_t)n / Q8_BLK * Q8_BYTES);
+        for (int i = 0; i < n; ++i) f[i] = or_f64_to_f32(x[i]);
+        or_quant_q8_0(f.data(), (size_t)n, blk.data());
+        or_dequant_q8_0(blk.data(), (size_t)n, out);
+    } else if (kv_type == OR_KV_BF16) {
+        for (int i = 0; i < n; ++i) out[i] = (float)or_bf16_to_f64(or_f64_to_bf16(x[i]));
+    } else {
+        for (int i = 0; i < n; ++i) out[i] = or_f64_to_f32(x[i]);
+    }
+}
+
+void or_attention_q8(const double* q, const float* K, const float* V, int T, int d, size_t row_stride,
+                     double* o) {
+    std::vector<float> qf(d);
+    or_kv_round_row(OR_KV_Q8_0, q, d, qf.data());
+    std::vector<double> qd(qf.begin(), qf.end());
+    or_attention(qd.data(), K, V, T, d, row_stride, o);
+}
+
 double or_silu(double z) { return z / (1.0 + std::exp(-z)); }
 
 void or_router(const double* logits, int n_exp, int k, int norm, int* idx, double* w) {
@@ -383,9 +409,13 @@ struct or_cache {
 
 namespace {
 
-float to_cache(const or_model* m, double v) {
-    if (m->d.kv_bf16) return (float)or_bf16_to_f64(or_f64_to_bf16(v));
-    return or_f64_to_f32(v);
+// one head's row of n values as the cache stores it
+void to_cache(const or_model* m, const double* x, int n, float* out) { or_kv_round_row(m->d.kv_type, x, n, out); }
+
+void attend(const or_model* m, const double* q, const float* K, const float* V, int T, size_t row_stride,
+            double* o) {
+    if (m->d.kv_type == OR_KV_Q8_0) or_attention_q8(q, K, V, T, m->d.head_dim, row_stride, o);
+    else or_attention(q, K, V, T, m->d.head_dim, row_stride, o);
 }
 
 // q/k/v for one token: xn -> per-head RMSNorm -> rope (section 14.2: per-head q/k RMSNorm,
@@ -475,6 +505,8 @@ int or_validate(const or_dims* d) {
     if (d->hidden <= 0 || d->layers <= 0 || d->n_q <= 0 || d->n_kv <= 0 || d->head_dim <= 0) return OR_INVALID_CONFIG;
     if (d->n_q % d->n_kv != 0) return OR_INVALID_CONFIG;
     if (d->head_dim % 2 != 0) return OR_INVALID_CONFIG;
+    if (d->kv_type < OR_KV_F32 || d->kv_type > OR_KV_Q8_0) return OR_INVALID_ARGUMENT;
+    if (d->kv_type == OR_KV_Q8_0 && d->head_dim % 32 != 0) return OR_INVALID_CONFIG;   // whole blocks per row
     bool any = d->n_exp || d->n_used || d->moe_ffn, all = d->n_exp && d->n_used && d->moe_ffn;
     if (any && !all) return OR_INVALID_CONFIG;
     if (all && d->n_used > d->n_exp) return OR_INVALID_CONFIG;
@@ -527,13 +559,17 @@ int or_cache_len(const or_cache* c) { return c->len; }
 int or_cache_write(or_cache* c, int layer, int pos0, int n, const float* k, const float* v) {
     const or_dims& d = c->m->d;
     if (layer < 0 || layer >= d.layers || pos0 < 0 || n < 0 || pos0 + n > c->cap) return OR_INVALID_ARGUMENT;
+    std::vector<double> kr(d.head_dim), vr(d.head_dim);
     for (int p = 0; p < n; ++p)
-        for (int h = 0; h < d.n_kv; ++h)
+        for (int h = 0; h < d.n_kv; ++h) {
+            size_t src = ((size_t)p * d.n_kv + h) * d.head_dim;
             for (int i = 0; i < d.head_dim; ++i) {
-                size_t src = ((size_t)p * d.n_kv + h) * d.head_dim + i;
-                c->k[c->idx(layer, h, pos0 + p) + i] = to_cache(c->m, k[src]);
-                c->v[c->idx(layer, h, pos0 + p) + i] = to_cache(c->m, v[src]);
+                kr[i] = k[src + i];
+                vr[i] = v[src + i];
             }
+            to_cache(c->m, kr.data(), d.head_dim, &c->k[c->idx(layer, h, pos0 + p)]);
+            to_cache(c->m, vr.data(), d.head_dim, &c->v[c->idx(layer, h, pos0 + p)]);
+        }
     return OR_OK;
 }
 
@@ -570,16 +606,15 @@ int or_layer_step(const or_model* m, int layer, or_cache* c, int pos, double* x,
     std::vector<double> xn(d.hidden), q(qd), k(kvd), v(kvd), o(qd), dx(d.hidden);
     or_rmsnorm(x, d.hidden, w.attn_norm, d.eps, xn.data());
     qkv_project(m, w, xn.data(), pos, q.data(), k.data(), v.data(), false);
-    for (int h = 0; h < d.n_kv; ++h)
-        for (int i = 0; i < D; ++i) {
-            c->k[c->idx(layer, h, pos) + i] = to_cache(m, k[(size_t)h * D + i]);
-            c->v[c->idx(layer, h, pos) + i] = to_cache(m, v[(size_t)h * D + i]);
-        }
+    for (int h = 0; h < d.n_kv; ++h) {
+        to_cache(m, &k[(size_t)h * D], D, &c->k[c->idx(layer, h, pos)]);
+        to_cache(m, &v[(size_t)h * D], D, &c->v[c->idx(layer, h, pos)]);
+    }
 #pragma omp parallel for schedule(static)
     for (int h = 0; h < d.n_q; ++h) {   // heads are independent outputs
         int g = h / group;
-        or_attention(&q[(size_t)h * D], &c->k[c->idx(layer, g, 0)], &c->v[c->idx(layer, g, 0)], pos + 1, D, D,
-                     &o[(size_t)h * D]);
+        attend(m, &q[(size_t)h * D], &c->k[c->idx(layer, g, 0)], &c->v[c->idx(layer, g, 0)], pos + 1, D,
+               &o[(size_t)h * D]);
     }
     gemv_parallel(d.wtype, w.wo, d.hidden, qd, o.data(), dx.data());
     for (int i = 0; i < d.hidden; ++i) x[i] += dx[i];
@@ -649,9 +684,9 @@ int or_forward_last_logits(const or_model* m, const int* tokens, int n, double* 
             std::vector<double> xn(d.hidden), k(kvd), v(kvd);
             or_rmsnorm(&X[(size_t)p * d.hidden], d.hidden, w.attn_norm, d.eps, xn.data());
             qkv_project(m, w, xn.data(), p, &Q[(size_t)p * qd], k.data(), v.data(), true);
-            for (int i = 0; i < kvd; ++i) {
-                K[(size_t)p * kvd + i] = to_cache(m, k[i]);
-                V[(size_t)p * kvd + i] = to_cache(m, v[i]);
+            for (int h = 0; h < d.n_kv; ++h) {
+                to_cache(m, &k[(size_t)h * D], D, &K[(size_t)p * kvd + (size_t)h * D]);
+                to_cache(m, &v[(size_t)h * D], D, &V[(size_t)p * kvd + (size_t)h * D]);
             }
         }
 #pragma omp parallel for schedule(dynamic)
@@ -659,8 +694,8 @@ int or_forward_last_logits(const or_model* m, const int* tokens, int n, double* 
             std::vector<double> o(qd), dx(d.hidden);
             for (int h = 0; h < d.n_q; ++h) {
                 int g = h / group;
-                or_attention(&Q[(size_t)p * qd + (size_t)h * D], &K[(size_t)g * D], &V[(size_t)g * D], p + 1, D,
-                             (size_t)kvd, &o[(size_t)h * D]);
+                attend(m, &Q[(size_t)p * qd + (size_t)h * D], &K[(size_t)g * D], &V[(size_t)g * D], p + 1,
+                       (size_t)kvd, &o[(size_t)h * D]);
             }
             double* x = &X[(size_t)p * d.hidden];
             gemv_serial(d.wtype, w.wo, d.hidden, qd, o.data(), dx.data());

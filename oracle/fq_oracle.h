@@ -23,13 +23,15 @@ extern "C" {
 #endif
 
 enum { OR_Q8_0 = 0, OR_Q4_K = 1, OR_F32 = 2 };
+/* what a KvCache stores: f32 values, bf16 values, or ggml Q8_0 blocks of 32 along head_dim */
+enum { OR_KV_F32 = 0, OR_KV_BF16 = 1, OR_KV_Q8_0 = 2 };
 
 typedef struct or_dims {
     int vocab, hidden, ffn, layers, n_q, n_kv, head_dim;
     double eps, theta;
     int n_exp, n_used, moe_ffn, norm_topk;
     int wtype;    /* OR_Q8_0 or OR_Q4_K: every linear except the f32 router */
-    int kv_bf16;  /* 1: cache stores bf16 values, 0: f32 values */
+    int kv_type;  /* OR_KV_F32, OR_KV_BF16 or OR_KV_Q8_0 */
 } or_dims;
 
 typedef struct or_model or_model;
@@ -56,6 +58,18 @@ void or_rmsnorm(const double* x, int n, const float* g, double eps, double* y);
 void or_rope(double* v, int d, int pos, double theta);
 void or_attention(const double* q, const float* K, const float* V, int T, int d, size_t row_stride,
                   double* o);
+/* The q8_0-cache form of the above ("integer q8 x q8 score path"): q is rounded to f32 and
+ * quantised to Q8_0 blocks of 32 like a cached row, K and V hold dequantised Q8_0 rows.
+ * Score t = (1/sqrt(d)) sum_b d_q[b] d_k[t][b] sum_i q_i k_i over the integer codes, which
+ * equals the dot product of the dequantised rows; that form is evaluated in f64, where
+ * every product of two dequantised values is exact. */
+void or_attention_q8(const double* q, const float* K, const float* V, int T, int d, size_t row_stride,
+                     double* o);
+/* The values a cache of kv_type holds for a row x of n values (one head's k or v): f32 or
+ * bf16 rounding of each value; for Q8_0 each value is rounded to f32 (the precision the
+ * quantiser's decisions are taken in), then each block of 32 is quantised (or_quant_q8_0)
+ * and dequantised.  n % 32 == 0 for Q8_0. */
+void or_kv_round_row(int kv_type, const double* x, int n, float* out);
 double or_silu(double z);
 void or_router(const double* logits, int n_exp, int k, int norm, int* idx, double* w);
 /* y[r] = sum_c W[r,c] x[c] over a packed [rows, cols] matrix (wtype OR_Q8_0/OR_Q4_K/OR_F32) */
@@ -75,9 +89,9 @@ void or_model_set_layer(or_model* m, int layer, const float* attn_norm, const vo
 or_cache* or_cache_new(const or_model* m, int capacity);
 void or_cache_free(or_cache* c);
 int  or_cache_len(const or_cache* c);
-/* write n prior positions of one layer (values in the cache dtype, given as f32; bf16
- * caches round them again, which is the identity for bf16 inputs) and set len = pos0+n
- * once every layer holds them; returns 0 or an error code */
+/* write n prior positions of one layer (values in the cache dtype, given as f32: bf16
+ * caches round them again, Q8_0 caches quantise each row again, which is the identity for
+ * dequantised Q8_0 rows); returns 0 or an error code */
 int  or_cache_write(or_cache* c, int layer, int pos0, int n, const float* k, const float* v);
 int  or_cache_set_len(or_cache* c, int len);
 /* read back [n][n_kv][head_dim] of one layer */

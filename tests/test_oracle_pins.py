@@ -243,6 +243,86 @@ def test_attention_special_cases():
     np.testing.assert_allclose(oracle.attention(q, K[perm], V[perm]), oracle.attention(q, K, V), rtol=1e-13)
 
 
+# ---------------------------------------------------------------- q8_0 KV cache
+
+def _q8_block_scale(x32: np.ndarray) -> float:
+    """fp16 of amax / 127 for one block of f32 values (numpy's float16 conversion)."""
+    return float(np.float16(np.abs(x32.astype(np.float64)).max() / 127.0))
+
+
+def test_q8_cache_row_holds_whole_codes_of_the_fp16_block_scale():
+    x = RNG.normal(0, 1, 256) * np.repeat([1e-3, 1.0, 30.0, 0.2, 5.0, 1e-6, 7.0, 0.5], 32)
+    r = oracle.kv_round_row("q8_0", x).astype(np.float64)
+    xf = x.astype(np.float32).astype(np.float64)
+    for b in range(8):
+        d = _q8_block_scale(xf[32 * b:32 * b + 32])
+        if d == 0.0:                     # amax / 127 below half the smallest fp16: zero block
+            assert b == 5 and np.all(r[32 * b:32 * b + 32] == 0)
+            continue
+        codes = r[32 * b:32 * b + 32] / d
+        assert np.array_equal(codes, np.round(codes)) and np.abs(codes).max() <= 127
+        assert np.abs(xf[32 * b:32 * b + 32] - r[32 * b:32 * b + 32]).max() <= d / 2
+    # quantising a cached row again changes nothing
+    assert np.array_equal(oracle.kv_round_row("q8_0", r), r.astype(np.float32))
+
+
+def test_q8_cache_blocks_are_independent_and_zero_blocks_stay_zero():
+    x = RNG.normal(0, 1, 128)
+    x[32:64] = 0.0
+    r = oracle.kv_round_row("q8_0", x)
+    assert np.all(r[32:64] == 0)
+    y = x.copy()
+    y[96:128] *= 50.0
+    ry = oracle.kv_round_row("q8_0", y)
+    assert np.array_equal(ry[:96], r[:96]) and not np.array_equal(ry[96:], r[96:])
+
+
+def test_q8_cache_ties_round_away_and_decisions_are_taken_in_f32():
+    d = 2.0 ** -4
+    x = np.zeros(32)
+    x[0] = 127 * d                       # sets the scale to d exactly
+    x[1], x[2], x[3], x[4] = 3.5 * d, -3.5 * d, 2.25 * d, -0.5 * d
+    # just below the tie in f64, but the f32 rounding of the value lands on the tie
+    x[5] = 5.5 * d - 2.0 ** -40
+    r = oracle.kv_round_row("q8_0", x) / d
+    assert list(r[:6]) == [127, 4, -4, 2, -1, 6]
+
+
+def test_q8_attention_equals_the_integer_score_path():
+    D, T = 128, 37
+    q = RNG.normal(0, 1, D)
+    kc = RNG.integers(-127, 128, (T, D)).astype(np.int64)
+    vc = RNG.integers(-127, 128, (T, D)).astype(np.int64)
+    kd = np.float16(RNG.uniform(0.005, 0.03, (T, D // 32))).astype(np.float64)
+    vd = np.float16(RNG.uniform(0.005, 0.03, (T, D // 32))).astype(np.float64)
+    K = (kc * np.repeat(kd, 32, axis=1)).astype(np.float32)
+    V = (vc * np.repeat(vd, 32, axis=1)).astype(np.float32)
+    qb = oracle.quant("q8_0", q.astype(np.float32)).reshape(D // 32, 34)
+    qdd = qb[:, :2].copy().view(np.float16).astype(np.float64).ravel()
+    qc = qb[:, 2:].view(np.int8).astype(np.int64)
+    # integer dot per block, then the two fp16 scales, then 1/sqrt(D)
+    isum = np.einsum("bi,tbi->tb", qc, kc.reshape(T, D // 32, 32))
+    s = (isum * qdd[None, :] * kd).sum(1) / math.sqrt(D)
+    p = np.exp(s - s.max())
+    ref = (p[:, None] * V.astype(np.float64)).sum(0) / p.sum()
+    np.testing.assert_allclose(oracle.attention_q8(q, K, V), ref, rtol=1e-12, atol=1e-14)
+
+
+def test_q8_attention_ignores_changes_of_q_inside_its_codes():
+    D = 64
+    K = oracle.kv_round_row("q8_0", RNG.normal(0, 1, 8 * D)).reshape(8, D)
+    V = oracle.kv_round_row("q8_0", RNG.normal(0, 1, 8 * D)).reshape(8, D)
+    q = RNG.normal(0, 1, D)
+    q[0], q[32] = 3.0, -3.0                  # block maxima stay put
+    base = oracle.attention_q8(q, K, V)
+    nudged = q.copy()
+    nudged[1:32] += 1e-7                     # far inside the code cells (step 3/127)
+    assert np.array_equal(oracle.attention_q8(nudged, K, V), base)
+    assert not np.array_equal(oracle.attention(nudged, K, V), oracle.attention(q, K, V))
+    # a single position returns its (dequantised) value row exactly
+    assert np.array_equal(oracle.attention_q8(q, K[:1], V[:1]), V[0].astype(np.float64))
+
+
 def test_silu_matches_torch():
     z = RNG.normal(0, 4, 200)
     ref = torch.nn.functional.silu(torch.from_numpy(z)).numpy()
@@ -301,7 +381,11 @@ def tiny_model(dims=TINY, wtype="q8_0", kv="bf16", seed=5):
     return oracle.Model(dims, W, wtype, kv), W, dims, hid
 
 
-@pytest.mark.parametrize("dims,wtype,kv", [(TINY, "q8_0", "bf16"), (TINY, "q4_k", "f32"), (TINY_MOE, "q8_0", "bf16")])
+TINY_Q8KV = dataclasses.replace(TINY, head_dim=32)   # whole Q8_0 blocks per cached row
+
+
+@pytest.mark.parametrize("dims,wtype,kv", [(TINY, "q8_0", "bf16"), (TINY, "q4_k", "f32"), (TINY_MOE, "q8_0", "bf16"),
+                                           (TINY_Q8KV, "q8_0", "q8_0")])
 def test_no_cache_logits_equal_cached_prefill_then_step(dims, wtype, kv):
     m, _, d, _ = tiny_model(dims, wtype, kv)
     toks = synth.uniform_i32(9, 1, 7, 0, d.vocab_size)
@@ -339,6 +423,23 @@ def test_cache_holds_bf16_values_after_step():
     k, v = c.read(1, 0, 1)
     assert np.all((k.view(np.uint32) & 0xFFFF) == 0) and np.all((v.view(np.uint32) & 0xFFFF) == 0)
     assert np.any(k != 0)
+
+
+def test_q8_cache_holds_quantised_rows_after_step():
+    m, _, d, _ = tiny_model(TINY_Q8KV, kv="q8_0")
+    mf, _, _, _ = tiny_model(TINY_Q8KV, kv="f32")
+    c, cf = m.new_cache(4), mf.new_cache(4)
+    for p, t in enumerate([3, 17]):
+        m.decode_step(c, t, p, logits=False)
+        mf.decode_step(cf, t, p, logits=False)
+    k, v = c.read(0, 0, 2)          # layer 0 saw identical inputs in both models
+    kf, vf = cf.read(0, 0, 2)
+    for got, exact in ((k, kf), (v, vf)):
+        assert np.array_equal(got.ravel(), oracle.kv_round_row("q8_0", exact.ravel().astype(np.float64)))
+    # the q8_0 cache perturbs the step by the size of its rounding, not more
+    lq = m.decode_step(c, 5, 2)
+    lf = mf.decode_step(cf, 5, 2)
+    assert 0 < np.abs(lq - lf).max() <= 2e-2 * np.abs(lf).max()
 
 
 def _zeros_like_packed(a):
@@ -403,9 +504,15 @@ def test_gqa_grouping_uses_consecutive_q_heads():
     wo[:, D:2 * D] = np.eye(H, D)          # x[r] += o_head1[r] for r < D
     lw["wo"] = synth.pack_q8_0(wo).reshape(H, -1)
     lw["w_down"] = np.zeros_like(lw["w_down"])
+    # the new position's value row is W_v xn with xn = rmsnorm(e_0) = sqrt(H) g_0 e_0: make it
+    # about +1 for kv head 0 and -1 for kv head 1 as well, so no softmax weight can flip the sign
+    wv = np.zeros((d.kv_dim, H), dtype=np.float32)
+    wv[:D, 0] = 1.0 / (math.sqrt(H) * lw["attn_norm"][0])
+    wv[D:, 0] = -wv[0, 0]
+    lw["wv"] = synth.pack_q8_0(wv).reshape(d.kv_dim, -1)
     m = oracle.Model(d, W, "q8_0", "f32")
     c = m.new_cache(8)
-    K = RNG.normal(0, 1, (5, d.num_key_value_heads, D)).astype(np.float32)
+    K = np.random.default_rng(77).normal(0, 1, (5, d.num_key_value_heads, D)).astype(np.float32)
     V = np.ones((5, d.num_key_value_heads, D), dtype=np.float32)
     V[:, 1, :] = -1
     c.write(0, 0, K, V)
@@ -414,8 +521,7 @@ def test_gqa_grouping_uses_consecutive_q_heads():
     x0[0] = 1.0
     x1, _, _ = m.layer_step(0, c, 5, x0)
     delta = (x1 - x0)[:D]
-    # head 1's own value row at the new position is W_v xn, not +1, so allow for its share
-    assert np.all(delta > 0.5), delta
+    assert np.all(delta > 0.9), delta
 
 
 def test_validation_rejects_bad_configs():
@@ -426,6 +532,9 @@ def test_validation_rejects_bad_configs():
            dataclasses.replace(TINY_MOE, num_experts_used=7)]
     for b in bad:
         assert oracle.validate(b) == oracle.INVALID_CONFIG, b
+    # a q8_0 cache stores whole blocks of 32 per row
+    assert oracle.validate(TINY, kv_dtype="q8_0") == oracle.INVALID_CONFIG
+    assert oracle.validate(dataclasses.replace(TINY, head_dim=32), kv_dtype="q8_0") == oracle.OK
 
 
 def test_step_contract_errors():
