@@ -67,6 +67,25 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
+KV_ELEM_BYTES = {"f32": 4.0, "bf16": 2.0, "q8_0": 34 / 32}   # per cached value (Q8_0: codes + fp16 scale)
+
+
+def workload_of(args):
+    """The named workload, with its cache dtype replaced when --kv asks for another."""
+    import dataclasses
+    import synth.workloads as wl
+    w = wl.WORKLOADS[args.workload]
+    if getattr(args, "kv", None) and args.kv != w.kv_dtype:
+        w = dataclasses.replace(w, kv_dtype=args.kv)
+    return w
+
+
+def kv_tensor(a: np.ndarray, dev):
+    """Prior cache rows as a device tensor of their raw bytes (bf16 bits, f32, Q8_0 blocks)."""
+    import torch
+    return torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a).to(dev)
+
+
 def step_bytes(dims, ctx: int) -> dict:
     """Algorithmic bytes of one batch-1 decode step at `ctx` cached positions."""
     q8 = 34 / 32
@@ -309,7 +328,7 @@ def run_fq(args):
     dev = torch.device("cuda", torch.cuda.current_device())
     st = torch.cuda.current_stream(dev)
     stream = st.cuda_stream
-    w = wl.WORKLOADS[args.workload]
+    w = workload_of(args)
     d = w.dims
     n = w.batch
     chain = w.steps
@@ -340,8 +359,7 @@ def run_fq(args):
         for s_i, (kv, c) in enumerate(zip(kvs, ctxs)):
             for L in range(d.num_layers):
                 k, v = wl.make_kv_prior(w, s_i, L, c)
-                kt = torch.from_numpy(k.view(np.int16)).to(dev)
-                vt = torch.from_numpy(v.view(np.int16)).to(dev)
+                kt, vt = kv_tensor(k, dev), kv_tensor(v, dev)
                 fq.fq_kv_append(kv, L, 0, c, kt.data_ptr(), vt.data_ptr(), stream)
             fq.fq_kv_commit(kv, c)
         torch.cuda.synchronize()
@@ -432,8 +450,9 @@ def run_fq(args):
     achieved = kbytes / kt / 1e9
 
     wb = weight_bytes(w, experts)
-    kv_read = sum(2 * d.num_layers * d.kv_dim * (c + (chain - 1) / 2) * 2 for c in ctxs)
-    kv_write = n * 2 * d.num_layers * d.kv_dim * 2
+    eb = KV_ELEM_BYTES[w.kv_dtype]
+    kv_read = sum(2 * d.num_layers * d.kv_dim * (c + (chain - 1) / 2) * eb for c in ctxs)
+    kv_write = n * 2 * d.num_layers * d.kv_dim * eb
     total = wb["layers"] + wb["lm_head"] + wb["embedding_rows"] + kv_read + kv_write
     step_gbs = total / (dt / args.steps) / 1e9
     # kernels inside the timed region: each step replays one captured graph; each chain adds
@@ -490,7 +509,7 @@ def run_kernel(args):
     dev = torch.device("cuda", 0)
     st = torch.cuda.current_stream(dev)
     stream = st.cuda_stream
-    w = wl.WORKLOADS[args.workload]
+    w = workload_of(args)
     d = w.dims
     ctx = CONTEXT if w.prefill_from_model else int(w.contexts().max())
     w1 = wl.scaled(w, num_layers=1)
@@ -525,10 +544,9 @@ def run_kernel(args):
         nbytes = sum(r * c * bpw + 4 * n * (r + c) for _, r, c in mats)
         flops = 2 * n * sum(r * c for _, r, c in mats)
     else:
-        kv = fq.fq_kv_init(model, ctx + 1, "bf16")
+        kv = fq.fq_kv_init(model, ctx + 1, w.kv_dtype)
         k, v = wl.make_kv_prior(w1, 0, 0, ctx)
-        kt = torch.from_numpy(k.view(np.int16)).to(dev)
-        vt = torch.from_numpy(v.view(np.int16)).to(dev)
+        kt, vt = kv_tensor(k, dev), kv_tensor(v, dev)
         fq.fq_kv_append(kv, 0, 0, ctx, kt.data_ptr(), vt.data_ptr(), stream)
         fq.fq_kv_commit(kv, ctx)
         x = torch.from_numpy(wl.layer_input(w1)).to(dev)
@@ -565,7 +583,7 @@ def run_verify(args):
     dev = torch.device("cuda", 0)
     st = torch.cuda.current_stream(dev)
     stream = st.cuda_stream
-    w = wl.WORKLOADS[args.workload]
+    w = workload_of(args)
     d = w.dims
     ctx = CONTEXT if w.prefill_from_model else int(w.contexts().max())
     W = wl.make_weights(w)
@@ -577,11 +595,10 @@ def run_verify(args):
     src, keep = fq.weight_src(desc, W, w.weight_dtype)
     model = fq.fq_load_weights(desc, src, stream)
     del src, keep
-    kv = fq.fq_kv_init(model, ctx + 32, "bf16")
+    kv = fq.fq_kv_init(model, ctx + 32, w.kv_dtype)
     for L in range(d.num_layers):
         k, v = wl.make_kv_prior(w, 0, L, ctx)
-        kt = torch.from_numpy(k.view(np.int16)).to(dev)
-        vt = torch.from_numpy(v.view(np.int16)).to(dev)
+        kt, vt = kv_tensor(k, dev), kv_tensor(v, dev)
         fq.fq_kv_append(kv, L, 0, ctx, kt.data_ptr(), vt.data_ptr(), stream)
     fq.fq_kv_commit(kv, ctx)
     logits = torch.empty((16, d.vocab_size), dtype=torch.float32, device=dev)
@@ -634,6 +651,8 @@ def main():
     ap.add_argument("--impl", default="fq", choices=["fq", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--kv", default=None, choices=["bf16", "q8_0"],
+                    help="cache dtype in place of the workload's own (q8_0: the integer-score cache)")
     ap.add_argument("--verify", action="store_true",
                     help="all-logits verify pass of k tokens against k single steps, k in 2/4/8/16")
     args = ap.parse_args()

@@ -124,15 +124,21 @@ fq_status fq_load_weights(const fq_desc* d, const fq_weight_src* src, void* stre
 void fq_model_free(fq_model* m);
 
 /* KvCache (section 14.2 initKvCache; uniform geometry layers x kv heads x head_dim x
- * capacity) in device memory owned by the cache, dtype FQ_F32 or FQ_BF16, len = 0.
- * Layout: [layer][kv_head][capacity][head_dim] for K and again for V. */
+ * capacity) in device memory owned by the cache, len = 0.  dtype FQ_F32, FQ_BF16 or FQ_Q8_0
+ * (the runner page's q8_0 cache: half the bf16 bytes; decode scores it through the integer
+ * q8 x q8 path, q quantised to Q8_0 blocks like a cached row).  Layout: [layer][kv_head]
+ * [capacity][head_dim] values for K and again for V; Q8_0 stores int8 codes in that layout
+ * and, after them, [layer][kv_head][capacity rounded up to even][head_dim / 32] fp16 block
+ * scales.  New rows are quantised with ggml's Q8_0 rule (d = fp16(amax / 127), codes x / d
+ * rounded half away from zero), the same as fq_quantize_q8_0. */
 fq_status fq_kv_init(const fq_model* m, uint32_t capacity, fq_dtype kv_dtype, fq_kv** out);
 void fq_kv_free(fq_kv* kv);
 uint32_t fq_kv_len(const fq_kv* kv);
 uint32_t fq_kv_capacity(const fq_kv* kv);
 
 /* Bulk-write positions [pos, pos+n_pos) of one layer: k, v are device [n_pos][kv_heads]
- * [head_dim] in the cache dtype.  pos must equal the cache's len (contiguous fill),
+ * [head_dim] in the cache dtype (Q8_0: ggml blocks, [n_pos][kv_heads][head_dim / 32] of 34
+ * bytes each, any alignment).  pos must equal the cache's len (contiguous fill),
  * pos + n_pos <= capacity.  Does not change len; fq_kv_commit(kv, len) sets it once every
  * layer holds the positions (len <= capacity, len >= current len).  Errors:
  * INVALID_SEQUENCE_LENGTH (pos != len), KV_CACHE_OVERFLOW, INVALID_ARGUMENT. */
@@ -143,7 +149,8 @@ fq_status fq_kv_commit(fq_kv* kv, uint32_t len);
  * cache capabilities): len <= current len, else INVALID_SEQUENCE_LENGTH.  Positions from
  * len on keep stale contents until later steps overwrite them.  Host-side only. */
 fq_status fq_kv_rewind(fq_kv* kv, uint32_t len);
-/* Copy positions [pos, pos+n_pos) of one layer out to device buffers in the cache dtype. */
+/* Copy positions [pos, pos+n_pos) of one layer out to device buffers in the cache dtype
+ * (Q8_0: ggml blocks as fq_kv_append takes them). */
 fq_status fq_kv_read(const fq_kv* kv, uint32_t layer, uint32_t pos, uint32_t n_pos, void* k, void* v,
                      void* stream);
 
@@ -215,6 +222,13 @@ typedef enum fq_weight_id {
  * decoding the GEMV kernels use. */
 fq_status fq_dequant_rows(const fq_model* m, uint32_t layer, fq_weight_id which, uint64_t row0, uint64_t n_rows,
                           float* out, void* stream);
+
+/* ggml Q8_0 blocks (34 bytes per 32 values) of x[0, n) with the device quantiser a Q8_0
+ * KvCache applies to q and to new k/v rows (runner page, "KV cache"): d = fp16(amax / 127)
+ * rounded to nearest even, codes x / d rounded half away from zero and clamped to +-127, zero
+ * when d is 0.  x: device f32, 16-byte aligned, n a multiple of 128; blocks: device, n / 32 * 34
+ * bytes.  Errors: INVALID_ARGUMENT. */
+fq_status fq_quantize_q8_0(const float* x, uint64_t n, void* blocks, void* stream);
 
 /* y[b][r] = sum_k W[r][k] x[b][k] for b < n (n <= 64) over one device-resident weight, with
  * the launch configuration the decode step uses: x device f32 [n][cols], y device f32

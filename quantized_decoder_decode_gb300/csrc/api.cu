@@ -89,10 +89,13 @@ struct fq_model {
 struct fq_kv {
     const fq_model* m = nullptr;
     uint32_t cap = 0, len = 0;
-    int bf16 = 1;
-    void* k = nullptr;
+    int type = KV_BF16;            // KvType
+    void* k = nullptr;             // [layer][kv head][cap][128] values or Q8_0 codes
     void* v = nullptr;
-    size_t elem() const { return bf16 ? 2 : 4; }
+    void* ks = nullptr;            // Q8_0: [layer][kv head][cap_s()][4] fp16 scales, inside the k
+    void* vs = nullptr;            //   and v allocations after the codes
+    size_t elem() const { return type == KV_F32 ? 4 : type == KV_BF16 ? 2 : 1; }
+    size_t cap_s() const { return (cap + 1) & ~1u; }   // even, so scale rows pair into 16 bytes
 };
 
 // Per-stream scratch and captured graphs (the pages' ExecContext: one per concurrent stream).
@@ -110,7 +113,7 @@ struct Workspace {
     MoeRoute* route = nullptr;
     std::vector<void*> allocs;
     struct Graph {
-        int mode, n, chunk, splits, kv_bf16;
+        int mode, n, chunk, splits, kv_type;
         float* logits;
         cudaGraphExec_t exec;
         uint32_t kernels;      // kernel nodes in the captured step
@@ -247,14 +250,14 @@ struct Body {
 // Batch 1 of a dense model can run as one persistent kernel (FQ_PERSIST=1).  Off by default:
 // measured on GB300 its grid barriers (about 2.4 us each, 5 per layer) cost more than the
 // launches of the captured kernel sequence they replace.
-bool persist_eligible(const Body& b) {
+bool persist_eligible(const Body& b, int kv_type) {
     static const bool persist = env_flag("FQ_PERSIST");
-    return b.n == 1 && !b.m->moe() && b.m->players && !b.layer_out && !b.route_idx && persist;
+    return b.n == 1 && !b.m->moe() && b.m->players && !b.layer_out && !b.route_idx && kv_type != KV_Q8_0 && persist;
 }
 
 // The kernels of one decode step, in order.  The first launch follows the set-up kernel
 // with ordinary stream order; every later one uses programmatic dependent launch.
-fq_status enqueue_step(const Body& b, cudaStream_t s, int kv_bf16, float* x_override, int layer_only) {
+fq_status enqueue_step(const Body& b, cudaStream_t s, int kv_type, float* x_override, int layer_only) {
     const fq_model* m = b.m;
     Workspace* w = b.w;
     const auto& p = m->d.p;
@@ -278,7 +281,7 @@ fq_status enqueue_step(const Body& b, cudaStream_t s, int kv_bf16, float* x_over
     float* x = x_override ? x_override : w->x;
 
     // batch 1 of a dense model: the whole step as one persistent kernel
-    if (layer_only < 0 && persist_eligible(b)) {
+    if (layer_only < 0 && persist_eligible(b, kv_type)) {
         PersistArgs pa;
         pa.layers = m->players;
         pa.n_layers = (int)p.num_layers;
@@ -293,7 +296,7 @@ fq_status enqueue_step(const Body& b, cudaStream_t s, int kv_bf16, float* x_over
         pa.out_norm = m->output_norm;
         AttnArgs& a = pa.at;
         a.qkv = w->qkv; a.qkv_stride = m->qkv_rows(); a.q_norm = nullptr; a.k_norm = nullptr;
-        a.rope = m->rope; a.eps = p.rms_norm_eps; a.Hq = Hq; a.Hkv = Hkv; a.layer = 0; a.kv_bf16 = kv_bf16;
+        a.rope = m->rope; a.eps = p.rms_norm_eps; a.Hq = Hq; a.Hkv = Hkv; a.layer = 0; a.kv_type = kv_type;
         a.chunk = b.chunk; a.splits = b.splits; a.st = w->st; a.part = w->part; a.counters = w->counters;
         a.out = w->attn; a.n = 1;
         pa.x = x;
@@ -324,7 +327,7 @@ fq_status enqueue_step(const Body& b, cudaStream_t s, int kv_bf16, float* x_over
 
         AttnArgs a;
         a.qkv = w->qkv; a.qkv_stride = m->qkv_rows(); a.q_norm = lw.q_norm; a.k_norm = lw.k_norm;
-        a.rope = m->rope; a.eps = p.rms_norm_eps; a.Hq = Hq; a.Hkv = Hkv; a.layer = L; a.kv_bf16 = kv_bf16;
+        a.rope = m->rope; a.eps = p.rms_norm_eps; a.Hq = Hq; a.Hkv = Hkv; a.layer = L; a.kv_type = kv_type;
         a.chunk = b.chunk; a.splits = b.splits; a.st = w->st; a.part = w->part; a.counters = w->counters;
         a.out = w->attn; a.n = n; a.err = m->err;
         if (b.block) {
@@ -418,6 +421,8 @@ fq_status setup_state(Workspace* w, fq_kv* const* caches, const int32_t* tokens,
         a.cap[b] = (int32_t)caches[b]->cap;
         a.k[b] = caches[b]->k;
         a.v[b] = caches[b]->v;
+        a.ks[b] = caches[b]->ks;
+        a.vs[b] = caches[b]->vs;
     }
     launch_setup(w->st, a, s);
     CK(cudaGetLastError());
@@ -425,18 +430,18 @@ fq_status setup_state(Workspace* w, fq_kv* const* caches, const int32_t* tokens,
 }
 
 // Run (capture once, replay) the step body for `reps` consecutive steps.
-fq_status run_body(const Body& b, cudaStream_t s, int kv_bf16, int reps) {
+fq_status run_body(const Body& b, cudaStream_t s, int kv_type, int reps) {
     Workspace* w = b.w;
     const int mode = b.greedy ? MODE_GREEDY : MODE_DECODE;
     // one persistent kernel per step needs no graph (and a cooperative launch is not captured)
-    if (env_flag("FQ_NO_GRAPH") || b.layer_out || b.route_idx || persist_eligible(b)) {
-        for (int r = 0; r < reps; ++r) TRY(enqueue_step(b, s, kv_bf16, nullptr, -1));
-        w->last_kernels = persist_eligible(b) ? 1u : 0u;
+    if (env_flag("FQ_NO_GRAPH") || b.layer_out || b.route_idx || persist_eligible(b, kv_type)) {
+        for (int r = 0; r < reps; ++r) TRY(enqueue_step(b, s, kv_type, nullptr, -1));
+        w->last_kernels = persist_eligible(b, kv_type) ? 1u : 0u;
         return FQ_OK;
     }
     cudaGraphExec_t exec = nullptr;
     for (auto& g : w->graphs)
-        if (g.mode == mode && g.n == b.n && g.chunk == b.chunk && g.splits == b.splits && g.kv_bf16 == kv_bf16 &&
+        if (g.mode == mode && g.n == b.n && g.chunk == b.chunk && g.splits == b.splits && g.kv_type == kv_type &&
             g.logits == b.logits) {
             exec = g.exec;
             w->last_kernels = g.kernels;
@@ -450,7 +455,7 @@ fq_status run_body(const Body& b, cudaStream_t s, int kv_bf16, int reps) {
             cudaStreamDestroy(cs);
             return fail(FQ_ERR_CUDA, "cudaStreamBeginCapture: %s", cudaGetErrorString(e));
         }
-        fq_status st = enqueue_step(b, cs, kv_bf16, nullptr, -1);
+        fq_status st = enqueue_step(b, cs, kv_type, nullptr, -1);
         e = cudaStreamEndCapture(cs, &graph);
         cudaStreamDestroy(cs);
         if (st != FQ_OK) return st;
@@ -468,7 +473,7 @@ fq_status run_body(const Body& b, cudaStream_t s, int kv_bf16, int reps) {
         e = cudaGraphInstantiate(&exec, graph, 0);
         cudaGraphDestroy(graph);
         if (e != cudaSuccess) return fail(FQ_ERR_CUDA, "cudaGraphInstantiate: %s", cudaGetErrorString(e));
-        w->graphs.push_back({mode, b.n, b.chunk, b.splits, kv_bf16, b.logits, exec, kernels});
+        w->graphs.push_back({mode, b.n, b.chunk, b.splits, kv_type, b.logits, exec, kernels});
         w->last_kernels = kernels;
     }
     for (int r = 0; r < reps; ++r) CK(cudaGraphLaunch(exec, s));
@@ -483,7 +488,7 @@ fq_status check_caches(const fq_model* m, fq_kv* const* caches, uint32_t n, uint
     for (uint32_t s = 0; s < n; ++s) {
         if (!caches[s]) return fail(FQ_ERR_INVALID_ARGUMENT, "cache %u is null", s);
         if (caches[s]->m != m) return fail(FQ_ERR_MISMATCHED_KV_CACHES, "cache %u belongs to another model", s);
-        if (caches[s]->bf16 != caches[0]->bf16) return fail(FQ_ERR_MISMATCHED_KV_CACHES, "cache dtypes differ");
+        if (caches[s]->type != caches[0]->type) return fail(FQ_ERR_MISMATCHED_KV_CACHES, "cache dtypes differ");
         for (uint32_t t = 0; t < s; ++t)
             if (caches[t] == caches[s]) return fail(FQ_ERR_MISMATCHED_KV_CACHES, "cache %u repeated", s);
         if ((uint64_t)caches[s]->len + steps > caches[s]->cap)
@@ -823,12 +828,16 @@ fq_status fq_kv_init(const fq_model* m, uint32_t capacity, fq_dtype kv_dtype, fq
     if (capacity == 0) return fail(FQ_ERR_INVALID_ARGUMENT, "zero capacity");
     if (capacity > (uint32_t)m->max_pos)
         return fail(FQ_ERR_INVALID_ARGUMENT, "capacity %u exceeds max_positions %d", capacity, m->max_pos);
-    if (kv_dtype != FQ_F32 && kv_dtype != FQ_BF16) return fail(FQ_ERR_INVALID_ARGUMENT, "kv dtype must be F32 or BF16");
+    if (kv_dtype != FQ_F32 && kv_dtype != FQ_BF16 && kv_dtype != FQ_Q8_0)
+        return fail(FQ_ERR_INVALID_ARGUMENT, "kv dtype must be F32, BF16 or Q8_0");
     fq_kv* kv = new fq_kv();
     kv->m = m;
     kv->cap = capacity;
-    kv->bf16 = kv_dtype == FQ_BF16;
-    size_t bytes = (size_t)m->d.p.num_layers * m->d.p.num_key_value_heads * capacity * HEAD_DIM * kv->elem();
+    kv->type = kv_dtype == FQ_F32 ? KV_F32 : kv_dtype == FQ_BF16 ? KV_BF16 : KV_Q8_0;
+    const size_t heads = (size_t)m->d.p.num_layers * m->d.p.num_key_value_heads;
+    const size_t vbytes = heads * capacity * HEAD_DIM * kv->elem();
+    const size_t sbytes = kv->type == KV_Q8_0 ? heads * kv->cap_s() * (HEAD_DIM / 32) * 2 : 0;
+    size_t bytes = vbytes + sbytes;
     cudaError_t e1 = cudaMalloc(&kv->k, bytes);
     cudaError_t e2 = e1 == cudaSuccess ? cudaMalloc(&kv->v, bytes) : e1;
     if (e1 != cudaSuccess || e2 != cudaSuccess) {
@@ -839,6 +848,10 @@ fq_status fq_kv_init(const fq_model* m, uint32_t capacity, fq_dtype kv_dtype, fq
     }
     cudaMemset(kv->k, 0, bytes);
     cudaMemset(kv->v, 0, bytes);
+    if (sbytes) {
+        kv->ks = (char*)kv->k + vbytes;   // vbytes is a multiple of 128
+        kv->vs = (char*)kv->v + vbytes;
+    }
     *out = kv;
     return FQ_OK;
 }
@@ -858,6 +871,15 @@ static fq_status kv_copy(const fq_kv* kv, uint32_t layer, uint32_t pos, uint32_t
     const auto& p = kv->m->d.p;
     const size_t es = kv->elem(), row = HEAD_DIM * es, Hkv = p.num_key_value_heads;
     cudaStream_t s = (cudaStream_t)stream;
+    if (kv->type == KV_Q8_0) {   // ggml blocks [n_pos][Hkv][4][34] <-> code and scale planes
+        const size_t lc = (size_t)layer * Hkv * kv->cap * HEAD_DIM, ls = (size_t)layer * Hkv * kv->cap_s() * 4;
+        launch_kv_q8_copy((int8_t*)kv->k + lc, (uint16_t*)kv->ks + ls, kv->cap, kv->cap_s(), (int)Hkv, (int)pos,
+                          (int)n_pos, (uint8_t*)k, to_cache, s);
+        launch_kv_q8_copy((int8_t*)kv->v + lc, (uint16_t*)kv->vs + ls, kv->cap, kv->cap_s(), (int)Hkv, (int)pos,
+                          (int)n_pos, (uint8_t*)v, to_cache, s);
+        CK(cudaGetLastError());
+        return FQ_OK;
+    }
     for (size_t h = 0; h < Hkv; ++h) {
         size_t coff = (((size_t)layer * Hkv + h) * kv->cap + pos) * row;
         char* ck = (char*)kv->k + coff;
@@ -921,7 +943,7 @@ fq_status fq_layer_step(const fq_model* m, uint32_t layer, fq_kv* kv, uint32_t p
     TRY(setup_state(w, caches, nullptr, 1, false, nullptr, nullptr, s));
     Body b{m, w, 1, 0, 0, nullptr, false};
     attn_split(1, m->d.p.num_key_value_heads, kv->cap, b.chunk, b.splits);
-    return enqueue_step(b, s, kv->bf16, x, (int)layer);
+    return enqueue_step(b, s, kv->type, x, (int)layer);
 }
 
 fq_status fq_decode_step_batch(const fq_model* m, fq_kv* const* caches, uint32_t n, const int32_t* tokens,
@@ -935,7 +957,7 @@ fq_status fq_decode_step_batch(const fq_model* m, fq_kv* const* caches, uint32_t
     TRY(setup_state(w, caches, tokens, (int)n, false, nullptr, logits, s));
     Body b{m, w, (int)n, 0, 0, logits, false};
     attn_split((int)n, m->d.p.num_key_value_heads, cap, b.chunk, b.splits);
-    TRY(run_body(b, s, caches[0]->bf16, 1));
+    TRY(run_body(b, s, caches[0]->type, 1));
     for (uint32_t i = 0; i < n; ++i) caches[i]->len += 1;
     return FQ_OK;
 }
@@ -959,7 +981,7 @@ fq_status fq_decode_step_all_logits(const fq_model* m, fq_kv* kv, const int32_t*
     Body b{m, w, (int)len, 0, 0, logits, false};
     b.block = true;
     attn_split((int)len, m->d.p.num_key_value_heads, kv->cap, b.chunk, b.splits);
-    TRY(enqueue_step(b, s, kv->bf16, nullptr, -1));
+    TRY(enqueue_step(b, s, kv->type, nullptr, -1));
     kv->len += len;
     return FQ_OK;
 }
@@ -985,7 +1007,7 @@ fq_status fq_decode_greedy(const fq_model* m, fq_kv* const* caches, uint32_t n, 
     TRY(setup_state(w, caches, first_tokens, (int)n, true, tokens_out, lg, s));
     Body b{m, w, (int)n, 0, 0, lg, true};
     attn_split((int)n, m->d.p.num_key_value_heads, cap, b.chunk, b.splits);
-    TRY(run_body(b, s, caches[0]->bf16, (int)n_steps));
+    TRY(run_body(b, s, caches[0]->type, (int)n_steps));
     for (uint32_t i = 0; i < n; ++i) caches[i]->len += n_steps;
     return FQ_OK;
 }
@@ -1003,7 +1025,7 @@ fq_status fq_decode_step_trace(const fq_model* m, fq_kv* const* caches, uint32_t
     TRY(setup_state(w, caches, tokens, (int)n, false, nullptr, logits, s));
     Body b{m, w, (int)n, 0, 0, logits, false, layer_out, route_idx, route_w};
     attn_split((int)n, m->d.p.num_key_value_heads, cap, b.chunk, b.splits);
-    TRY(enqueue_step(b, s, caches[0]->bf16, nullptr, -1));
+    TRY(enqueue_step(b, s, caches[0]->type, nullptr, -1));
     for (uint32_t i = 0; i < n; ++i) caches[i]->len += 1;
     return FQ_OK;
 }
@@ -1069,6 +1091,15 @@ fq_status fq_check_device(const fq_model* m, void* stream) {
         CK(cudaMemsetAsync(m->err, 0, sizeof(uint32_t), s));
         return fail(FQ_ERR_DEVICE_TIMEOUT, "a bounded device wait gave up (code %u)", host);
     }
+    return FQ_OK;
+}
+
+fq_status fq_quantize_q8_0(const float* x, uint64_t n, void* blocks, void* stream) {
+    if (!x || !blocks) return fail(FQ_ERR_INVALID_ARGUMENT, "null argument");
+    if (n % 128) return fail(FQ_ERR_INVALID_ARGUMENT, "n = %llu is not a multiple of 128", (unsigned long long)n);
+    if ((uintptr_t)x % 16) return fail(FQ_ERR_INVALID_ARGUMENT, "x is not 16-byte aligned");
+    launch_quantize_q8_0(x, (size_t)n, (uint8_t*)blocks, (cudaStream_t)stream);
+    CK(cudaGetLastError());
     return FQ_OK;
 }
 
@@ -1220,5 +1251,5 @@ extern "C" fq_status fq_layer_step_noalloc(const fq_model* m, uint32_t layer, fq
     fq_kv* caches[1] = {kv};
     TRY(setup_state(&w, caches, nullptr, 1, false, nullptr, nullptr, s));
     Body body{m, &w, 1, chunk, splits, nullptr, false};
-    return enqueue_step(body, s, kv->bf16, x, (int)layer);
+    return enqueue_step(body, s, kv->type, x, (int)layer);
 }

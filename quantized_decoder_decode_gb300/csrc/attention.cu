@@ -22,6 +22,11 @@
 //     registers of two CTAs per SM.
 //   * Partial (m, l, o) per chunk; the last CTA of a (sequence, kv head) to finish (atomic
 //     ticket, no waiting) merges the chunks and writes the head outputs.
+// A q8_0 cache holds each row as 128 int8 codes plus four fp16 block scales (separate planes,
+// both staged per tile).  Its scores take the integer q8 x q8 path the runner page names for
+// that cache: q is quantised to Q8_0 blocks like a cached row, each lane forms 16-code
+// integer dot products (dp4a) and scales them by d_q d_k; V rows are dequantised as they are
+// accumulated.  The new k and v are quantised before they are stored and used.
 // A step over several positions of one sequence (the all-logits step) runs the kernel twice:
 // an append-only pass writes every row's new k/v, then the full pass reads them as cached rows
 // (no store), so each row sees the rows before it.
@@ -46,16 +51,21 @@ constexpr float LOG2E_A = 1.4426950408889634f;
 template <int KVT> struct KvT;
 template <> struct KvT<0> { using T = float; static constexpr int TILE = 32; };
 template <> struct KvT<1> { using T = uint16_t; static constexpr int TILE = 64; };
+template <> struct KvT<2> { using T = int8_t; static constexpr int TILE = 64; };   // Q8_0 codes
 
 template <int KVT, int G>
 struct ASmem {
     using T = typename KvT<KVT>::T;
     static constexpr int TILE = KvT<KVT>::TILE;
     static constexpr int ROW = HEAD_DIM * (int)sizeof(T);        // bytes per cached row
-    static constexpr int SLOT = 2 * TILE * ROW;                   // K tile | V tile
+    static constexpr int SROW = KVT == 2 ? 8 : 0;                 // Q8_0: four fp16 block scales
+    static constexpr int KPART = TILE * (ROW + SROW);             // codes/values, then scales
+    static constexpr int SLOT = 2 * KPART;                        // K tile | V tile
     // ring first (16-byte aligned slots); the warps' final merge reuses it
-    static constexpr int OFF_Q = A_STAGES * SLOT;                 // float4 q[G][4][8] (piece, lane group)
-    static constexpr int OFF_KN = OFF_Q + G * HEAD_DIM * 4;       // float kn[128], vn[128]
+    static constexpr int OFF_Q = A_STAGES * SLOT;                 // float4 q[G][4][8] (piece, lane group);
+                                                                  // Q8_0: u32 codes[G][32], float d[G][4]
+    static constexpr int OFF_KN = OFF_Q + G * HEAD_DIM * 4;       // float kn[128], vn[128]; Q8_0: kn =
+                                                                  // u32 codes[32], float d[4]
     static constexpr int OFF_ML = OFF_KN + 2 * HEAD_DIM * 4;      // float mw[8][G], lw[8][G]
     static constexpr int OFF_P = (OFF_ML + 2 * A_WARPS * G * 4 + 15) & ~15;   // float pw[8][G][TILE/8 + 4]
     static constexpr int PSTRIDE = TILE / A_WARPS + 4;            // probabilities of a head, then its rescale
@@ -146,19 +156,31 @@ __global__ void __launch_bounds__(A_THREADS, 2) attn_kernel(const AttnArgs a, in
     if (s >= n_act) return;
     const int t0 = s * a.chunk, t1 = min(T_len, t0 + a.chunk);
     const int nt = (t1 - t0 + TILE - 1) / TILE;
-    const size_t head_off = ((size_t)a.layer * a.Hkv + g) * (size_t)ss.cap * HEAD_DIM;
+    const size_t head_row0 = (size_t)a.layer * a.Hkv + g;
+    const size_t head_off = head_row0 * (size_t)ss.cap * HEAD_DIM;
     const T* Kc = reinterpret_cast<const T*>(ss.k) + head_off;
     const T* Vc = reinterpret_cast<const T*>(ss.v) + head_off;
+    // Q8_0 scale planes [layer][kv head][cap rounded up to even][4] fp16 (16-byte aligned rows
+    // pairs, so a tile's scales are one bulk copy)
+    const size_t sc_off = head_row0 * (size_t)((ss.cap + 1) & ~1) * 4;
+    const uint16_t* Ksc = reinterpret_cast<const uint16_t*>(ss.ks) + sc_off;
+    const uint16_t* Vsc = reinterpret_cast<const uint16_t*>(ss.vs) + sc_off;
 
     // ---- cached rows (written by earlier steps) go out first
     auto issue = [&](int i) {
         const int tb = t0 + i * TILE;
         const int nr = max(0, min(tb + TILE, pos) - tb);   // cached rows of the tile (pos excluded)
         uint8_t* slot = sm + (size_t)(i % A_STAGES) * S::SLOT;
-        mbar_arrive_expect_tx(&full[i % A_STAGES], (uint32_t)(2 * nr * S::ROW));
+        // scales go in pairs of rows (16 bytes); an odd count ends at row pos, inside the plane
+        const uint32_t sbytes = KVT == 2 ? (uint32_t)(((nr + 1) & ~1) * S::SROW) : 0u;
+        mbar_arrive_expect_tx(&full[i % A_STAGES], (uint32_t)(2 * nr * S::ROW) + 2 * sbytes);
         if (nr > 0) {
             bulk_g2s(slot, Kc + (size_t)tb * HEAD_DIM, (uint32_t)(nr * S::ROW), &full[i % A_STAGES]);
-            bulk_g2s(slot + TILE * S::ROW, Vc + (size_t)tb * HEAD_DIM, (uint32_t)(nr * S::ROW), &full[i % A_STAGES]);
+            bulk_g2s(slot + S::KPART, Vc + (size_t)tb * HEAD_DIM, (uint32_t)(nr * S::ROW), &full[i % A_STAGES]);
+            if constexpr (KVT == 2) {
+                bulk_g2s(slot + TILE * S::ROW, Ksc + (size_t)tb * 4, sbytes, &full[i % A_STAGES]);
+                bulk_g2s(slot + S::KPART + TILE * S::ROW, Vsc + (size_t)tb * 4, sbytes, &full[i % A_STAGES]);
+            }
         }
     };
     // append-only pass (rows of one sequence in one step): just the new k/v of the chunk's owner
@@ -185,9 +207,18 @@ __global__ void __launch_bounds__(A_THREADS, 2) attn_kernel(const AttnArgs a, in
             const float4 raw = __ldcg(reinterpret_cast<const float4*>(qkv + (size_t)h * HEAD_DIM + 4 * lane));
             float v[4] = {raw.x, raw.y, raw.z, raw.w};
             norm_rope4(v, a.q_norm, rope_row, a.eps, lane);
-            // dims 4 lane..4 lane+3 = piece ((lane / 2) >= 8 ? 2 : 0) + (lane & 1) of lane group (lane / 2) % 8
-            const int dim0 = 4 * lane, half = dim0 >= 64, grp8 = (dim0 % 64) / 8, piece = 2 * half + ((dim0 / 4) & 1);
-            qp[(w * 4 + piece) * 8 + grp8] = make_float4(v[0] * qscale, v[1] * qscale, v[2] * qscale, v[3] * qscale);
+            if constexpr (KVT == 2) {
+                // q as Q8_0 blocks: codes of dims 4 lane..4 lane+3, block scale per 8 lanes
+                unsigned short db;
+                float d;
+                const uint32_t code4 = q8_quant_lane4(v, db, d);
+                reinterpret_cast<uint32_t*>(sm + S::OFF_Q)[w * 32 + lane] = code4;
+                if ((lane & 7) == 0) reinterpret_cast<float*>(sm + S::OFF_Q + G * 128)[w * 4 + (lane >> 3)] = d;
+            } else {
+                // dims 4 lane..4 lane+3 = piece ((lane / 2) >= 8 ? 2 : 0) + (lane & 1) of lane group (lane / 2) % 8
+                const int dim0 = 4 * lane, half = dim0 >= 64, grp8 = (dim0 % 64) / 8, piece = 2 * half + ((dim0 / 4) & 1);
+                qp[(w * 4 + piece) * 8 + grp8] = make_float4(v[0] * qscale, v[1] * qscale, v[2] * qscale, v[3] * qscale);
+            }
         } else {
             const bool isk = w == G;
             T* dst = const_cast<T*>(isk ? Kc : Vc) + (size_t)pos * HEAD_DIM;
@@ -196,15 +227,34 @@ __global__ void __launch_bounds__(A_THREADS, 2) attn_kernel(const AttnArgs a, in
             float v[4] = {raw.x, raw.y, raw.z, raw.w};
             if (isk) norm_rope4(v, a.k_norm, rope_row, a.eps, lane);
             float* keep = isk ? kn : vn;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                if constexpr (KVT == 1) {
-                    const __nv_bfloat16 hb = __float2bfloat16_rn(v[j]);
-                    if (store) dst[4 * lane + j] = __bfloat16_as_ushort(hb);
-                    keep[4 * lane + j] = __bfloat162float(hb);
+            if constexpr (KVT == 2) {
+                unsigned short db;
+                float d;
+                const uint32_t code4 = q8_quant_lane4(v, db, d);
+                if (store) {
+                    reinterpret_cast<uint32_t*>(dst)[lane] = code4;
+                    if ((lane & 7) == 0) const_cast<uint16_t*>(isk ? Ksc : Vsc)[(size_t)pos * 4 + (lane >> 3)] = db;
+                }
+                if (isk) {
+                    reinterpret_cast<uint32_t*>(kn)[lane] = code4;
+                    if ((lane & 7) == 0) kn[32 + (lane >> 3)] = d;
                 } else {
-                    if (store) dst[4 * lane + j] = v[j];
-                    keep[4 * lane + j] = v[j];
+                    float f[4];
+                    s8x4_to_f32(code4, f);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) vn[4 * lane + j] = f[j] * d;
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    if constexpr (KVT == 1) {
+                        const __nv_bfloat16 hb = __float2bfloat16_rn(v[j]);
+                        if (store) dst[4 * lane + j] = __bfloat16_as_ushort(hb);
+                        keep[4 * lane + j] = __bfloat162float(hb);
+                    } else {
+                        if (store) dst[4 * lane + j] = v[j];
+                        keep[4 * lane + j] = v[j];
+                    }
                 }
             }
         }
@@ -214,10 +264,20 @@ __global__ void __launch_bounds__(A_THREADS, 2) attn_kernel(const AttnArgs a, in
 
     const int l8 = lane & 7, grp = lane >> 3;
     float4 qr[G][4];
+    uint4 qw[G];           // Q8_0: codes of dims 16 l8..16 l8+15 and the scale of their block
+    float qdl[G];
+    if constexpr (KVT == 2) {
 #pragma unroll
-    for (int h = 0; h < G; ++h)
+        for (int h = 0; h < G; ++h) {
+            qw[h] = reinterpret_cast<const uint4*>(sm + S::OFF_Q)[h * 8 + l8];
+            qdl[h] = reinterpret_cast<const float*>(sm + S::OFF_Q + G * 128)[h * 4 + (l8 >> 1)];
+        }
+    } else {
 #pragma unroll
-        for (int pc = 0; pc < 4; ++pc) qr[h][pc] = qp[(h * 4 + pc) * 8 + l8];
+        for (int h = 0; h < G; ++h)
+#pragma unroll
+            for (int pc = 0; pc < 4; ++pc) qr[h][pc] = qp[(h * 4 + pc) * 8 + l8];
+    }
     // online softmax state of the lane's head (all lanes holding a head agree) and the V
     // accumulators of every head for dims 4 lane..4 lane+3
     float m_run[1] = {-INFINITY}, l_run[1] = {0.f}, acc[G][4];
@@ -231,7 +291,7 @@ __global__ void __launch_bounds__(A_THREADS, 2) attn_kernel(const AttnArgs a, in
         const int st = i % A_STAGES;
         if (!mbar_wait(&full[st], (uint32_t)(i / A_STAGES) & 1u) && lane == 0 && a.err) atomicOr(a.err, 128u);
         const uint8_t* Kt = sm + (size_t)st * S::SLOT;
-        const uint8_t* Vt = Kt + TILE * S::ROW;
+        const uint8_t* Vt = Kt + S::KPART;
         const int tb = t0 + i * TILE;
         const int nv = min(TILE, t1 - tb);
         const int jw = warp * PW;                      // this warp's positions jw..jw+PW-1
@@ -244,6 +304,31 @@ __global__ void __launch_bounds__(A_THREADS, 2) attn_kernel(const AttnArgs a, in
         for (int r = 0; r < PW / 4; ++r) {
             const int j = jw + 4 * r + grp;
             const bool valid = j < nv;
+            if constexpr (KVT == 2) {
+                // integer dot of 16 codes per lane, scaled by d_q d_k of their block
+                uint4 kw = make_uint4(0u, 0u, 0u, 0u);
+                float dk = 0.f;
+                if (tb + j == pos) {
+                    kw = reinterpret_cast<const uint4*>(kn)[l8];
+                    dk = kn[32 + (l8 >> 1)];
+                } else if (valid) {
+                    kw = *reinterpret_cast<const uint4*>(Kt + j * S::ROW + 16 * l8);
+                    dk = h2f(reinterpret_cast<const unsigned short*>(Kt + TILE * S::ROW)[j * 4 + (l8 >> 1)]);
+                }
+                float dd[G];
+#pragma unroll
+                for (int h = 0; h < G; ++h) {
+                    int acc = __dp4a((int)kw.x, (int)qw[h].x, 0);
+                    acc = __dp4a((int)kw.y, (int)qw[h].y, acc);
+                    acc = __dp4a((int)kw.z, (int)qw[h].z, acc);
+                    acc = __dp4a((int)kw.w, (int)qw[h].w, acc);
+                    dd[h] = (float)acc * (qdl[h] * dk);
+                }
+                const float sc = reduce8<G>(dd, l8, hl) * qscale;
+                hl_own = hl;
+                sr[r] = valid ? sc : -INFINITY;
+                continue;
+            }
             float kf[16];
             if (tb + j == pos) {
 #pragma unroll
@@ -345,6 +430,12 @@ __global__ void __launch_bounds__(A_THREADS, 2) attn_kernel(const AttnArgs a, in
                 if (tb + j == pos) {
                     const float4 x = *reinterpret_cast<const float4*>(vn + 4 * lane);
                     v4[0] = x.x; v4[1] = x.y; v4[2] = x.z; v4[3] = x.w;
+                } else if constexpr (KVT == 2) {
+                    const uint32_t w = *reinterpret_cast<const uint32_t*>(Vt + j * S::ROW + 4 * lane);
+                    const float dv = h2f(reinterpret_cast<const unsigned short*>(Vt + TILE * S::ROW)[j * 4 + (lane >> 3)]);
+                    s8x4_to_f32(w, v4);
+#pragma unroll
+                    for (int d = 0; d < 4; ++d) v4[d] *= dv;
                 } else if constexpr (KVT == 1) {
                     const uint2 w = *reinterpret_cast<const uint2*>(Vt + j * S::ROW + 8 * lane);
                     v4[0] = bf_lo_f(w.x); v4[1] = bf_hi_f(w.x); v4[2] = bf_lo_f(w.y); v4[3] = bf_hi_f(w.y);
@@ -510,10 +601,12 @@ void prepare_t() {
 void attention_prepare() {
     prepare_t<0, 1>(); prepare_t<0, 2>(); prepare_t<0, 4>();
     prepare_t<1, 1>(); prepare_t<1, 2>(); prepare_t<1, 4>();
+    prepare_t<2, 1>(); prepare_t<2, 2>(); prepare_t<2, 4>();
 }
 
 void launch_attention(const AttnArgs& a, cudaStream_t s, bool pdl) {
-    if (a.kv_bf16) launch_kv<1>(a, s, pdl);
+    if (a.kv_type == KV_Q8_0) launch_kv<2>(a, s, pdl);
+    else if (a.kv_type == KV_BF16) launch_kv<1>(a, s, pdl);
     else launch_kv<0>(a, s, pdl);
 }
 

@@ -15,9 +15,9 @@ constexpr int ATT_THREADS = 128;
 constexpr int ATT_WARPS = 4;
 constexpr float LOG2E = 1.4426950408889634f;
 
-template <int KVT> struct KvType;
-template <> struct KvType<0> { using T = float; };
-template <> struct KvType<1> { using T = uint16_t; };
+template <int KVT> struct KvElem;
+template <> struct KvElem<0> { using T = float; };
+template <> struct KvElem<1> { using T = uint16_t; };
 
 // normalise + rope one head held as 4 dims per lane (dims 4l..4l+3) by one warp
 FQ_DEV void norm_rope_head(float v[4], const float* gain, const float2* rope_row, float eps, int lane) {
@@ -37,7 +37,7 @@ FQ_DEV void norm_rope_head(float v[4], const float* gain, const float2* rope_row
 }
 
 template <int KVT>
-FQ_DEV void to_cache(float f, typename KvType<KVT>::T* dst, float& rounded) {
+FQ_DEV void to_cache(float f, typename KvElem<KVT>::T* dst, float& rounded) {
     if constexpr (KVT == 1) {
         __nv_bfloat16 h = __float2bfloat16_rn(f);
         *dst = __bfloat16_as_ushort(h);
@@ -67,7 +67,7 @@ struct alignas(16) AttnSmem {
 // runs one unit per CTA; the persistent decode kernel runs several per CTA.
 template <int KVT, int G, class Sync>
 FQ_DEV void attn_unit(const AttnArgs& a, int s, int g, int b, int tid, AttnSmem<G>& sm, Sync sync) {
-    using T = typename KvType<KVT>::T;
+    using T = typename KvElem<KVT>::T;
     const int lane = tid & 31, warp = tid >> 5;
     const SeqState ss = a.st->seq[b];
     const int pos = ss.pos, T_len = pos + 1;

@@ -92,6 +92,39 @@ FQ_DEV void u8x4_to_f32(uint32_t u, float* f) {
     f[3] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7443)) - bias;
 }
 
+// ggml Q8_0 quantisation of one value x of a block whose scale is d = fp16(amax / 127):
+// the code is x / d rounded half away from zero, clamped to +-127 (0 when d is 0).  The
+// quotient only picks a candidate n = trunc(|x| / d); the exact answer is n or n + 1, and
+// |x| >= (n + 1/2) d decides it without rounding, because (n + 1/2) d has at most 20
+// significant bits (n + 1/2 below 2^8 in halves, d an fp16 of 11 bits).
+FQ_DEV int q8_code(float x, float d) {
+    if (!(d > 0.f)) return 0;
+    const float a = fabsf(x);
+    int n = (int)fminf(__fdiv_rn(a, d), 255.f);
+    if (a >= ((float)n + 0.5f) * d) ++n;
+    n = n > 127 ? 127 : n;
+    return x < 0.f ? -n : n;
+}
+
+// Q8_0 quantisation of a block of 32 values held 4 per lane by 8 consecutive lanes (lanes
+// 8j..8j+7 of a warp, all of which call this): returns the lane's 4 codes as bytes of one
+// word and sets the fp16 scale.  d = fp16(amax / 127), rounded to nearest even; the f32
+// quotient cannot move amax / 127 across an fp16 rounding boundary (such a boundary lies
+// more than half an f32 ulp away from any quotient of an f32 by 127 that is not on it).
+FQ_DEV uint32_t q8_quant_lane4(const float v[4], unsigned short& d_bits, float& d) {
+    float am = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+    am = fmaxf(am, __shfl_xor_sync(0xFFFFFFFFu, am, 1));
+    am = fmaxf(am, __shfl_xor_sync(0xFFFFFFFFu, am, 2));
+    am = fmaxf(am, __shfl_xor_sync(0xFFFFFFFFu, am, 4));
+    const __half dh = __float2half_rn(__fdiv_rn(am, 127.f));
+    d = __half2float(dh);
+    d_bits = __half_as_ushort(dh);
+    uint32_t w = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) w |= ((uint32_t)q8_code(v[j], d) & 0xFFu) << (8 * j);
+    return w;
+}
+
 // Order-preserving map of a float to u32 (larger float -> larger key).
 FQ_DEV uint32_t float_order_key(float f) {
     uint32_t b = __float_as_uint(f);

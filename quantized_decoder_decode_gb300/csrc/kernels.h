@@ -50,6 +50,10 @@ struct QMat {
 // Per-sequence state of one step, resident in the per-stream workspace.  Written by the
 // set-up kernel before a step (or a chain of greedy steps); read by every kernel, so a
 // captured graph is independent of the token, the positions and the cache pointers.
+// What a KvCache stores per row: f32 or bf16 values, or Q8_0 (int8 codes and a plane of
+// fp16 block scales).
+enum KvType : int { KV_F32 = 0, KV_BF16 = 1, KV_Q8_0 = 2 };
+
 struct SeqState {
     int32_t token;        // token consumed by this step's embedding
     int32_t pos;          // absolute position of the new token (== cache len)
@@ -57,6 +61,8 @@ struct SeqState {
     int32_t pad;
     void* k;              // cache planes, [layer][kv_head][cap][head_dim]
     void* v;
+    void* ks;             // Q8_0 scale planes, [layer][kv_head][cap rounded up to even][4] fp16
+    void* vs;
 };
 
 constexpr int MAX_SEQ = 64;
@@ -133,7 +139,7 @@ struct AttnArgs {
     float eps;
     int Hq, Hkv;
     int layer;
-    int kv_bf16;                  // 1: bf16 cache, 0: f32 cache
+    int kv_type;                  // KvType of the caches
     int chunk;                    // positions per CTA (multiple of 32)
     int splits;                   // grid.x
     const StepState* st;
@@ -188,8 +194,17 @@ struct SetupArgs {
     int32_t cap[MAX_SEQ];
     void* k[MAX_SEQ];
     void* v[MAX_SEQ];
+    void* ks[MAX_SEQ];
+    void* vs[MAX_SEQ];
 };
 void launch_setup(StepState* st, const SetupArgs& a, cudaStream_t s);
+
+// Q8_0 cache rows <-> ggml blocks: blocks [n_pos][Hkv][4][34 bytes]; codes / scales point at
+// row 0 of kv head 0 of one layer, with per-head strides of cap and cap_s rows.
+void launch_kv_q8_copy(int8_t* codes, uint16_t* scales, size_t cap, size_t cap_s, int Hkv, int pos, int n_pos,
+                       uint8_t* blocks, bool to_cache, cudaStream_t s);
+// ggml Q8_0 blocks of x[0, n) (n a multiple of 128) with the attention kernel's quantiser
+void launch_quantize_q8_0(const float* x, size_t n, uint8_t* blocks, cudaStream_t s);
 
 // LM-head finisher: decode argmax keys, hand the token to the next step.
 void launch_lm_finish(StepState* st, int n, int vocab, cudaStream_t s, bool pdl);

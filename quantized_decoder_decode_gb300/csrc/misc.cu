@@ -30,6 +30,8 @@ __global__ void setup_kernel(StepState* st, const SetupArgs a) {
         q.cap = a.cap[b];
         q.k = a.k[b];
         q.v = a.v[b];
+        q.ks = a.ks[b];
+        q.vs = a.vs[b];
         st->keys[b] = 0ull;
     }
     if (b == 0) {
@@ -121,7 +123,66 @@ __global__ void dequant_kernel(const QMat W, int64_t row0, int64_t n_rows, float
         out[t] = dequant_one(W, row0 + t / W.K, t % W.K);
 }
 
+// Q8_0 cache rows <-> ggml blocks, one thread per (position, kv head, block of 32)
+__global__ void kv_q8_copy_kernel(int8_t* codes, uint16_t* scales, size_t cap, size_t cap_s, int Hkv, int pos,
+                                  int n_pos, uint8_t* blocks, int to_cache) {
+    const int64_t total = (int64_t)n_pos * Hkv * (HEAD_DIM / 32);
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+        const int j = (int)(i % (HEAD_DIM / 32));
+        const int64_t ph = i / (HEAD_DIM / 32);
+        const int h = (int)(ph % Hkv);
+        const int64_t p = pos + ph / Hkv;
+        uint8_t* blk = blocks + i * 34;
+        int8_t* c = codes + ((size_t)h * cap + p) * HEAD_DIM + 32 * j;
+        uint16_t* sc = scales + ((size_t)h * cap_s + p) * (HEAD_DIM / 32) + j;
+        if (to_cache) {
+            *sc = (uint16_t)(blk[0] | (blk[1] << 8));
+            for (int k = 0; k < 32; ++k) c[k] = (int8_t)blk[2 + k];
+        } else {
+            const uint16_t d = *sc;
+            blk[0] = (uint8_t)(d & 0xFFu);
+            blk[1] = (uint8_t)(d >> 8);
+            for (int k = 0; k < 32; ++k) blk[2 + k] = (uint8_t)c[k];
+        }
+    }
+}
+
+// ggml Q8_0 blocks of x, one warp per 128 values, with the quantiser the attention kernel
+// applies to q and to the new k and v
+__global__ void quantize_q8_0_kernel(const float* x, size_t n, uint8_t* blocks) {
+    const size_t rows = n / 128;
+    const int lane = threadIdx.x & 31;
+    const size_t warps = ((size_t)gridDim.x * blockDim.x) >> 5;
+    for (size_t r = ((size_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < rows; r += warps) {
+        const float4 f = reinterpret_cast<const float4*>(x + r * 128)[lane];
+        const float v[4] = {f.x, f.y, f.z, f.w};
+        unsigned short db;
+        float d;
+        const uint32_t w = q8_quant_lane4(v, db, d);
+        uint8_t* blk = blocks + (r * 4 + (lane >> 3)) * 34;
+        if ((lane & 7) == 0) {
+            blk[0] = (uint8_t)(db & 0xFFu);
+            blk[1] = (uint8_t)(db >> 8);
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) blk[2 + 4 * (lane & 7) + j] = (uint8_t)(w >> (8 * j));
+    }
+}
+
 }  // namespace
+
+void launch_kv_q8_copy(int8_t* codes, uint16_t* scales, size_t cap, size_t cap_s, int Hkv, int pos, int n_pos,
+                       uint8_t* blocks, bool to_cache, cudaStream_t s) {
+    const int64_t total = (int64_t)n_pos * Hkv * (HEAD_DIM / 32);
+    const int grid = (int)std::min<int64_t>((total + 255) / 256, 4096);
+    kv_q8_copy_kernel<<<grid, 256, 0, s>>>(codes, scales, cap, cap_s, Hkv, pos, n_pos, blocks, to_cache ? 1 : 0);
+}
+
+void launch_quantize_q8_0(const float* x, size_t n, uint8_t* blocks, cudaStream_t s) {
+    const size_t warps = n / 128;
+    const int grid = (int)std::min<size_t>((warps * 32 + 255) / 256, 1024);
+    if (grid > 0) quantize_q8_0_kernel<<<grid, 256, 0, s>>>(x, n, blocks);
+}
 
 void launch_setup(StepState* st, const SetupArgs& a, cudaStream_t s) {
     setup_kernel<<<1, MAX_SEQ, 0, s>>>(st, a);

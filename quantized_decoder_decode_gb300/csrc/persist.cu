@@ -484,7 +484,7 @@ int persist_ctas() { return g_sms_p; }
 
 bool launch_persist(const PersistArgs& a, cudaStream_t s) {
     if (g_sms_p == 0) return false;
-    return a.at.kv_bf16 ? launch_k<1>(a, s) : launch_k<0>(a, s);
+    return a.at.kv_type == KV_BF16 ? launch_k<1>(a, s) : launch_k<0>(a, s);
 }
 
 }  // namespace fq

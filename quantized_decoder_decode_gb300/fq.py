@@ -87,6 +87,7 @@ def lib():
                 "fq_decode_greedy": [vp, vp, u32, vp, u32, vp, vp, vp],
                 "fq_decode_step_trace": [vp, vp, u32, vp, vp, vp, vp, vp, vp],
                 "fq_dequant_rows": [vp, u32, ctypes.c_int, u64, u64, vp, vp],
+                "fq_quantize_q8_0": [vp, u64, vp, vp],
                 "fq_layer_step_trace": [vp, u32, vp, u32, vp, vp, vp, vp, vp],
                 "fq_gemv": [vp, u32, ctypes.c_int, u32, vp, vp, vp],
                 "fq_check_device": [vp, vp],
@@ -115,7 +116,7 @@ def lib():
 
 EXPORTED = ("fq_desc_init", "fq_load_weights", "fq_model_free", "fq_kv_init", "fq_kv_free", "fq_kv_len",
             "fq_kv_capacity", "fq_kv_append", "fq_kv_commit", "fq_kv_rewind", "fq_kv_read", "fq_layer_step", "fq_decode_step",
-            "fq_decode_step_batch", "fq_decode_step_all_logits", "fq_decode_greedy", "fq_decode_step_trace", "fq_dequant_rows", "fq_layer_step_trace",
+            "fq_decode_step_batch", "fq_decode_step_all_logits", "fq_decode_greedy", "fq_decode_step_trace", "fq_dequant_rows", "fq_quantize_q8_0", "fq_layer_step_trace",
             "fq_gemv", "fq_step_kernels", "fq_check_device", "fq_layer_step_noalloc", "fq_last_error",
             "fq_status_str")
 
@@ -269,6 +270,10 @@ def fq_decode_step_trace(model: int, kvs, tokens, logits_ptr: int, layer_out_ptr
 
 def fq_dequant_rows(model: int, layer: int, which: int, row0: int, n_rows: int, out_ptr: int, stream: int = 0) -> None:
     _check(lib().fq_dequant_rows(model, layer, which, row0, n_rows, out_ptr, stream), "fq_dequant_rows")
+
+
+def fq_quantize_q8_0(x_ptr: int, n: int, blocks_ptr: int, stream: int = 0) -> None:
+    _check(lib().fq_quantize_q8_0(x_ptr, n, blocks_ptr, stream), "fq_quantize_q8_0")
 
 
 def fq_layer_step_trace(model: int, layer: int, kv: int, pos: int, x_ptr: int, qkv_ptr: int = 0, attn_ptr: int = 0,
