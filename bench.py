@@ -638,6 +638,65 @@ def run_verify(args):
     return 0
 
 
+def run_prefill(args):
+    """Multi-token forwardStep (section 14.1) as a prefill: the 0.6B workload's 2048 prompt ids
+    in one call (passes of 32 rows) against the same ids decoded one token at a time, both
+    from an empty cache, both ending with the last row's logits."""
+    import torch
+    import synth.workloads as wl
+    from quantized_decoder_decode_gb300 import fq
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    st = torch.cuda.current_stream(dev)
+    stream = st.cuda_stream
+    w = workload_of(args)
+    if not w.prefill_from_model:
+        print(json.dumps({"kernel": "prefill", "unavailable": f"{w.name} has no prompt; use the default workload"}))
+        return 0
+    d = w.dims
+    ids = [int(t) for t in wl.prefill_ids(w)]
+    n = len(ids)
+    W = wl.make_weights(w)
+    desc = fq.fq_desc_init(vocab_size=d.vocab_size, hidden_size=d.hidden_size, intermediate_size=d.intermediate_size,
+                           num_layers=d.num_layers, num_attention_heads=d.num_attention_heads,
+                           num_key_value_heads=d.num_key_value_heads, head_dim=d.head_dim,
+                           num_experts=d.num_experts, num_experts_used=d.num_experts_used,
+                           moe_intermediate_size=d.moe_intermediate_size, max_positions=n + 64)
+    src, keep = fq.weight_src(desc, W, w.weight_dtype)
+    model = fq.fq_load_weights(desc, src, stream)
+    del src, keep
+    kv = fq.fq_kv_init(model, n, w.kv_dtype)
+    logits = torch.empty(d.vocab_size, dtype=torch.float32, device=dev)
+
+    def timed(fn, reps):
+        for _ in range(max(args.warmup, 3) if reps > 1 else 1):
+            fq.fq_kv_rewind(kv, 0)
+            fn()
+        torch.cuda.synchronize()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        for a_, b_ in evs:
+            fq.fq_kv_rewind(kv, 0)
+            a_.record(st)
+            fn()
+            b_.record(st)
+        torch.cuda.synchronize()
+        t = sorted(a_.elapsed_time(b_) for a_, b_ in evs)
+        return t[len(t) // 2]
+
+    p_ms = timed(lambda: fq.fq_forward_step(model, kv, ids, 0, logits.data_ptr(), stream), 5)
+
+    def tokenwise():
+        for p, t in enumerate(ids):
+            fq.fq_decode_step(model, kv, t, p, logits.data_ptr() if p == n - 1 else 0, stream)
+    t_ms = timed(tokenwise, 2)
+    print(json.dumps({"kernel": "prefill", "workload": w.name, "kv": w.kv_dtype, "tokens": n,
+                      "forward_step_ms": p_ms, "token_by_token_ms": t_ms, "speedup": t_ms / p_ms,
+                      "prefill_tokens_per_s": n / (p_ms * 1e-3)}))
+    fq.fq_kv_free(kv)
+    fq.fq_model_free(model)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--kernel", choices=["lm_head", "layer", "proj"], default=None,
@@ -655,7 +714,11 @@ def main():
                     help="cache dtype in place of the workload's own (q8_0: the integer-score cache)")
     ap.add_argument("--verify", action="store_true",
                     help="all-logits verify pass of k tokens against k single steps, k in 2/4/8/16")
+    ap.add_argument("--prefill", action="store_true",
+                    help="the 2048-token prompt through one multi-token forwardStep against token-by-token decode")
     args = ap.parse_args()
+    if args.prefill:
+        return run_prefill(args)
     if args.verify:
         return run_verify(args)
     if args.kernel:

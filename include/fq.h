@@ -160,6 +160,19 @@ fq_status fq_kv_read(const fq_kv* kv, uint32_t layer, uint32_t pos, uint32_t n_p
  * INVALID_SEQUENCE_LENGTH, KV_CACHE_OVERFLOW, INVALID_ARGUMENT. */
 fq_status fq_layer_step(const fq_model* m, uint32_t layer, fq_kv* kv, uint32_t pos, float* x, void* stream);
 
+/* Section 14.1 forwardStep over len >= 1 tokens of one sequence: tokens (host, [len]) at
+ * positions pos0..pos0+len-1, every row's K/V appended, len advanced by len, the last row's
+ * logits written to `logits` (device f32 [vocab], caller-owned; NULL: append only).  A
+ * prefill is one call on a fresh cache at pos0 == 0, and its logits equal forwardLastLogits
+ * over the same ids.  Runs in passes of up to 32 rows: the dense projections of a pass read
+ * every weight once for all its rows (tensor cores from 8 rows); each row attends causally
+ * to the cache and the rows before it.  Errors (state unchanged): INVALID_SEQUENCE_LENGTH
+ * (len == 0, pos0 != len), KV_CACHE_OVERFLOW (len + n > capacity), INVALID_ARGUMENT (a token
+ * out of range, no embedding, or logits without an LM head), MISMATCHED_KV_CACHES (another
+ * model's cache).  After a CUDA error the cache length covers the passes enqueued. */
+fq_status fq_forward_step(const fq_model* m, fq_kv* kv, const int32_t* tokens, uint32_t len, uint32_t pos0,
+                          float* logits, void* stream);
+
 /* Section 14.1 forwardStep for one token: embedding row of `token`, every layer,
  * output norm, LM head -> logits device f32 [vocab] (caller-owned).  Contract: pos0 ==
  * len (else INVALID_SEQUENCE_LENGTH), len + 1 <= capacity (else KV_CACHE_OVERFLOW).

@@ -245,6 +245,8 @@ struct Body {
     // rows are consecutive positions of one sequence (the all-logits step): every row's new
     // k/v is appended before any row attends
     bool block = false;
+    // LM head on this row only (its logits go to `logits` as one row); -1: every row
+    int head_row = -1;
 };
 
 // Batch 1 of a dense model can run as one persistent kernel (FQ_PERSIST=1).  Off by default:
@@ -396,7 +398,9 @@ fq_status enqueue_step(const Body& b, cudaStream_t s, int kv_type, float* x_over
     }
     if (b.logits) {
         GemvArgs lm;
-        lm.W = m->output; lm.B = n; lm.x = x; lm.x_stride = H; lm.norm_g = m->output_norm; lm.eps = p.rms_norm_eps;
+        const bool one = b.head_row >= 0;
+        lm.W = m->output; lm.B = one ? 1 : n; lm.x = one ? x + (size_t)b.head_row * H : x; lm.x_stride = H;
+        lm.norm_g = m->output_norm; lm.eps = p.rms_norm_eps;
         lm.y = b.logits; lm.y_stride = p.vocab_size; lm.epi = b.greedy ? EPI_LOGITS : EPI_STORE; lm.st = w->st;
         lm.ksplit = choose_ksplit(lm.W, rows_per_warp(lm.W));
         proj(lm);
@@ -959,6 +963,39 @@ fq_status fq_decode_step_batch(const fq_model* m, fq_kv* const* caches, uint32_t
     attn_split((int)n, m->d.p.num_key_value_heads, cap, b.chunk, b.splits);
     TRY(run_body(b, s, caches[0]->type, 1));
     for (uint32_t i = 0; i < n; ++i) caches[i]->len += 1;
+    return FQ_OK;
+}
+
+// Rows of one sequence per pass of a multi-token forwardStep: the lockstep batch the
+// tensor-core projections are built and tested for.
+constexpr uint32_t FORWARD_ROWS = 32;
+
+fq_status fq_forward_step(const fq_model* m, fq_kv* kv, const int32_t* tokens, uint32_t len, uint32_t pos0,
+                          float* logits, void* stream) {
+    if (!m || !kv) return fail(FQ_ERR_INVALID_ARGUMENT, "null argument");
+    if (kv->m != m) return fail(FQ_ERR_MISMATCHED_KV_CACHES, "cache belongs to another model");
+    if (!m->tok_embd.q) return fail(FQ_ERR_INVALID_ARGUMENT, "model has no embedding");
+    if (logits && !m->output.q) return fail(FQ_ERR_INVALID_ARGUMENT, "model has no LM head");
+    if (len == 0) return fail(FQ_ERR_INVALID_SEQUENCE_LENGTH, "empty input");
+    if (pos0 != kv->len) return fail(FQ_ERR_INVALID_SEQUENCE_LENGTH, "pos0 %u != len %u", pos0, kv->len);
+    if ((uint64_t)kv->len + len > kv->cap)
+        return fail(FQ_ERR_KV_CACHE_OVERFLOW, "len %u + %u > capacity %u", kv->len, len, kv->cap);
+    TRY(check_tokens(m, tokens, len));
+    cudaStream_t s = (cudaStream_t)stream;
+    std::vector<fq_kv*> rows(std::min(len, FORWARD_ROWS), kv);
+    for (uint32_t off = 0; off < len; off += FORWARD_ROWS) {
+        const uint32_t n = std::min(FORWARD_ROWS, len - off);
+        const bool last = off + n == len;
+        Workspace* w;
+        TRY(ensure_ws(m, s, (int)n, kv->cap, &w));   // grows only; a shorter last pass may want more splits
+        TRY(setup_state(w, rows.data(), tokens + off, (int)n, false, nullptr, nullptr, s, 1));
+        Body b{m, w, (int)n, 0, 0, last ? logits : nullptr, false};
+        b.block = true;
+        b.head_row = (int)n - 1;
+        attn_split((int)n, m->d.p.num_key_value_heads, kv->cap, b.chunk, b.splits);
+        TRY(enqueue_step(b, s, kv->type, nullptr, -1));
+        kv->len += n;   // the next pass's rows sit after this one's
+    }
     return FQ_OK;
 }
 

@@ -84,6 +84,7 @@ def lib():
                 "fq_decode_step": [vp, vp, i32, u32, vp, vp],
                 "fq_decode_step_batch": [vp, vp, u32, vp, vp, vp],
                 "fq_decode_step_all_logits": [vp, vp, vp, u32, u32, vp, vp],
+                "fq_forward_step": [vp, vp, vp, u32, u32, vp, vp],
                 "fq_decode_greedy": [vp, vp, u32, vp, u32, vp, vp, vp],
                 "fq_decode_step_trace": [vp, vp, u32, vp, vp, vp, vp, vp, vp],
                 "fq_dequant_rows": [vp, u32, ctypes.c_int, u64, u64, vp, vp],
@@ -116,7 +117,7 @@ def lib():
 
 EXPORTED = ("fq_desc_init", "fq_load_weights", "fq_model_free", "fq_kv_init", "fq_kv_free", "fq_kv_len",
             "fq_kv_capacity", "fq_kv_append", "fq_kv_commit", "fq_kv_rewind", "fq_kv_read", "fq_layer_step", "fq_decode_step",
-            "fq_decode_step_batch", "fq_decode_step_all_logits", "fq_decode_greedy", "fq_decode_step_trace", "fq_dequant_rows", "fq_quantize_q8_0", "fq_layer_step_trace",
+            "fq_decode_step_batch", "fq_decode_step_all_logits", "fq_forward_step", "fq_decode_greedy", "fq_decode_step_trace", "fq_dequant_rows", "fq_quantize_q8_0", "fq_layer_step_trace",
             "fq_gemv", "fq_step_kernels", "fq_check_device", "fq_layer_step_noalloc", "fq_last_error",
             "fq_status_str")
 
@@ -245,6 +246,13 @@ def _i32(v):
 def fq_decode_step_batch(model: int, kvs, tokens, logits_ptr: int, stream: int = 0) -> None:
     toks, tp = _i32(tokens)
     _check(lib().fq_decode_step_batch(model, _caches(kvs), len(kvs), tp, logits_ptr, stream), "fq_decode_step_batch")
+
+
+def fq_forward_step(model: int, kv: int, tokens, pos0: int, logits_ptr: int = 0, stream: int = 0) -> None:
+    """forwardStep over len(tokens) tokens of one sequence at pos0..: the last row's logits
+    ([vocab], device) or, with logits_ptr 0, only the K/V appends (a prefill at pos0 = 0)."""
+    toks, tp = _i32(tokens)
+    _check(lib().fq_forward_step(model, kv, tp, len(toks), pos0, logits_ptr or None, stream), "fq_forward_step")
 
 
 def fq_decode_step_all_logits(model: int, kv: int, tokens, pos0: int, logits_ptr: int, stream: int = 0) -> None:

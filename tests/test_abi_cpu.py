@@ -75,5 +75,7 @@ def test_null_arguments_are_rejected_without_a_gpu(lib):
     assert lib.fq_load_weights(None, None, None, None) == fq.INVALID_ARGUMENT
     assert lib.fq_decode_step_batch(None, None, 0, None, None, None) == fq.INVALID_ARGUMENT
     assert lib.fq_decode_step_all_logits(None, None, None, 1, 0, None, None) == fq.INVALID_ARGUMENT
+    assert lib.fq_forward_step(None, None, None, 1, 0, None, None) == fq.INVALID_ARGUMENT
+    assert lib.fq_quantize_q8_0(None, 128, None, None) == fq.INVALID_ARGUMENT
     out = ctypes.c_void_p()
     assert lib.fq_kv_init(None, 4, fq.BF16, ctypes.byref(out)) == fq.INVALID_ARGUMENT
