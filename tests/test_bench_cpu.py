@@ -1,0 +1,52 @@
+"""Host-side accounting of bench.py, without a GPU: the algorithmic bytes a step moves (the
+numerator of every roofline figure the bench reports) against the per-configuration totals
+derived from the Qwen3 shapes and the ggml block sizes, and the --kv workload switch."""
+import argparse
+
+import numpy as np
+import pytest
+import torch
+
+import bench
+import synth.workloads as wl
+
+MB = 1e6
+
+
+def test_step_bytes_of_the_0p6b_decode_step():
+    # Qwen3-0.6B Q8_0: 633.5 MB of weights (165 MB of them the LM head), bf16 KV of 28 layers
+    # x 8 kv heads x 128 x 2 bytes x (K, V) = 114,688 bytes per cached position
+    b = bench.step_bytes(wl.QWEN3_0P6B, 2048)
+    assert (b["weights"] + b["lm_head"]) / MB == pytest.approx(633.5, rel=1e-3)
+    assert b["lm_head"] / MB == pytest.approx(165.3, rel=1e-3)
+    assert b["kv_read"] == 2048 * 114688 and b["kv_write"] == 114688
+    assert b["total"] / MB == pytest.approx(868.5, rel=1e-3)
+
+
+def test_weight_bytes_of_the_8b_q8_0_model():
+    # Qwen3-8B Q8_0: 8.04 GB of weights touched per step, of which the LM head is
+    # 151936 x 4096 x 34/32 bytes
+    wb = bench.weight_bytes(wl.WORKLOADS["qwen3-8b-batch32"])
+    assert (wb["layers"] + wb["lm_head"]) / 1e9 == pytest.approx(8.04, rel=2e-3)
+    assert wb["lm_head"] == pytest.approx(151936 * 4096 * 34 / 32 + 4096 * 4)
+
+
+def test_q8_0_cache_rows_cost_34_bytes_per_32_values():
+    # a head's cached row of 128 values: 4 blocks of 34 bytes = 136 bytes (bf16: 256)
+    assert bench.KV_ELEM_BYTES["q8_0"] * 128 == 136
+    assert bench.KV_ELEM_BYTES["bf16"] * 128 == 256
+
+
+def test_kv_switch_replaces_only_the_cache_dtype():
+    base = wl.WORKLOADS["qwen3-8b-batch32"]
+    w = bench.workload_of(argparse.Namespace(workload="qwen3-8b-batch32", kv="q8_0"))
+    assert w.kv_dtype == "q8_0" and w.dims == base.dims and w.seed == base.seed and w.batch == base.batch
+    assert bench.workload_of(argparse.Namespace(workload="qwen3-8b-batch32", kv=None)) is base
+
+
+def test_kv_tensor_keeps_the_bytes():
+    bf = np.array([0x3F80, 0xBF80], dtype=np.uint16)
+    t = bench.kv_tensor(bf, torch.device("cpu"))
+    assert t.dtype == torch.int16 and t.numpy().view(np.uint16).tolist() == [0x3F80, 0xBF80]
+    blocks = np.arange(34, dtype=np.uint8)
+    assert bench.kv_tensor(blocks, torch.device("cpu")).dtype == torch.uint8
