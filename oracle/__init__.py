@@ -79,6 +79,8 @@ def lib():
                 "or_decode_step_batch": ([vp, vp, i32, vp, vp], i32),
                 "or_forward_last_logits": ([vp, vp, i32, vp], i32),
                 "or_argmax": ([vp, i32], i32),
+                "or_sample": ([vp, i32, vp, vp, i32, f64], i32),
+                "or_uniform24": ([ctypes.c_uint64, ctypes.c_uint64], f64),
             }
             for name, (args, res) in sig.items():
                 fn = getattr(L, name)
@@ -225,6 +227,25 @@ def gemv(wtype: str, W: np.ndarray, rows: int, cols: int, x: np.ndarray) -> np.n
 def argmax(v: np.ndarray) -> int:
     v = np.ascontiguousarray(v, dtype=np.float64)
     return lib().or_argmax(_p(v), v.size)
+
+
+class _Sampling(ctypes.Structure):
+    _fields_ = [("temp", ctypes.c_double), ("top_k", ctypes.c_int), ("top_p", ctypes.c_double),
+                ("min_p", ctypes.c_double), ("repeat_penalty", ctypes.c_double)]
+
+
+def sample(z: np.ndarray, u: float, temp: float = 1.0, top_k: int = 0, top_p: float = 1.0, min_p: float = 0.0,
+           repeat_penalty: float = 1.0, history=()) -> int:
+    """The next token from one row of logits (or_sample gives the order of the steps)."""
+    z = np.ascontiguousarray(z, dtype=np.float64)
+    h = np.ascontiguousarray(history, dtype=np.int32)
+    s = _Sampling(temp, top_k, top_p, min_p, repeat_penalty)
+    return lib().or_sample(_p(z), z.size, ctypes.byref(s), _p(h) if h.size else None, h.size, float(u))
+
+
+def uniform24(seed: int, counter: int) -> float:
+    """Counter-based uniform in [0, 1) on a 2^-24 grid (SplitMix64 of seed + (counter + 1) * golden)."""
+    return lib().or_uniform24(seed, counter)
 
 
 # ---------------------------------------------------------------- model

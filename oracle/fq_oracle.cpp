@@ -708,4 +708,65 @@ int or_forward_last_logits(const or_model* m, const int* tokens, int n, double* 
     return OR_OK;
 }
 
+int or_sample(const double* z, int n, const or_sampling* s, const int* history, int n_hist, double u) {
+    std::vector<double> v(z, z + n);
+    if (s->repeat_penalty != 1.0) {
+        std::vector<char> seen(n, 0);
+        for (int i = 0; i < n_hist; ++i) {
+            int t = history[i];
+            if (t < 0 || t >= n || seen[t]) continue;
+            seen[t] = 1;
+            v[t] = v[t] > 0 ? v[t] / s->repeat_penalty : v[t] * s->repeat_penalty;
+        }
+    }
+    if (s->temp == 0) return or_argmax(v.data(), n);
+    double mx = -INFINITY;
+    for (int i = 0; i < n; ++i) mx = std::max(mx, v[i] / s->temp);
+    std::vector<double> p(n);
+    double sum = 0;
+    for (int i = 0; i < n; ++i) {
+        p[i] = std::exp(v[i] / s->temp - mx);
+        sum += p[i];
+    }
+    for (int i = 0; i < n; ++i) p[i] /= sum;
+    std::vector<int> order(n);
+    std::iota(order.begin(), order.end(), 0);
+    std::stable_sort(order.begin(), order.end(), [&](int a, int b) { return p[a] > p[b]; });   // ties: lower id first
+    int keep = n;
+    if (s->top_k > 0) keep = std::min(keep, s->top_k);
+    if (s->top_p < 1.0) {
+        double mass = 0, total = 0;
+        for (int j = 0; j < keep; ++j) total += p[order[j]];
+        int j = 0;
+        while (j < keep) {
+            mass += p[order[j]];
+            ++j;
+            if (mass >= s->top_p * total) break;
+        }
+        keep = j;
+    }
+    if (s->min_p > 0) {
+        double cut = s->min_p * p[order[0]];
+        int j = 1;
+        while (j < keep && p[order[j]] >= cut) ++j;
+        keep = j;
+    }
+    double Z = 0;
+    for (int j = 0; j < keep; ++j) Z += p[order[j]];
+    double target = u * Z, c = 0;
+    for (int j = 0; j < keep; ++j) {
+        c += p[order[j]];
+        if (c > target) return order[j];
+    }
+    return order[keep - 1];
+}
+
+double or_uniform24(uint64_t seed, uint64_t counter) {
+    uint64_t x = seed + (counter + 1) * 0x9E3779B97F4A7C15ull;
+    x = (x ^ (x >> 30)) * 0xBF58476D1CE4E5B9ull;
+    x = (x ^ (x >> 27)) * 0x94D049BB133111EBull;
+    x ^= x >> 31;
+    return (double)(x >> 40) * (1.0 / 16777216.0);
+}
+
 }  // extern "C"

@@ -125,6 +125,32 @@ int or_forward_last_logits(const or_model* m, const int* tokens, int n, double* 
 /* index of the largest value, ties to the lowest index */
 int or_argmax(const double* v, int n);
 
+/* ---- sampling (runner page: --temp, --top-k, --top-p, --min-p, --repeat-penalty, --seed) ---- */
+typedef struct or_sampling {
+    double temp;            /* 0: greedy argmax */
+    int top_k;              /* 0: off */
+    double top_p;           /* 1: off */
+    double min_p;           /* 0: off */
+    double repeat_penalty;  /* 1: off */
+} or_sampling;
+
+/* The next token from one row of logits z[n]:
+ *   1. repeat penalty over the distinct ids of history[n_hist]: z > 0 is divided by it,
+ *      otherwise multiplied;
+ *   2. temp == 0: argmax (ties to the lowest id);
+ *   3. p = softmax(z / temp); candidates ordered by p descending, ties to the lower id;
+ *   4. top_k > 0 keeps the first top_k; top_p < 1 keeps the shortest prefix whose mass
+ *      reaches top_p of the kept mass; min_p > 0 drops p < min_p * (largest p); at least one
+ *      candidate always stays;
+ *   5. with Z the kept mass, the first candidate whose cumulative mass exceeds u * Z
+ *      (u in [0, 1)). */
+int or_sample(const double* z, int n, const or_sampling* s, const int* history, int n_hist, double u);
+
+/* Counter-based uniform in [0, 1) on a 2^-24 grid (exact in f32): the top 24 bits of the
+ * SplitMix64 output for state seed + (counter + 1) * 0x9E3779B97F4A7C15 (Steele, Lea and
+ * Flood, "Fast splittable pseudorandom number generators", 2014). */
+double or_uniform24(uint64_t seed, uint64_t counter);
+
 #ifdef __cplusplus
 }
 #endif

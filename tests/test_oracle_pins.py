@@ -555,3 +555,67 @@ def test_step_contract_errors():
     with pytest.raises(oracle.OracleError) as e:
         m.forward_last_logits(np.array([], dtype=np.int32))
     assert e.value.code == oracle.INVALID_SEQUENCE_LENGTH
+
+
+# ---------------------------------------------------------------- sampling
+
+def _freqs(z, n_grid=1 << 14, **kw):
+    """How often each token is drawn as u sweeps a uniform grid of [0, 1)."""
+    counts = np.zeros(len(z))
+    for i in range(n_grid):
+        counts[oracle.sample(z, (i + 0.5) / n_grid, **kw)] += 1
+    return counts / n_grid
+
+
+def test_uniform24_is_the_top_of_splitmix64():
+    # SplitMix64 from seed 0 begins 0xE220A8397B1DCDAF, 0x6E789E6AA1B965F4, 0x06C45D188009454F
+    for c, out in enumerate((0xE220A8397B1DCDAF, 0x6E789E6AA1B965F4, 0x06C45D188009454F)):
+        assert oracle.uniform24(0, c) == (out >> 40) / 2.0 ** 24
+    us = [oracle.uniform24(12345, c) for c in range(1000)]
+    assert all(0.0 <= u < 1.0 and (u * 2 ** 24).is_integer() for u in us)
+    assert abs(np.mean(us) - 0.5) < 0.05
+
+
+def test_greedy_cases_are_argmax():
+    z = RNG.normal(0, 1, 40)
+    z[[7, 21]] = z.max() + 1.0                  # a tie: the lower id wins
+    for u in (0.0, 0.3, 0.999):
+        assert oracle.sample(z, u, temp=0.0, top_p=0.5, min_p=0.2) == 7
+        assert oracle.sample(z, u, temp=0.8, top_k=1) == 7
+
+
+def test_inverse_cdf_draws_follow_the_tempered_softmax():
+    from scipy.special import softmax
+    z = RNG.normal(0, 2, 30)
+    for temp in (1.0, 0.6, 1.7):
+        np.testing.assert_allclose(_freqs(z, temp=temp), softmax(z / temp), atol=2.0 / (1 << 14))
+
+
+def test_cutoffs_on_a_hand_built_distribution():
+    z = np.log([0.5, 0.3, 0.15, 0.05])
+    np.testing.assert_allclose(_freqs(z, top_p=0.75), [0.5 / 0.8, 0.3 / 0.8, 0, 0], atol=1e-3)
+    np.testing.assert_allclose(_freqs(z, top_p=0.81), [0.5 / 0.95, 0.3 / 0.95, 0.15 / 0.95, 0], atol=1e-3)
+    # top-k first, then top-p of the kept mass: 0.9 * 0.95 is reached at the third candidate
+    np.testing.assert_allclose(_freqs(z, top_k=3, top_p=0.9), [0.5 / 0.95, 0.3 / 0.95, 0.15 / 0.95, 0], atol=1e-3)
+    np.testing.assert_allclose(_freqs(z, top_k=2), [0.5 / 0.8, 0.3 / 0.8, 0, 0], atol=1e-3)
+    # min-p relative to the top probability: 0.35 * 0.5 = 0.175 drops the last two
+    np.testing.assert_allclose(_freqs(z, min_p=0.35), [0.5 / 0.8, 0.3 / 0.8, 0, 0], atol=1e-3)
+    assert _freqs(z, min_p=0.1)[3] > 0          # 0.05 >= 0.1 * 0.5 stays
+    # at least one candidate always stays
+    assert oracle.sample(z, 0.99, top_p=1e-9) == 0 and oracle.sample(z, 0.99, min_p=1.0) == 0
+
+
+def test_candidates_run_in_probability_order_with_ties_to_the_lower_id():
+    z = np.log([0.2, 0.4, 0.2, 0.2])
+    assert oracle.sample(z, 0.0) == 1           # the most probable first
+    assert oracle.sample(z, 0.45) == 0          # then the tied ones by id: 0, 2, 3
+    assert oracle.sample(z, 0.65) == 2 and oracle.sample(z, 0.85) == 3
+
+
+def test_repeat_penalty_divides_positive_and_multiplies_negative_logits():
+    z = np.array([2.0, 1.0, -1.0])
+    assert oracle.sample(z, 0.5, temp=0.0, repeat_penalty=2.0, history=[0, 2, 0]) == 0   # [1, 1, -2]: tie
+    assert oracle.sample(z, 0.5, temp=0.0, repeat_penalty=4.0, history=[0, 2]) == 1      # [0.5, 1, -4]
+    from scipy.special import softmax
+    np.testing.assert_allclose(_freqs(z, repeat_penalty=2.0, history=[0, 2]), softmax([1.0, 1.0, -2.0]),
+                               atol=2.0 / (1 << 14))
