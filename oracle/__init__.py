@@ -75,6 +75,7 @@ def lib():
                 "or_cache_write": ([vp, i32, i32, i32, vp, vp], i32), "or_cache_set_len": ([vp, i32], i32),
                 "or_cache_read": ([vp, i32, i32, i32, vp, vp], i32),
                 "or_layer_step": ([vp, i32, vp, i32, vp, vp, vp], i32),
+                "or_qkv_project": ([vp, i32, vp, i32, vp, vp, vp], i32),
                 "or_decode_step": ([vp, vp, i32, i32, vp, vp, vp, vp], i32),
                 "or_decode_step_batch": ([vp, vp, i32, vp, vp], i32),
                 "or_forward_last_logits": ([vp, vp, i32, vp], i32),
@@ -298,6 +299,18 @@ class Model:
         if rc:
             raise OracleError(rc, "or_layer_step")
         return x, idx, w
+
+    def qkv_project(self, layer: int, xn: np.ndarray, pos: int):
+        """q, k, v of one token from the normalised input xn (q, k after QK-norm and RoPE)."""
+        d = self.dims
+        xn = np.ascontiguousarray(xn, dtype=np.float64)
+        q = np.empty((d.num_attention_heads, d.head_dim), dtype=np.float64)
+        k = np.empty((d.num_key_value_heads, d.head_dim), dtype=np.float64)
+        v = np.empty_like(k)
+        rc = lib().or_qkv_project(self._h, layer, _p(xn), pos, _p(q), _p(k), _p(v))
+        if rc:
+            raise OracleError(rc, "or_qkv_project")
+        return q, k, v
 
     def decode_step(self, cache: "Cache", token: int, pos0: int, logits: bool = True, trace: bool = False):
         d = self.dims

@@ -592,6 +592,13 @@ int or_cache_read(const or_cache* c, int layer, int pos0, int n, float* k, float
     return OR_OK;
 }
 
+int or_qkv_project(const or_model* m, int layer, const double* xn, int pos, double* q, double* k, double* v) {
+    const or_dims& d = m->d;
+    if (layer < 0 || layer >= d.layers || !xn || !q || !k || !v || pos < 0) return OR_INVALID_ARGUMENT;
+    qkv_project(m, m->layers[layer], xn, pos, q, k, v, true);
+    return OR_OK;
+}
+
 int or_layer_step(const or_model* m, int layer, or_cache* c, int pos, double* x, int* route_idx,
                   double* route_w) {
     const or_dims& d = m->d;

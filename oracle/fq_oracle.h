@@ -107,6 +107,11 @@ enum { OR_OK = 0, OR_INVALID_CONFIG = 1, OR_INVALID_SEQUENCE_LENGTH = 2, OR_KV_C
 int or_layer_step(const or_model* m, int layer, or_cache* c, int pos, double* x, int* route_idx,
                   double* route_w);
 
+/* The attention block's projections for one token of layer `layer` at position pos, from the
+ * already normalised input xn (length hidden): q [n_q][head_dim], k and v [n_kv][head_dim],
+ * q and k after the per-head RMSNorm with q_norm / k_norm and then RoPE, v as projected. */
+int or_qkv_project(const or_model* m, int layer, const double* xn, int pos, double* q, double* k, double* v);
+
 /* forwardStep with one token at pos0 == cache len: embedding, all layers, output norm and
  * LM head into logits (vocab, may be NULL to skip the head).  layer_out (may be NULL)
  * receives the residual stream after every layer, [layers][hidden]; route (may be NULL)

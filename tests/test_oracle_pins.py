@@ -130,6 +130,18 @@ def test_q4_k_hand_built_block(golden_dir):
         assert np.all(out[32 * j:32 * j + 32] == expect[j]), j
 
 
+def test_q4_k_element_order_inside_sub_blocks(golden_dir):
+    # 128 distinct nibble bytes: any other byte <-> element map inside a chunk moves some byte
+    # to another element and changes its low or its high nibble
+    g = read_golden(f"{golden_dir}/q4_k_block_distinct.txt")
+    blk = np.array([int(b, 16) for key in ("header", "scales", "nibbles") for b in g[key][0].split()],
+                   dtype=np.uint8)
+    assert blk.size == 144 and len(set(blk[16:].tolist())) == 128
+    expect = np.array([float(v) for v in g["expect"][0].split()])
+    out = oracle.dequant("q4_k", blk, 256)
+    assert np.array_equal(out, expect)
+
+
 def test_q4_k_scale_min_pack_roundtrip_exhaustive():
     # every (scale, min) value in every sub-block slot, with the other slots holding
     # distinct values so that a crossed bit field shows up
@@ -216,6 +228,39 @@ def test_rope_relative_position_identity():
         a = oracle.rope(q, p, 1e6) @ oracle.rope(k, pp, 1e6)
         b = oracle.rope(q, p + s, 1e6) @ oracle.rope(k, pp + s, 1e6)
         assert abs(a - b) <= 1e-9 * (1 + abs(a))
+
+
+def _q8_rows_of_equal_codes(codes, d_bits=0x2800):
+    """Q8_0 rows of one block each: fp16 scale d_bits, then 32 copies of the row's code."""
+    rows = []
+    for c in codes:
+        rows.append([d_bits & 0xFF, d_bits >> 8] + [int(c) & 0xFF] * 32)
+    return np.array(rows, dtype=np.uint8)
+
+
+def test_qk_norm_then_rope_worked_example(golden_dir):
+    # the worked example of the golden file: per-head RMSNorm with non-constant gains, then
+    # the rotate-half RoPE at position 2 (rotating first would change elements 2 and 3)
+    g = read_golden(f"{golden_dir}/qk_norm_rope_order.txt")
+    vec = lambda key: np.array([float(v) for v in g[key][0].split()])  # noqa: E731
+    # eight heads of dim 4 so that every matrix has whole Q8_0 blocks; heads 1-7 project to
+    # zero (all-zero rows) and must stay zero through the norm and the rotation
+    dims = wl.Dims(vocab_size=40, hidden_size=32, intermediate_size=32, num_layers=1, num_attention_heads=8,
+                   num_key_value_heads=8, head_dim=4)
+    W = wl.make_weights(wl.Workload("qk-order", dims, "q8_0", "f32", seed=3))
+    lw = W["layers"][0]
+    pad = lambda c: np.concatenate([c, np.zeros(28)]).astype(int)  # noqa: E731
+    lw["wq"] = _q8_rows_of_equal_codes(pad(vec("wq_codes")))
+    lw["wk"] = _q8_rows_of_equal_codes(pad(vec("wk_codes")))
+    lw["wv"] = _q8_rows_of_equal_codes(pad(vec("wv_codes")))
+    lw["q_norm"] = vec("q_norm").astype(np.float32)
+    lw["k_norm"] = vec("k_norm").astype(np.float32)
+    m = oracle.Model(dims, W, "q8_0", "f32")
+    q, k, v = m.qkv_project(0, np.ones(32), int(g["pos"][0]))
+    np.testing.assert_allclose(q[0], vec("q"), rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(k[0], vec("k"), rtol=1e-12, atol=1e-14)
+    np.testing.assert_array_equal(v[0], vec("v"))
+    assert not q[1:].any() and not k[1:].any() and not v[1:].any()
 
 
 def test_attention_matches_torch_sdpa():
