@@ -43,7 +43,7 @@ typedef enum fq_status {
     FQ_ERR_INVALID_ARGUMENT = 5,        /* null pointer, bad shape/dtype, token out of range */
     FQ_ERR_OUT_OF_MEMORY = 6,           /* device allocation failed */
     FQ_ERR_CUDA = 7,                    /* a CUDA runtime call failed (message has the text) */
-    FQ_ERR_DEVICE_TIMEOUT = 8,          /* reserved: a bounded device wait gave up */
+    FQ_ERR_DEVICE_TIMEOUT = 8,          /* a bounded device wait gave up (fq_check_device) */
     FQ_ERR_UNSUPPORTED = 9              /* valid per the pages but not built here (e.g. head_dim != 128) */
 } fq_status;
 
@@ -265,17 +265,53 @@ fq_status fq_gemv(const fq_model* m, uint32_t layer, fq_weight_id which, uint32_
  * streams, other threads) race and give wrong results; serialise them. */
 fq_status fq_layer_step_noalloc(const fq_model* m, uint32_t layer, fq_kv* kv, uint32_t pos, float* x, void* stream);
 
+/* Execution options of a model (no counterpart on the pages; they choose between equivalent
+ * implementations of the same step).  Set them between steps, not while a step of the model
+ * is in flight on another thread; a change drops the CUDA graphs captured so far.
+ *   FQ_OPT_STEP_PATH          FQ_PATH_AUTO (default): a batch-1 step of a dense model with
+ *                             a bf16 cache runs as one streamed persistent kernel whose
+ *                             producer warps copy the step's weights and cached K/V into
+ *                             shared memory ahead of the activations; FQ_PATH_KERNELS: the
+ *                             sequence of per-stage kernels (replayed from a CUDA graph).
+ *   FQ_OPT_DEPENDENT_LAUNCH   0 (default) / 1: programmatic dependent launch between the
+ *                             kernels of the sequence.
+ *   FQ_OPT_GRAPHS             1 (default) / 0: capture the kernel sequence of a step once and
+ *                             replay it, or launch the kernels directly every step.
+ *   FQ_OPT_TENSOR_CORES       1 (default) / 0: tcgen05 GEMM for lockstep batches of 8 or more
+ *                             rows, or the CUDA-core GEMV for every batch.
+ * FQ_ERR_INVALID_ARGUMENT for an unknown option or value. */
+typedef enum fq_option {
+    FQ_OPT_STEP_PATH = 0, FQ_OPT_DEPENDENT_LAUNCH = 1, FQ_OPT_GRAPHS = 2, FQ_OPT_TENSOR_CORES = 3
+} fq_option;
+enum { FQ_PATH_AUTO = 0, FQ_PATH_KERNELS = 1 };
+fq_status fq_set_option(fq_model* m, fq_option opt, int value);
+
+/* *streamed = 1 when a step of n sequences with caches of kv_dtype runs as the streamed
+ * persistent kernel under the model's current options, else 0.  Host-only. */
+fq_status fq_step_path(const fq_model* m, uint32_t n, fq_dtype kv_dtype, int* streamed);
+
 /* Number of kernels one step launches on `stream`: the kernel nodes of the CUDA graph most
  * recently replayed there by fq_decode_step / fq_decode_step_batch / fq_decode_greedy, or 1
- * when the step ran as the single persistent kernel (batch 1, dense model); 0 when nothing
+ * when the step ran as the single streamed kernel (batch 1, dense model); 0 when nothing
  * has run there or the steps ran as direct launches.  Host-only; for accounting by
  * benchmarks. */
 fq_status fq_step_kernels(const fq_model* m, void* stream, uint32_t* kernels);
 
 /* Synchronise `stream` and report device-side failures recorded since the last check:
- * FQ_ERR_DEVICE_TIMEOUT when a kernel's bounded wait on its own copy pipeline gave up
- * (the kernel returned early; results of that step are invalid).  Clears the record. */
+ * FQ_ERR_DEVICE_TIMEOUT when a kernel's bounded wait on its own copy pipeline or on another
+ * CTA gave up (the kernel returned early; results of that step are invalid).  Clears the
+ * record and, on a timeout, zeroes the arrival counters and tickets of every workspace of
+ * the model (on each workspace's own stream), so that later steps start from a clean state. */
 fq_status fq_check_device(const fq_model* m, void* stream);
+
+/* Test hook for the failure path of the bounded device waits (no counterpart on the pages).
+ * Launches the bulk-copy GEMV over the LM head with a producer that issues no copies, so
+ * every consumer's bounded wait on its stage runs out (about a quarter second) with nothing
+ * in flight; the kernel records the failure and returns without writing outputs.  The next
+ * fq_check_device on `stream` reports FQ_ERR_DEVICE_TIMEOUT and re-arms the model's
+ * workspaces, after which steps run normally.  FQ_ERR_UNSUPPORTED when the LM head is not
+ * served by the bulk-copy GEMV (K % 256 != 0). */
+fq_status fq_debug_wait_timeout(const fq_model* m, void* stream);
 
 const char* fq_last_error(void);
 const char* fq_status_str(fq_status s);

@@ -51,11 +51,6 @@ fq_status fail(fq_status s, const char* fmt, ...) {
         if (s_ != FQ_OK) return s_; \
     } while (0)
 
-bool env_flag(const char* name) {
-    const char* v = getenv(name);
-    return v && *v && strcmp(v, "0") != 0;
-}
-
 }  // namespace
 
 // ---------------------------------------------------------------- model and cache objects
@@ -78,7 +73,14 @@ struct fq_model {
     int max_pos = 0;
     uint32_t* err = nullptr;       // device error word (bounded waits that gave up)
     std::deque<TmaMaps> tmaps;     // tensor maps of the dense weights (stable addresses)
-    PersistLayer* players = nullptr;   // device copy of the layer table for the persistent step
+    StreamLayer* slayers = nullptr;    // device layer table of the streamed batch-1 step (null: not served)
+    StreamArgs splan;                  // its shapes and shared-memory plan
+    int sfmt = 0, sG = 0;
+    // options (fq_set_option)
+    int opt_path = FQ_PATH_AUTO;
+    int opt_pdl = 0;
+    int opt_graphs = 1;
+    int opt_tc = 1;
     std::vector<void*> allocs;
     std::mutex ws_mu;
     std::map<cudaStream_t, Workspace*> ws;
@@ -109,7 +111,8 @@ struct Workspace {
     float* tc_part = nullptr;  // its split-K partial sums
     uint32_t* tc_tickets = nullptr;
     uint32_t* counters = nullptr;
-    uint32_t* pbar = nullptr;  // persistent step: grid barrier [2] + LM-head ticket
+    unsigned long long* sx = nullptr;   // streamed step: exchange words (see StreamArgs)
+    uint32_t* sctl = nullptr;           //                finishing ticket + launch sequence
     MoeRoute* route = nullptr;
     std::vector<void*> allocs;
     struct Graph {
@@ -172,6 +175,14 @@ int choose_ksplit(const QMat& W, int R) {
 
 int rows_per_warp(const QMat& W) { return W.fmt == FMT_Q4_K ? 2 : 4; }
 
+// exchange words of the streamed step: xf, xa [H], qkv, part [Hq][S][130], o [Hq*128], h [F]
+size_t stream_words(const fq_model* m) {
+    const auto& p = m->d.p;
+    return 2 * (size_t)p.hidden_size + (size_t)m->qkv_rows() +
+           (size_t)p.num_attention_heads * m->splan.S * (HEAD_DIM + 2) + (size_t)p.num_attention_heads * HEAD_DIM +
+           (size_t)p.intermediate_size;
+}
+
 fq_status ensure_ws(const fq_model* mc, cudaStream_t stream, int n, uint32_t cap_max, Workspace** out) {
     fq_model* m = const_cast<fq_model*>(mc);
     std::lock_guard<std::mutex> lk(m->ws_mu);
@@ -199,9 +210,14 @@ fq_status ensure_ws(const fq_model* mc, cudaStream_t stream, int n, uint32_t cap
         TRY(dalloc(A, &w->part, pc));
         TRY(dalloc(A, &w->counters, (size_t)nn * p.num_attention_heads));   // one per (row, CTA head group) at most
         TRY(dalloc(A, &w->logits, (size_t)nn * p.vocab_size));
-        TRY(dalloc(A, &w->pbar, 4));
         CK(cudaMemsetAsync(w->counters, 0, sizeof(uint32_t) * nn * p.num_attention_heads, stream));
-        CK(cudaMemsetAsync(w->pbar, 0, sizeof(uint32_t) * 4, stream));
+        if (m->slayers) {
+            const size_t words = stream_words(m);
+            TRY(dalloc(A, &w->sx, words));
+            TRY(dalloc(A, &w->sctl, 4));
+            CK(cudaMemsetAsync(w->sx, 0, sizeof(unsigned long long) * words, stream));
+            CK(cudaMemsetAsync(w->sctl, 0, sizeof(uint32_t) * 4, stream));
+        }
         if (nn >= TC_MIN_BATCH) {
             const int kmax = (int)std::max<size_t>({H, (size_t)p.num_attention_heads * HEAD_DIM,
                                                      (size_t)std::max<uint32_t>(p.intermediate_size, 1)});
@@ -229,6 +245,17 @@ fq_status ensure_ws(const fq_model* mc, cudaStream_t stream, int n, uint32_t cap
     return FQ_OK;
 }
 
+// Zero the counters and tickets that the kernels of a step leave at zero when they finish
+// normally (attention arrivals, tensor-core split-K tickets, the streamed step's ticket).
+fq_status rearm_ws(const fq_model* m, Workspace* w, cudaStream_t s) {
+    const auto& p = m->d.p;
+    if (w->counters) CK(cudaMemsetAsync(w->counters, 0, sizeof(uint32_t) * w->n_cap * p.num_attention_heads, s));
+    if (w->sctl) CK(cudaMemsetAsync(w->sctl, 0, sizeof(uint32_t), s));   // the ticket; the sequence may stay
+    if (w->tc_tickets) CK(cudaMemsetAsync(w->tc_tickets, 0, sizeof(uint32_t) * TC_TICKETS, s));
+    if (w->route) CK(cudaMemsetAsync(w->route, 0, sizeof(MoeRoute), s));
+    return FQ_OK;
+}
+
 enum Mode { MODE_DECODE = 1, MODE_GREEDY = 2 };
 
 struct Body {
@@ -249,12 +276,12 @@ struct Body {
     int head_row = -1;
 };
 
-// Batch 1 of a dense model can run as one persistent kernel (FQ_PERSIST=1).  Off by default:
-// measured on GB300 its grid barriers (about 2.4 us each, 5 per layer) cost more than the
-// launches of the captured kernel sequence they replace.
-bool persist_eligible(const Body& b, int kv_type) {
-    static const bool persist = env_flag("FQ_PERSIST");
-    return b.n == 1 && !b.m->moe() && b.m->players && !b.layer_out && !b.route_idx && kv_type != KV_Q8_0 && persist;
+// Batch 1 of a dense model with a bf16 cache runs as one streamed persistent kernel
+// (stream_step.cu) unless the caller asked for the kernel sequence.
+bool stream_eligible(const Body& b, int kv_type) {
+    const fq_model* m = b.m;
+    return m->slayers && m->opt_path != FQ_PATH_KERNELS && b.n == 1 && !b.route_idx && !b.block && b.head_row < 0 &&
+           kv_type == KV_BF16;
 }
 
 // The kernels of one decode step, in order.  The first launch follows the set-up kernel
@@ -265,10 +292,10 @@ fq_status enqueue_step(const Body& b, cudaStream_t s, int kv_type, float* x_over
     const auto& p = m->d.p;
     const int n = b.n, H = p.hidden_size, Hq = p.num_attention_heads, Hkv = p.num_key_value_heads;
     bool first = true;
-    // Programmatic dependent launch is opt-in: measured on GB300 the early-resident CTAs of
-    // the next kernel slowed the step down (FQ_PDL=1 enables it)
-    static const bool use_pdl = env_flag("FQ_PDL");
-    static const bool no_tc = env_flag("FQ_NO_TC");
+    // Programmatic dependent launch is an option (off by default: measured on GB300 the
+    // early-resident CTAs of the next kernel slowed the step down)
+    const bool use_pdl = m->opt_pdl != 0;
+    const bool no_tc = m->opt_tc == 0;
     auto pdl = [&]() { bool r = !first && use_pdl; first = false; return r; };
     // dense projection: tensor cores for lockstep batches, the GEMV kernels otherwise
     auto proj = [&](GemvArgs& g) {
@@ -282,39 +309,29 @@ fq_status enqueue_step(const Body& b, cudaStream_t s, int kv_type, float* x_over
     };
     float* x = x_override ? x_override : w->x;
 
-    // batch 1 of a dense model: the whole step as one persistent kernel
-    if (layer_only < 0 && persist_eligible(b, kv_type)) {
-        PersistArgs pa;
-        pa.layers = m->players;
-        pa.n_layers = (int)p.num_layers;
-        pa.H = H;
-        pa.F = (int)p.intermediate_size;
-        pa.Hq = Hq;
-        pa.Hkv = Hkv;
-        pa.V = (int)p.vocab_size;
-        pa.eps = p.rms_norm_eps;
-        pa.emb = m->tok_embd;
-        pa.out = m->output;
-        pa.out_norm = m->output_norm;
-        AttnArgs& a = pa.at;
-        a.qkv = w->qkv; a.qkv_stride = m->qkv_rows(); a.q_norm = nullptr; a.k_norm = nullptr;
-        a.rope = m->rope; a.eps = p.rms_norm_eps; a.Hq = Hq; a.Hkv = Hkv; a.layer = 0; a.kv_type = kv_type;
-        a.chunk = b.chunk; a.splits = b.splits; a.st = w->st; a.part = w->part; a.counters = w->counters;
-        a.out = w->attn; a.n = 1;
-        pa.x = x;
-        pa.qkv = w->qkv;
-        pa.attn = w->attn;
-        pa.h = w->h;
-        pa.logits = b.logits;
-        pa.greedy = b.greedy ? 1 : 0;
-        pa.bar = w->pbar;
-        pa.lm_ticket = w->pbar + 2;
-        pa.err = m->err;
-        if (launch_persist(pa, s)) {
-            CK(cudaGetLastError());
-            return FQ_OK;
+    // batch 1 of a dense model: the whole step as one streamed persistent kernel
+    if (layer_only < 0 && stream_eligible(b, kv_type)) {
+        StreamArgs sa = m->splan;
+        unsigned long long* q = w->sx;
+        sa.xf = q; q += H;
+        sa.xa = q; q += H;
+        sa.qkv = q; q += m->qkv_rows();
+        sa.part = q; q += (size_t)Hq * sa.S * (HEAD_DIM + 2);
+        sa.o = q; q += (size_t)Hq * HEAD_DIM;
+        sa.h = q;
+        sa.st = w->st;
+        sa.logits = b.logits;
+        sa.trace_x = b.layer_out;
+        sa.head = (b.logits || b.greedy) ? 1 : 0;
+        sa.greedy = b.greedy ? 1 : 0;
+        sa.ctl = w->sctl;
+        sa.err = m->err;
+        if (!launch_stream(sa, m->sfmt, m->sG, s)) {
+            cudaGetLastError();
+            return fail(FQ_ERR_CUDA, "streamed step launch refused");
         }
-        cudaGetLastError();   // a refused launch: fall through to the kernel sequence
+        CK(cudaGetLastError());
+        return FQ_OK;
     }
 
     if (layer_only < 0) launch_embed(m->tok_embd, w->st, n, x, s, pdl());
@@ -437,10 +454,10 @@ fq_status setup_state(Workspace* w, fq_kv* const* caches, const int32_t* tokens,
 fq_status run_body(const Body& b, cudaStream_t s, int kv_type, int reps) {
     Workspace* w = b.w;
     const int mode = b.greedy ? MODE_GREEDY : MODE_DECODE;
-    // one persistent kernel per step needs no graph (and a cooperative launch is not captured)
-    if (env_flag("FQ_NO_GRAPH") || b.layer_out || b.route_idx || persist_eligible(b, kv_type)) {
+    // one streamed kernel per step needs no graph
+    if (!b.m->opt_graphs || b.layer_out || b.route_idx || stream_eligible(b, kv_type)) {
         for (int r = 0; r < reps; ++r) TRY(enqueue_step(b, s, kv_type, nullptr, -1));
-        w->last_kernels = persist_eligible(b, kv_type) ? 1u : 0u;
+        w->last_kernels = stream_eligible(b, kv_type) ? 1u : 0u;
         return FQ_OK;
     }
     cudaGraphExec_t exec = nullptr;
@@ -716,7 +733,7 @@ fq_status fq_load_weights(const fq_desc* d, const fq_weight_src* src, void* stre
     gemv_prepare();
     gemm_tc_prepare();
     attention_prepare();
-    persist_prepare();
+    stream_prepare();
     CK(cudaGetLastError());
     fq_model* m = new fq_model();
     m->d = *d;
@@ -786,26 +803,53 @@ fq_status fq_load_weights(const fq_desc* d, const fq_weight_src* src, void* stre
         for (auto& lw : m->layers) {
             attach(lw.qkv); attach(lw.o); attach(lw.gate_up); attach(lw.down); attach(lw.router);
         }
-        // layer table of the persistent batch-1 step (dense models, quantised projections)
-        auto quant = [](const QMat& q) { return q.q && (q.fmt == FMT_Q8_0 || q.fmt == FMT_Q4_K); };
-        const uint32_t G = p.num_attention_heads / p.num_key_value_heads;
-        bool persist_ok = !m->moe() && m->tok_embd.q && quant(m->output) && (G == 1 || G == 2 || G == 4 || G == 8);
-        std::vector<PersistLayer> pl(p.num_layers);
-        for (uint32_t L = 0; L < p.num_layers && persist_ok; ++L) {
-            const LayerW& lw = m->layers[L];
-            persist_ok = quant(lw.qkv) && quant(lw.o) && quant(lw.gate_up) && quant(lw.down);
-            pl[L] = PersistLayer{lw.qkv, lw.o, lw.gate_up, lw.down, lw.attn_norm, lw.ffn_norm, lw.q_norm, lw.k_norm};
-        }
-        if (persist_ok) {
-            PersistLayer* dpl;
-            TRY(dalloc(m->allocs, &dpl, pl.size()));
-            CK(cudaMemcpyAsync(dpl, pl.data(), sizeof(PersistLayer) * pl.size(), cudaMemcpyHostToDevice, s));
-            m->players = dpl;
+        // layer table of the streamed batch-1 step: a dense model whose projections and LM
+        // head share one quantised format, with K % 256 == 0 (whole bulk-copy rows)
+        {
+            const int fmt = m->output.fmt;
+            auto fits = [&](const QMat& q) { return q.q && q.fmt == fmt && q.K % 256 == 0; };
+            const uint32_t G = p.num_attention_heads / p.num_key_value_heads;
+            bool ok = !m->moe() && m->tok_embd.q && m->output.q && (fmt == FMT_Q8_0 || fmt == FMT_Q4_K) &&
+                      m->output.K % 256 == 0 && (G == 1 || G == 2 || G == 4);
+            std::vector<StreamLayer> sl(p.num_layers);
+            for (uint32_t L = 0; L < p.num_layers && ok; ++L) {
+                const LayerW& lw = m->layers[L];
+                ok = fits(lw.qkv) && fits(lw.o) && fits(lw.gate_up) && fits(lw.down);
+                sl[L] = StreamLayer{lw.qkv, lw.o, lw.gate_up, lw.down, lw.attn_norm, lw.ffn_norm, lw.q_norm, lw.k_norm};
+            }
+            StreamArgs& sp = m->splan;
+            sp.n_layers = (int)p.num_layers;
+            sp.H = (int)H;
+            sp.F = (int)p.intermediate_size;
+            sp.Hq = (int)Hq;
+            sp.Hkv = (int)Hkv;
+            sp.V = (int)p.vocab_size;
+            sp.eps = p.rms_norm_eps;
+            sp.emb = m->tok_embd;
+            sp.out = m->output;
+            sp.out_norm = m->output_norm;
+            sp.head = 1;
+            sp.S = stream_chunks((int)Hkv);
+            std::vector<ProjPlan> plans;
+            if (ok && stream_plan(sp, sl[0], fmt, (int)G, plans)) {
+                StreamLayer* dsl;
+                TRY(dalloc(m->allocs, &dsl, sl.size()));
+                CK(cudaMemcpyAsync(dsl, sl.data(), sizeof(StreamLayer) * sl.size(), cudaMemcpyHostToDevice, s));
+                ProjPlan* dpp;
+                TRY(dalloc(m->allocs, &dpp, plans.size()));
+                CK(cudaMemcpyAsync(dpp, plans.data(), sizeof(ProjPlan) * plans.size(), cudaMemcpyHostToDevice, s));
+                m->slayers = dsl;
+                sp.layers = dsl;
+                sp.plan = dpp;
+                m->sfmt = fmt;
+                m->sG = (int)G;
+            }
         }
         m->max_pos = (int)p.max_positions;
         float2* rope;
         TRY(dalloc(m->allocs, &rope, (size_t)m->max_pos * (HEAD_DIM / 2)));
         m->rope = rope;
+        m->splan.rope = rope;
         launch_rope_table(rope, m->max_pos, (double)p.rope_theta, s);
         CK(cudaGetLastError());
         CK(cudaStreamSynchronize(s));
@@ -1103,10 +1147,38 @@ fq_status fq_gemv(const fq_model* m, uint32_t layer, fq_weight_id which, uint32_
     cudaStream_t s = (cudaStream_t)stream;
     Workspace* w = nullptr;
     if (n >= (uint32_t)TC_MIN_BATCH) TRY(ensure_ws(m, s, (int)n, 1, &w));
-    if (w && w->xh && gemm_tc_applicable(g) && !env_flag("FQ_NO_TC"))
+    if (w && w->xh && gemm_tc_applicable(g) && m->opt_tc)
         launch_gemm_tc(g, w->xh, w->tc_part, TC_PART_FLOATS, w->tc_tickets, s, false, false);
     else launch_gemv(g, s, false);
     CK(cudaGetLastError());
+    return FQ_OK;
+}
+
+fq_status fq_set_option(fq_model* m, fq_option opt, int value) {
+    if (!m) return fail(FQ_ERR_INVALID_ARGUMENT, "null model");
+    switch (opt) {
+        case FQ_OPT_STEP_PATH:
+            if (value != FQ_PATH_AUTO && value != FQ_PATH_KERNELS)
+                return fail(FQ_ERR_INVALID_ARGUMENT, "step path %d (FQ_PATH_AUTO or FQ_PATH_KERNELS)", value);
+            m->opt_path = value;
+            break;
+        case FQ_OPT_DEPENDENT_LAUNCH: m->opt_pdl = value != 0; break;
+        case FQ_OPT_GRAPHS: m->opt_graphs = value != 0; break;
+        case FQ_OPT_TENSOR_CORES: m->opt_tc = value != 0; break;
+        default: return fail(FQ_ERR_INVALID_ARGUMENT, "unknown option %d", (int)opt);
+    }
+    // graphs captured under the old setting must not replay
+    std::lock_guard<std::mutex> lk(m->ws_mu);
+    for (auto& kv : m->ws) {
+        cudaStreamSynchronize(kv.first);
+        kv.second->drop_graphs();
+    }
+    return FQ_OK;
+}
+
+fq_status fq_step_path(const fq_model* m, uint32_t n, fq_dtype kv_dtype, int* streamed) {
+    if (!m || !streamed) return fail(FQ_ERR_INVALID_ARGUMENT, "null argument");
+    *streamed = m->slayers && m->opt_path != FQ_PATH_KERNELS && n == 1 && kv_dtype == FQ_BF16 ? 1 : 0;
     return FQ_OK;
 }
 
@@ -1125,9 +1197,30 @@ fq_status fq_check_device(const fq_model* m, void* stream) {
     CK(cudaMemcpyAsync(&host, m->err, sizeof host, cudaMemcpyDeviceToHost, s));
     CK(cudaStreamSynchronize(s));
     if (host) {
+        // A CTA that gave up left its arrival counters and tickets half counted; every
+        // workspace of the model is re-armed on its own stream (after the work queued there)
+        // so that the next step pairs its partial results correctly.
+        fq_model* mm = const_cast<fq_model*>(m);
+        std::lock_guard<std::mutex> lk(mm->ws_mu);
+        for (auto& kv : mm->ws) TRY(rearm_ws(m, kv.second, kv.first));
         CK(cudaMemsetAsync(m->err, 0, sizeof(uint32_t), s));
         return fail(FQ_ERR_DEVICE_TIMEOUT, "a bounded device wait gave up (code %u)", host);
     }
+    return FQ_OK;
+}
+
+fq_status fq_debug_wait_timeout(const fq_model* m, void* stream) {
+    if (!m) return fail(FQ_ERR_INVALID_ARGUMENT, "null model");
+    if (!m->output.q || !m->output.tm || !m->output.tm->ok)
+        return fail(FQ_ERR_UNSUPPORTED, "the model's LM head has no bulk-copy GEMV maps");
+    cudaStream_t s = (cudaStream_t)stream;
+    Workspace* w;
+    TRY(ensure_ws(m, s, 1, 1, &w));
+    GemvArgs g;
+    g.W = m->output; g.B = 1; g.x = w->x; g.x_stride = m->output.K; g.y = w->logits; g.y_stride = m->output.N;
+    g.epi = EPI_STORE; g.err = m->err; g.starve = 1;
+    if (!launch_gemv_tma(g, s, false)) return fail(FQ_ERR_UNSUPPORTED, "bulk-copy GEMV not applicable");
+    CK(cudaGetLastError());
     return FQ_OK;
 }
 
@@ -1211,9 +1304,13 @@ void* g_noalloc_ptr[64] = {};
 // Device address of the array on the current device.  In host code the symbol is only a
 // host-side stand-in, so the address is looked up once per device (with that device
 // current) and cached.
-fq_status noalloc_base(void** out) {
+fq_status noalloc_base(int model_device, void** out) {
     int dev = 0;
     CK(cudaGetDevice(&dev));
+    if (dev != model_device)
+        return fail(FQ_ERR_INVALID_ARGUMENT,
+                    "current device %d is not the model's device %d (the built-in scratch array is per device)", dev,
+                    model_device);
     if (dev < 0 || dev >= 64) return fail(FQ_ERR_INVALID_ARGUMENT, "device %d beyond the scratch table", dev);
     std::lock_guard<std::mutex> lk(g_noalloc_mu);
     if (!g_noalloc_ptr[dev]) {
@@ -1264,7 +1361,7 @@ extern "C" fq_status fq_layer_step_noalloc(const fq_model* m, uint32_t layer, fq
                     "array holds %zu (use fq_layer_step)",
                     off, NOALLOC_SCRATCH_BYTES);
     void* base = nullptr;
-    TRY(noalloc_base(&base));
+    TRY(noalloc_base(m->device, &base));
     unsigned char* b = (unsigned char*)base;
     Workspace w;   // a view into the array; owns nothing
     w.n_cap = 1;

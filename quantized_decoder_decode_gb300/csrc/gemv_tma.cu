@@ -107,7 +107,7 @@ __global__ void __launch_bounds__(THREADS_T, 2) gemv_tma_kernel(const __grid_con
     if (warp == CONSUMER_WARPS) {
         // ---------------- producer: weights only, so no wait for the previous kernel
         constexpr uint32_t STAGE_BYTES = (uint32_t)(Lay::QSTAGE + Lay::SSTAGE);
-        for (int it = 0; it < n_iters; ++it) {
+        for (int it = 0; it < (a.starve ? 0 : n_iters); ++it) {
             const int stage = it % STAGES;
             const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
             if (!mbar_wait(&empty[stage], ph ^ 1u)) {
@@ -306,7 +306,7 @@ bool launch_t(const GemvArgs& a, cudaStream_t s, bool pdl) {
     const int tiles = (a.W.N + C::RT - 1) / C::RT;
     // fewer row tiles than SMs (the 1024-row O and down projections of small models): the
     // register-fed kernel, which also splits K inside a CTA, keeps more SMs streaming
-    if (tiles < g_sms_t) return false;
+    if (tiles < g_sms_t && !a.starve) return false;
     TmaParams prm;
     prm.maps = *a.W.tm;
     prm.a = a;

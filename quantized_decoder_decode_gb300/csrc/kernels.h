@@ -4,6 +4,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <vector>
+
 #ifdef __CUDACC__
 #define FQ_HD __host__ __device__
 #else
@@ -103,6 +105,8 @@ struct GemvArgs {
     int x_by_pair = 0;            // input row = token*moe_k + slot (else token)
     int max_experts = 0;          // grid.y
     uint32_t* err = nullptr;      // device error word: bit set when a bounded wait gave up
+    int starve = 0;               // bulk-copy GEMV only: the producer issues no copies (the
+                                  // consumers' bounded waits run out; used to test the timeout)
 };
 
 void launch_gemv(const GemvArgs& a, cudaStream_t s, bool pdl);
@@ -156,29 +160,47 @@ void launch_attention(const AttnArgs& a, cudaStream_t s, bool pdl);
 // one-time kernel attributes of the attention kernels; call before any graph capture
 void attention_prepare();
 
-// The whole batch-1 step of a dense model as one cooperative persistent kernel (persist.cu).
-struct PersistLayer {
+// The whole batch-1 step of a dense model as one persistent kernel whose producer warps
+// stream the step's weights and cached K/V ahead of the activations (stream_step.cu).
+struct StreamLayer {
     QMat qkv, o, gate_up, down;
     const float *attn_norm, *ffn_norm, *q_norm, *k_norm;
 };
-struct PersistArgs {
-    const PersistLayer* layers;   // device array [n_layers]
-    int n_layers, H, F, Hq, Hkv, V;
-    float eps;
-    QMat emb, out;
-    const float* out_norm;
-    AttnArgs at;                  // attention template: state, scratch, chunking (layer set per layer)
-    float *x, *qkv, *attn, *h;
-    float* logits;                // null: no LM head
-    int greedy;                   // argmax hand-off after the LM head
-    uint32_t* bar;                // grid barrier [2], zero between launches
-    uint32_t* lm_ticket;          // zero between launches
-    uint32_t* err;
+// One CTA's share of one projection (every layer has the same shapes): rows [r0, r1), rows
+// per ring item, and the K split of its tasks (kparts parts of `up` units of U per row).
+struct ProjPlan {
+    int r0, r1, rs, kparts, up, U;
 };
-void persist_prepare();
-int persist_ctas();
-// false when the shapes are not covered or the launch was refused (caller uses the kernels)
-bool launch_persist(const PersistArgs& a, cudaStream_t s);
+enum { P_QKV = 0, P_O = 1, P_GU = 2, P_DN = 3, P_LM = 4, NPROJ = 5 };
+struct StreamArgs {
+    const StreamLayer* layers;    // device array [n_layers]
+    int n_layers = 0, H = 0, F = 0, Hq = 0, Hkv = 0, V = 0;
+    float eps = 1e-6f;
+    QMat emb, out;
+    const float* out_norm = nullptr;
+    const float2* rope = nullptr;
+    StepState* st = nullptr;
+    // exchange words between CTAs (value bits | tag << 32): layer output, attention-block
+    // output, raw QKV, attention partials [Hq][S][130], merged attention, SwiGLU activations
+    unsigned long long *xf = nullptr, *xa = nullptr, *qkv = nullptr, *part = nullptr, *o = nullptr, *h = nullptr;
+    float* logits = nullptr;      // LM-head output [V] or null
+    float* trace_x = nullptr;     // optional: the residual stream after every layer [n_layers][H]
+    int head = 0;                 // run the LM head
+    int greedy = 0;               // argmax hand-off after the LM head
+    uint32_t* ctl = nullptr;      // [0] finishing ticket (zero between launches), [1] launch sequence
+    uint32_t* err = nullptr;
+    int S = 0;                    // attention chunks per kv head
+    const ProjPlan* plan = nullptr;   // device [CTAs][NPROJ]
+    // shared-memory plan (stream_plan)
+    int nslot = 0, kmax = 0, lay_xs = 0, lay_xq = 0, lay_xr = 0, lay_red = 0, lay_bars = 0, smem_bytes = 0;
+};
+void stream_prepare();
+int stream_ctas();
+int stream_chunks(int Hkv);       // S for a model with Hkv kv heads
+// fills the shared-memory plan and the per-CTA projection plans (host [CTAs][NPROJ]);
+// false when the shapes do not fit
+bool stream_plan(StreamArgs& a, const StreamLayer& l0, int fmt, int G, std::vector<ProjPlan>& plans);
+bool launch_stream(const StreamArgs& a, int fmt, int G, cudaStream_t s);
 
 // Embedding rows -> x [n][H]
 void launch_embed(const QMat& emb, const StepState* st, int n, float* x, cudaStream_t s, bool pdl);

@@ -1,0 +1,1170 @@
+// The whole batch-1 decode step of a dense model as one persistent kernel that streams the
+// step's bytes ahead of its dependency chain (sm_103a).
+//
+// forwardStep ("14. Model families", section 14.2) at batch 1 is bound by the bytes it must
+// read: every weight of every layer, the LM head and the cached K/V rows (the fucina README,
+// Performance: single-token decode is bound by the total weight bytes).  None of those bytes
+// depends on the token being decoded -- only the activations do.  So each CTA (one per SM)
+// runs two roles at once:
+//   * a producer warp walks the CTA's fixed share of the whole step -- per layer its rows of
+//     the QKV projection, its chunk of the cached K/V rows, its rows of the O, gate_up and
+//     down projections, then its rows of the LM head -- and copies it into a ring of 16 KB
+//     shared-memory slots with bulk asynchronous copies (cp.async.bulk + mbarrier), as fast
+//     as slots free up.  It never waits for an activation, so HBM keeps streaming while the
+//     consumers wait for the other CTAs;
+//   * eight consumer warps run the step's phases on what has landed.  Per layer:
+//       QKV   RMSNorm(x) . W_qkv rows                        (x: the previous layer's output)
+//       ATT   per-head QK-RMSNorm, half-rope, KV append, attention over the CTA's chunk of
+//             one kv head's cached positions (split-K flash decode; partial m, l, o)
+//       MERGE the chunks of a kv head merged, 8 dimensions per CTA
+//       O     x_att = x + W_o . o
+//       GU    h = silu(W_g . RMSNorm(x_att)) * (W_u . RMSNorm(x_att))  (gate/up rows paired)
+//       DN    x_next = x_att + W_d . h
+//     then the final RMSNorm + LM head with the greedy argmax.
+// Activations cross CTAs as 64-bit exchange words (value bits | tag << 32) written with one
+// store and read with one load: a reader polls the words it needs until every tag is the
+// current (launch, layer) tag, so one L2 round trip carries both the data and its readiness
+// -- no counters, fences or grid barriers.  A buffer is rewritten once per layer, and every
+// reader of a buffer has finished with it before any CTA can write its next version (the
+// layer's later phases depend on all of those readers), so one buffer per activation
+// suffices.  Every wait is bounded; a CTA that gives up records the error word and leaves
+// after its producer has waited for the copies it issued.
+
+#include "common.cuh"
+#include "kernels.h"
+#include "quant.cuh"
+#include "tma.cuh"
+
+#include <algorithm>
+
+namespace fq {
+
+namespace {
+
+constexpr int NW = 15;                // consumer warps (16 warps per CTA: 4 per scheduler, 128 registers)
+constexpr int NC = NW * 32;           // consumer threads
+constexpr int NTH = NC + 32;          // + the producer warp
+constexpr int SLOT = 16384;           // bytes per ring slot
+constexpr int MAXSLOT = 16;
+constexpr int TP = 32;                // cached positions per attention tile (bf16 K and V rows: 8 KB each)
+constexpr int MSL = 16;               // merge slices per kv head (8 dimensions each)
+constexpr int MAXS = 160;             // attention chunks per kv head at most
+constexpr long long BUDGET = 1ll << 29;
+
+// ---------------------------------------------------------------- exchange words
+
+FQ_DEV void xw_store(unsigned long long* p, float v, uint32_t tag) {
+    const unsigned long long w = ((unsigned long long)tag << 32) | (unsigned long long)__float_as_uint(v);
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(w) : "memory");
+}
+FQ_DEV void xw_load2(const unsigned long long* p, unsigned long long& a, unsigned long long& b) {
+    asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "l"(p) : "memory");
+}
+FQ_DEV bool tag_ok(unsigned long long a, unsigned long long b, uint32_t tag) {
+    return (uint32_t)(a >> 32) == tag && (uint32_t)(b >> 32) == tag;
+}
+FQ_DEV uint32_t ld_volatile(const uint32_t* p) { return *reinterpret_cast<const volatile uint32_t*>(p); }
+
+// A launch-wide stop: a CTA that gives up writes `val` (its launch's sequence + 1) to `word`,
+// and every wait of the same launch that sees it gives up too.  The next launch has another
+// sequence, so a failed step does not stop later ones.
+struct Stop {
+    uint32_t* word;
+    uint32_t val;
+    FQ_DEV bool seen() const { return *reinterpret_cast<const volatile uint32_t*>(word) == val; }
+    FQ_DEV void raise() const { atomicExch(word, val); }
+};
+
+// Shared state of one CTA besides the ring.
+struct Ctl {
+    int abort;                        // a wait gave up: every role leaves
+    float inv;                        // 1/rms of the staged input
+    unsigned long long best;          // LM head: this CTA's argmax key
+    int last;                         // this CTA took the last finishing ticket
+};
+
+// Poll n exchange words (n even; src 16-byte aligned) until all carry `tag`, handing each
+// value to put(i, v).  Threads take pairs tid, tid + nthr, ... in batches of four; every
+// round re-issues the loads of all pairs of the batch that are not ready yet, so a batch
+// costs one round trip after its last pair was written.
+template <class Put>
+FQ_DEV bool xw_read(const unsigned long long* src, int n, uint32_t tag, int tid, int nthr, const Stop& stop,
+                    Put put) {
+    constexpr int B = 4;
+    for (int base = 2 * tid; base < n; base += 2 * nthr * B) {
+        unsigned long long a[B], b[B];
+        uint32_t pending = 0;
+#pragma unroll
+        for (int j = 0; j < B; ++j) {
+            const int i = base + 2 * nthr * j;
+            if (i < n) {
+                xw_load2(src + i, a[j], b[j]);
+                pending |= 1u << j;
+            }
+        }
+        long long t0 = 0;
+        int rounds = 0;
+        while (true) {
+#pragma unroll
+            for (int j = 0; j < B; ++j)
+                if ((pending >> j & 1u) && tag_ok(a[j], b[j], tag)) {
+                    const int i = base + 2 * nthr * j;
+                    put(i, __uint_as_float((uint32_t)a[j]));
+                    put(i + 1, __uint_as_float((uint32_t)b[j]));
+                    pending &= ~(1u << j);
+                }
+            if (!pending) break;
+            if (rounds == 0) t0 = clock64();
+            else if (clock64() - t0 > BUDGET) return false;
+            if ((++rounds & 15) == 0 && stop.seen()) return false;
+#pragma unroll
+            for (int j = 0; j < B; ++j)
+                if (pending >> j & 1u) xw_load2(src + base + 2 * nthr * j, a[j], b[j]);
+        }
+    }
+    return true;
+}
+
+// Poll NP pairs of exchange words at p[0], p[1], ... (each 16-byte aligned) until all
+// carry `tag`; every round re-issues the loads of the pairs not ready yet.
+template <int NP>
+FQ_DEV bool xw_read_pairs(const unsigned long long* const (&p)[NP], uint32_t tag, const Stop& stop,
+                          float (&v)[2 * NP]) {
+    unsigned long long a[NP], b[NP];
+#pragma unroll
+    for (int j = 0; j < NP; ++j) xw_load2(p[j], a[j], b[j]);
+    uint32_t pending = (1u << NP) - 1u;
+    long long t0 = 0;
+    int rounds = 0;
+    while (true) {
+#pragma unroll
+        for (int j = 0; j < NP; ++j)
+            if ((pending >> j & 1u) && tag_ok(a[j], b[j], tag)) {
+                v[2 * j] = __uint_as_float((uint32_t)a[j]);
+                v[2 * j + 1] = __uint_as_float((uint32_t)b[j]);
+                pending &= ~(1u << j);
+            }
+        if (!pending) return true;
+        if (rounds == 0) t0 = clock64();
+        else if (clock64() - t0 > BUDGET) return false;
+        if ((++rounds & 15) == 0 && stop.seen()) return false;
+#pragma unroll
+        for (int j = 0; j < NP; ++j)
+            if (pending >> j & 1u) xw_load2(p[j], a[j], b[j]);
+    }
+}
+
+FQ_DEV void csync() { asm volatile("bar.sync 1, %0;" ::"r"(NC) : "memory"); }
+
+inline int align_up(int v, int a) { return (v + a - 1) / a * a; }
+
+// ---------------------------------------------------------------- the step's schedule
+// Producer and consumers derive the same item sequence from these functions.
+
+FQ_HD inline void row_range(int N, bool pairs, int c, int G, int& r0, int& r1) {
+    if (pairs) {
+        const long long P = N / 2;
+        r0 = 2 * (int)(P * c / G);
+        r1 = 2 * (int)(P * (c + 1) / G);
+    } else {
+        r0 = (int)((long long)N * c / G);
+        r1 = (int)((long long)N * (c + 1) / G);
+    }
+}
+
+// bytes of one row in a slot: Q8_0 codes + fp16 scales, or Q4_K super-blocks
+FQ_HD int slot_row_bytes(const QMat& W) { return W.fmt == FMT_Q8_0 ? W.K + W.K / 16 : W.K / 256 * 144; }
+FQ_HD int rows_per_item(const QMat& W) { return SLOT / slot_row_bytes(W); }
+
+// How a phase's rows x K are cut into tasks (R rows x `up` units): the K split that gives the
+// busiest warp the least work, with whole 32-lane passes.
+struct Split {
+    int kparts, up;
+};
+FQ_HD inline Split choose_split(int r0, int r1, int rs, int R, int U) {
+    int groups = 0;
+    for (int r = r0; r < r1; r += rs) groups += ((rs < r1 - r ? rs : r1 - r) + R - 1) / R;
+    const int kmax = (U / 32 > 1 ? U / 32 : 1);
+    Split best{1, U};
+    long long best_cost = -1;
+    for (int kp = 1; kp <= kmax; ++kp) {
+        const int up = ((U + kp - 1) / kp + 31) / 32 * 32;
+        const int kpe = (U + up - 1) / up;
+        const long long cost = (long long)((groups * kpe + NW - 1) / NW) * up;
+        if (best_cost < 0 || cost < best_cost) {
+            best_cost = cost;
+            best = Split{kpe, up};
+        }
+    }
+    return best;
+}
+
+
+
+// the attention unit of this CTA: kv head g, chunk c of S; positions [t0, t1) of T = pos + 1
+struct AttnUnit {
+    bool active;
+    int g, c, t0, t1;
+    int nt, e;        // ring tiles of cached rows [t0, e), e = min(t1, pos)
+};
+FQ_DEV AttnUnit attn_unit_of(int Hkv, int S, int pos) {
+    AttnUnit u;
+    u.active = (int)blockIdx.x < Hkv * S;
+    u.g = blockIdx.x / S;
+    u.c = blockIdx.x % S;
+    const long long T = (long long)pos + 1;
+    u.t0 = (int)(T * u.c / S);
+    u.t1 = (int)(T * (u.c + 1) / S);
+    if (!u.active) u.t0 = u.t1 = 0;
+    u.e = min(u.t1, pos);
+    u.nt = u.e > u.t0 ? (u.e - u.t0 + TP - 1) / TP : 0;
+    return u;
+}
+// ---------------------------------------------------------------- producer
+
+struct Ring {
+    uint8_t* buf;
+    uint64_t* full;
+    uint64_t* empty;
+    int nslot;
+};
+
+struct Producer {
+    Ring r;
+    volatile int* abort;
+    uint32_t* err;
+    Stop stop;
+    uint32_t it = 0;
+
+    FQ_DEV bool wait_free() {
+        const int s = it % r.nslot;
+        const uint32_t ph = ((it / r.nslot) & 1u) ^ 1u;
+        if (mbar_try_wait(&r.empty[s], ph)) return true;
+        const long long t0 = clock64();
+        while (!mbar_try_wait(&r.empty[s], ph)) {
+            __nanosleep(128);   // the ring is full: back off instead of spinning on the barrier
+            if (*abort) return false;
+            if (clock64() - t0 > BUDGET) {
+                atomicOr(err, 128u);
+                stop.raise();
+                *abort = 1;
+                return false;
+            }
+        }
+        return true;
+    }
+    // one item of up to two contiguous byte ranges (sizes multiples of 16) into the next slot
+    FQ_DEV bool item(const void* a, uint32_t an, const void* b, uint32_t bn, uint32_t b_off) {
+        if (!wait_free()) return false;
+        const int s = it % r.nslot;
+        uint8_t* dst = r.buf + (size_t)s * SLOT;
+        mbar_arrive_expect_tx(&r.full[s], an + bn);
+        if (an) bulk_g2s(dst, a, an, &r.full[s]);
+        if (bn) bulk_g2s(dst + b_off, b, bn, &r.full[s]);
+        ++it;
+        return true;
+    }
+    FQ_DEV bool rows(const QMat& W, const ProjPlan& pp) {
+        const int r0 = pp.r0, r1 = pp.r1, rs = pp.rs;
+        for (int r = r0; r < r1; r += rs) {
+            const int nr = min(rs, r1 - r);
+            if (W.fmt == FMT_Q8_0) {
+                if (!item(W.q + (size_t)r * W.K, (uint32_t)nr * W.K, reinterpret_cast<const uint8_t*>(W.s) + (size_t)r * (W.K / 16),
+                          (uint32_t)nr * (W.K / 16), (uint32_t)nr * W.K))
+                    return false;
+            } else {
+                const size_t rb = (size_t)W.K / 256 * 144;
+                if (!item(W.q + (size_t)r * rb, (uint32_t)(nr * rb), nullptr, 0, 0)) return false;
+            }
+        }
+        return true;
+    }
+    FQ_DEV bool kv(const StreamArgs& a, int layer, const SeqState& ss, const AttnUnit& u) {
+        const int nt = u.nt;
+        const int e = u.e;
+        const size_t head = ((size_t)layer * a.Hkv + u.g) * (size_t)ss.cap * HEAD_DIM;
+        const uint16_t* K = reinterpret_cast<const uint16_t*>(ss.k) + head;
+        const uint16_t* V = reinterpret_cast<const uint16_t*>(ss.v) + head;
+        for (int t = 0; t < nt; ++t) {
+            const int tb = u.t0 + t * TP, n = min(TP, e - tb);
+            if (!item(K + (size_t)tb * HEAD_DIM, (uint32_t)n * HEAD_DIM * 2, V + (size_t)tb * HEAD_DIM,
+                      (uint32_t)n * HEAD_DIM * 2, TP * HEAD_DIM * 2))
+                return false;
+        }
+        return true;
+    }
+    // wait until the copies of the last issued items have landed (the CTA must not leave
+    // with copies in flight into its shared memory)
+    FQ_DEV void drain() {
+        const uint32_t n = min((uint32_t)r.nslot, it);
+        for (uint32_t j = it - n; j < it; ++j) {
+            const int s = j % r.nslot;
+            if (!mbar_wait(&r.full[s], (j / r.nslot) & 1u)) atomicOr(err, 256u);
+        }
+    }
+};
+
+FQ_DEV void produce(const StreamArgs& a, Ring ring, volatile int* abort, Stop stop, const ProjPlan* pp,
+                    const AttnUnit& u) {
+    const SeqState ss = a.st->seq[0];
+    Producer p{ring, abort, a.err, stop};
+    // the consumers' phase order (one loop, so that each kind of copy exists once in the code)
+    const int nq = 5 * a.n_layers + (a.head ? 1 : 0);
+    for (int q = 0; q < nq; ++q) {
+        const int L = q / 5, ph = q - 5 * L;
+        const bool lm = L == a.n_layers;
+        const StreamLayer& lw = a.layers[lm ? 0 : L];
+        bool ok;
+        if (ph == 1) {
+            ok = p.kv(a, L, ss, u);
+        } else {
+            const int j = lm ? P_LM : ph == 0 ? P_QKV : ph == 2 ? P_O : ph == 3 ? P_GU : P_DN;
+            const QMat& W = lm ? a.out : ph == 0 ? lw.qkv : ph == 2 ? lw.o : ph == 3 ? lw.gate_up : lw.down;
+            ok = p.rows(W, pp[j]);
+        }
+        if (!ok) break;
+    }
+    p.drain();
+}
+
+// ---------------------------------------------------------------- consumers: projections
+
+struct Cons {
+    Ring ring;
+    Ctl& ctl;
+    uint32_t* err;
+    Stop stop;
+    uint32_t it = 0;           // items consumed so far (same sequence as the producer's)
+
+    // this CTA gives up: record `code`, stop the launch, leave at the next barrier
+    FQ_DEV void fail(uint32_t code) {
+        atomicOr(err, code);
+        stop.raise();
+        ctl.abort = 1;
+    }
+
+    FQ_DEV bool wait_full(int lane) {
+        const int s = it % ring.nslot;
+        const uint32_t ph = (it / ring.nslot) & 1u;
+        if (mbar_try_wait(&ring.full[s], ph)) return true;
+        const long long t0 = clock64();
+        while (!mbar_try_wait(&ring.full[s], ph)) {
+            if (ctl.abort) return false;
+            if (clock64() - t0 > BUDGET) {
+                fail(512u);
+                return false;
+            }
+        }
+        return true;
+    }
+    FQ_DEV const uint8_t* slot() const { return ring.buf + (size_t)(it % ring.nslot) * SLOT; }
+    FQ_DEV void release(int lane) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ring.empty[it % ring.nslot]);
+        ++it;
+    }
+};
+
+// Butterfly sums of R values over the 32 lanes of a warp, transposing as it goes; the sum of
+// value r ends in lane r * (32 / R).
+template <int R>
+FQ_DEV float reduce_rows(float (&v)[R], int lane) {
+    if constexpr (R == 4) {
+        const bool hi = lane & 16;
+        float k0 = hi ? v[2] : v[0], k1 = hi ? v[3] : v[1];
+        const float s0 = hi ? v[0] : v[2], s1 = hi ? v[1] : v[3];
+        k0 += __shfl_xor_sync(0xFFFFFFFFu, s0, 16);
+        k1 += __shfl_xor_sync(0xFFFFFFFFu, s1, 16);
+        const bool h8 = lane & 8;
+        float k = h8 ? k1 : k0;
+        k += __shfl_xor_sync(0xFFFFFFFFu, h8 ? k0 : k1, 8);
+        k += __shfl_xor_sync(0xFFFFFFFFu, k, 4);
+        k += __shfl_xor_sync(0xFFFFFFFFu, k, 2);
+        k += __shfl_xor_sync(0xFFFFFFFFu, k, 1);
+        return k;
+    } else {
+        const bool hi = lane & 16;
+        float k = hi ? v[1] : v[0];
+        k += __shfl_xor_sync(0xFFFFFFFFu, hi ? v[0] : v[1], 16);
+        k += __shfl_xor_sync(0xFFFFFFFFu, k, 8);
+        k += __shfl_xor_sync(0xFFFFFFFFu, k, 4);
+        k += __shfl_xor_sync(0xFFFFFFFFu, k, 2);
+        k += __shfl_xor_sync(0xFFFFFFFFu, k, 1);
+        return k;
+    }
+}
+
+// ---------------------------------------------------------------- staged input of a projection
+// The input vector of a projection (times its RMSNorm gain) is staged once per phase as
+// 16-bit block fixed point: per block of 32 elements (the Q8_0 block, the Q4_K sub-block) a
+// float scale s = max|x| / 32767 and integers v = round(x / s) in [-32767, 32767], stored as
+// two byte planes hi = v >> 8 (signed) and lo = v & 255 (unsigned), v = 256 hi + lo.  A dot
+// product with integer weight codes then runs on dp4a, exact in integers, and
+// sum_k q_k x_k = s (256 sum q hi + sum q lo) up to the rounding of x, at most s / 2 per
+// element (a relative 1.5e-5 of the block's largest value).
+struct XStage {
+    float* xs;        // [K] floats of the input (times the gain), before quantisation
+    int8_t* hi;       // [K] high bytes, in the format's unit layout
+    uint8_t* lo;      // [K] low bytes
+    float* sc;        // [K / 32] block scales
+    float* sum32;     // [K / 32] Q4_K: float sums of the input per sub-block (the min term)
+};
+
+// Byte index of element e in the unit layout: Q8_0 units (16 elements per lane) are plain
+// runs; Q4_K units (64 elements per lane) are split into four 16-byte pieces stored
+// piece-major, so that the lanes of a warp reading piece p of consecutive units hit
+// consecutive 16-byte words.
+template <int FMT>
+FQ_DEV int xq_index(int e, int K) {
+    if constexpr (FMT == FMT_Q8_0) return e;
+    else return ((e & 63) >> 4) * (K >> 2) + (e >> 6) * 16 + (e & 15);
+}
+
+FQ_DEV int dp4a_ss(uint32_t a, uint32_t b, int c) {
+    int d;
+    asm("dp4a.s32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+FQ_DEV int dp4a_su(uint32_t a, uint32_t b, int c) {
+    int d;
+    asm("dp4a.s32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+FQ_DEV int dp4a_us(uint32_t a, uint32_t b, int c) {
+    int d;
+    asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+FQ_DEV int dp4a_uu(uint32_t a, uint32_t b, int c) {
+    int d;
+    asm("dp4a.u32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+template <int FMT> struct PCfg;
+// rows per task R; elements per unit (one lane's share of a row per pass)
+template <> struct PCfg<FMT_Q8_0> { static constexpr int R = 4, UE = 16; };
+template <> struct PCfg<FMT_Q4_K> { static constexpr int R = 2, UE = 64; };
+
+// R rows of an item (rows row0.. of its nr rows), units [ua, ub) of each row: lane takes units
+// ua + lane, ua + lane + 32, ...  Returns per-row partial sums before the warp reduction.
+template <int FMT>
+FQ_DEV void task_dot(const uint8_t* slot, int nr, int K, int row0, int ua, int ub, int lane, const XStage& x,
+                     float (&acc)[PCfg<FMT>::R]) {
+    constexpr int R = PCfg<FMT>::R;
+#pragma unroll
+    for (int r = 0; r < R; ++r) acc[r] = 0.f;
+    if constexpr (FMT == FMT_Q8_0) {
+        const uint16_t* sc = reinterpret_cast<const uint16_t*>(slot + (size_t)nr * K);
+        const int K32 = K >> 5;
+        for (int u = ua + lane; u < ub; u += 32) {
+            const uint4 h = *reinterpret_cast<const uint4*>(x.hi + 16 * u);
+            const uint4 l = *reinterpret_cast<const uint4*>(x.lo + 16 * u);
+            const float s = x.sc[u >> 1];
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                const int row = row0 + r;
+                if (row < nr) {
+                    const uint4 c = *reinterpret_cast<const uint4*>(slot + (size_t)row * K + 16 * u);
+                    const float d = h2f(sc[row * K32 + (u >> 1)]);
+                    int A = dp4a_ss(c.x, h.x, 0);
+                    A = dp4a_ss(c.y, h.y, A);
+                    A = dp4a_ss(c.z, h.z, A);
+                    A = dp4a_ss(c.w, h.w, A);
+                    int B = dp4a_su(c.x, l.x, 0);
+                    B = dp4a_su(c.y, l.y, B);
+                    B = dp4a_su(c.z, l.z, B);
+                    B = dp4a_su(c.w, l.w, B);
+                    acc[r] = fmaf(d * s, (float)(A * 256 + B), acc[r]);
+                }
+            }
+        }
+    } else {
+        const int rb = K / 256 * 144;
+        const int P = K >> 2;   // bytes per piece plane
+        for (int u = ua + lane; u < ub; u += 32) {   // 64-element unit: nibble chunk c of super-block u / 4
+            const int c = u & 3;
+            const int e0 = (u >> 2) * 256 + 64 * c;
+            // pieces 0, 1: the low-nibble sub-block (elements e0 .. e0 + 31); 2, 3: the high one
+            uint4 h[4], l[4];
+#pragma unroll
+            for (int p = 0; p < 4; ++p) {
+                h[p] = *reinterpret_cast<const uint4*>(x.hi + p * P + 16 * u);
+                l[p] = *reinterpret_cast<const uint4*>(x.lo + p * P + 16 * u);
+            }
+            const float s_lo = x.sc[e0 >> 5], s_hi = x.sc[(e0 >> 5) + 1];
+            const float m_lo = x.sum32[e0 >> 5], m_hi = x.sum32[(e0 >> 5) + 1];
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                const int row = row0 + r;
+                if (row >= nr) break;
+                const uint8_t* blk = slot + (size_t)row * rb + (u >> 2) * 144;
+                const uint4 hdr = *reinterpret_cast<const uint4*>(blk);
+                const uint4 q0 = *reinterpret_cast<const uint4*>(blk + 16 + 32 * c);
+                const uint4 q1 = *reinterpret_cast<const uint4*>(blk + 32 + 32 * c);
+                const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+                int Alo = 0, Blo = 0, Ahi = 0, Bhi = 0;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const uint32_t qlo = w[i] & 0x0F0F0F0Fu, qhi = (w[i] >> 4) & 0x0F0F0F0Fu;
+                    const uint4& hl = h[i >> 2];
+                    const uint4& ll = l[i >> 2];
+                    const uint4& hh = h[2 + (i >> 2)];
+                    const uint4& lh = l[2 + (i >> 2)];
+                    const int k = i & 3;
+                    Alo = dp4a_us(qlo, (&hl.x)[k], Alo);
+                    Blo = dp4a_uu(qlo, (&ll.x)[k], Blo);
+                    Ahi = dp4a_us(qhi, (&hh.x)[k], Ahi);
+                    Bhi = dp4a_uu(qhi, (&lh.x)[k], Bhi);
+                }
+                const float d = h2f((unsigned short)(hdr.x & 0xFFFFu));
+                const float dmin = h2f((unsigned short)(hdr.x >> 16));
+                const uint32_t W0 = hdr.y, W1 = hdr.z, W2 = hdr.w;
+                uint32_t sc0, mn0, sc1, mn1;
+                if (c < 2) {
+                    const uint32_t sh = 16u * c;
+                    sc0 = (W0 >> sh) & 63u; sc1 = (W0 >> (sh + 8)) & 63u;
+                    mn0 = (W1 >> sh) & 63u; mn1 = (W1 >> (sh + 8)) & 63u;
+                } else {
+                    const uint32_t sh = 16u * (c - 2);
+                    const uint32_t a0 = W2 >> sh, b0 = W0 >> sh, b1 = W1 >> sh;
+                    sc0 = (a0 & 15u) | ((b0 >> 2) & 48u); sc1 = ((a0 >> 8) & 15u) | ((b0 >> 10) & 48u);
+                    mn0 = ((a0 >> 4) & 15u) | ((b1 >> 2) & 48u); mn1 = ((a0 >> 12) & 15u) | ((b1 >> 10) & 48u);
+                }
+                acc[r] += d * (float)sc0 * s_lo * (float)(Alo * 256 + Blo) - dmin * (float)mn0 * m_lo +
+                          d * (float)sc1 * s_hi * (float)(Ahi * 256 + Bhi) - dmin * (float)mn1 * m_hi;
+            }
+        }
+    }
+}
+
+// Rows [r0, r1) of W times the staged input: every item of the phase is waited for and
+// released by every consumer warp in order; the phase's tasks (R rows of one item x one K
+// part) go to the warps round-robin.  Partial sums land in red[row - r0][kpart]; returns the
+// number of K parts (0 when a wait gave up).
+template <int FMT>
+FQ_DEV int proj_tasks(Cons& cs, const QMat& W, const ProjPlan& pp, const XStage& x, float* red) {
+    constexpr int R = PCfg<FMT>::R;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int r0 = pp.r0, r1 = pp.r1, rs = pp.rs, U = pp.U;
+    const Split sp{pp.kparts, pp.up};
+    int owner = 0;   // warp of the next task
+    for (int r = r0; r < r1; r += rs) {
+        const int nr = min(rs, r1 - r);
+        if (!cs.wait_full(lane)) return 0;
+        const uint8_t* slot = cs.slot();
+        for (int g = 0; g < nr; g += R)
+            for (int kp = 0; kp < sp.kparts; ++kp) {
+                if (owner == warp) {
+                    float acc[R];
+                    task_dot<FMT>(slot, nr, W.K, g, kp * sp.up, min(U, (kp + 1) * sp.up), lane, x, acc);
+                    const float s = reduce_rows<R>(acc, lane);
+                    const int rr = lane / (32 / R);
+                    if ((lane & (32 / R - 1)) == 0 && g + rr < nr) red[(size_t)(r - r0 + g + rr) * sp.kparts + kp] = s;
+                }
+                owner = owner + 1 == NW ? 0 : owner + 1;
+            }
+        cs.release(lane);
+    }
+    return sp.kparts;
+}
+
+// ---------------------------------------------------------------- consumers: attention
+
+// q / k head held as 4 dims per lane (dims 4l..4l+3) by one warp: RMSNorm with the gain,
+// then the rotate-half RoPE (pairs (i, i + 64): lane l < 16 holds i, lane l + 16 holds i + 64)
+FQ_DEV void norm_rope4(float v[4], const float* gain, const float2* rope_row, float eps, int lane) {
+    float ss = v[0] * v[0] + v[1] * v[1] + v[2] * v[2] + v[3] * v[3];
+    ss = warp_sum(ss);
+    const float inv = rsqrtf(ss / (float)HEAD_DIM + eps);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) v[j] = v[j] * inv * gain[4 * lane + j];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const float partner = __shfl_xor_sync(0xFFFFFFFFu, v[j], 16);
+        const float2 cs = rope_row[(4 * lane + j) & 63];
+        v[j] = lane < 16 ? v[j] * cs.x - partner * cs.y : partner * cs.y + v[j] * cs.x;
+    }
+}
+
+// Shared memory of the attention phase (inside the staging area).  The arrays read or
+// written with 16-byte vector accesses come first, each a multiple of 16 bytes long.
+template <int G>
+struct alignas(16) AttSmem {
+    float qs[G][HEAD_DIM];            // normalised, rotated, scaled by log2(e)/sqrt(D)
+    float ow[NW][G][HEAD_DIM];        // per-warp accumulators for the cross-warp merge
+    uint16_t kv_new[2][HEAD_DIM];     // the new position's k and v as stored (bf16)
+    float mw[NW][G], lw[NW][G];
+    float pm[G][MAXS], pl[G][MAXS];   // merge: (m, l) of every chunk of the kv head
+    float po[G * MAXS * 8];           //        and its 8 dimensions of the slice
+};
+static_assert(sizeof(float) * HEAD_DIM % 16 == 0, "vector-accessed attention arrays stay 16-byte aligned");
+
+// One warp's online-softmax state over the positions it has seen.  q lives in registers for
+// up to two heads per kv head (lane (j, i): dims 8i..8i+7 and 64+8i..64+8i+7 of every head),
+// else it is read from shared memory as it is used.
+constexpr int QREG_MAX_G = 2;
+template <int G>
+struct WarpAtt {
+    float q[G <= QREG_MAX_G ? G : 1][16];
+    float m[G], l[G], acc[G][4];      // acc: dims 4 lane .. 4 lane + 3
+};
+
+// Positions 4 quad + (lane >> 3) of a tile of n valid rows: K rows at kb, V rows at vb, both
+// bf16 rows of 128 dims (256 bytes).  8 lanes share a position, 16 dims each.
+template <int G>
+FQ_DEV void att_quad(WarpAtt<G>& w, const float (*qs)[HEAD_DIM], const uint8_t* kb, const uint8_t* vb, int n, int quad,
+                     int lane) {
+    const int j = lane >> 3, i = lane & 7;
+    const int row = 4 * quad + j;
+    const bool valid = row < n;
+    float s[G];
+#pragma unroll
+    for (int h = 0; h < G; ++h) s[h] = 0.f;
+    if (valid) {
+        const uint4 a = *reinterpret_cast<const uint4*>(kb + (size_t)row * 256 + 16 * i);
+        const uint4 b = *reinterpret_cast<const uint4*>(kb + (size_t)row * 256 + 128 + 16 * i);
+        const float k[16] = {bf_lo(a.x), bf_hi(a.x), bf_lo(a.y), bf_hi(a.y), bf_lo(a.z), bf_hi(a.z),
+                             bf_lo(a.w), bf_hi(a.w), bf_lo(b.x), bf_hi(b.x), bf_lo(b.y), bf_hi(b.y),
+                             bf_lo(b.z), bf_hi(b.z), bf_lo(b.w), bf_hi(b.w)};
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+            float q[16];
+            if constexpr (G <= QREG_MAX_G) {
+#pragma unroll
+                for (int e = 0; e < 16; ++e) q[e] = w.q[h][e];
+            } else {
+                const float4* q0 = reinterpret_cast<const float4*>(&qs[h][8 * i]);
+                const float4* q1 = reinterpret_cast<const float4*>(&qs[h][64 + 8 * i]);
+                const float4 x0 = q0[0], x1 = q0[1], x2 = q1[0], x3 = q1[1];
+                q[0] = x0.x; q[1] = x0.y; q[2] = x0.z; q[3] = x0.w; q[4] = x1.x; q[5] = x1.y; q[6] = x1.z; q[7] = x1.w;
+                q[8] = x2.x; q[9] = x2.y; q[10] = x2.z; q[11] = x2.w; q[12] = x3.x; q[13] = x3.y; q[14] = x3.z;
+                q[15] = x3.w;
+            }
+            float t0 = 0.f, t1 = 0.f;
+#pragma unroll
+            for (int e = 0; e < 16; e += 2) {
+                t0 = fmaf(q[e], k[e], t0);
+                t1 = fmaf(q[e + 1], k[e + 1], t1);
+            }
+            s[h] = t0 + t1;
+        }
+    }
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+        s[h] += __shfl_xor_sync(0xFFFFFFFFu, s[h], 4);
+        s[h] += __shfl_xor_sync(0xFFFFFFFFu, s[h], 2);
+        s[h] += __shfl_xor_sync(0xFFFFFFFFu, s[h], 1);
+        if (!valid) s[h] = -INFINITY;
+    }
+    float p[G];
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+        float mt = fmaxf(s[h], __shfl_xor_sync(0xFFFFFFFFu, s[h], 8));
+        mt = fmaxf(mt, __shfl_xor_sync(0xFFFFFFFFu, mt, 16));
+        const float mn = fmaxf(w.m[h], mt);
+        if (mn == -INFINITY) {             // nothing seen yet and no valid row here
+            p[h] = 0.f;
+            continue;
+        }
+        const float corr = exp2f(w.m[h] - mn);
+        p[h] = valid ? exp2f(s[h] - mn) : 0.f;
+        float ps = p[h] + __shfl_xor_sync(0xFFFFFFFFu, p[h], 8);
+        ps += __shfl_xor_sync(0xFFFFFFFFu, ps, 16);
+        w.l[h] = w.l[h] * corr + ps;
+        w.m[h] = mn;
+#pragma unroll
+        for (int d = 0; d < 4; ++d) w.acc[h][d] *= corr;
+    }
+#pragma unroll
+    for (int jj = 0; jj < 4; ++jj) {
+        if (4 * quad + jj >= n) break;
+        const uint2 v = *reinterpret_cast<const uint2*>(vb + (size_t)(4 * quad + jj) * 256 + 8 * lane);
+        const float vf[4] = {bf_lo(v.x), bf_hi(v.x), bf_lo(v.y), bf_hi(v.y)};
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+            const float pj = __shfl_sync(0xFFFFFFFFu, p[h], 8 * jj);
+#pragma unroll
+            for (int d = 0; d < 4; ++d) w.acc[h][d] = fmaf(pj, vf[d], w.acc[h][d]);
+        }
+    }
+}
+
+// ---------------------------------------------------------------- consumers: phases
+
+// Shared scratch of the consumers besides the staging area.
+struct CtlX {
+    float wsum[NW];
+};
+
+// Stage an input vector of K values (times `gain` when given; its raw values into xr when
+// asked), then quantise it into the 16-bit block fixed point of XStage; returns 1/rms when a
+// gain is given, else 1.  src == null: the embedding row of `tok` instead of exchange words.
+template <int FMT>
+FQ_DEV float stage(const StreamArgs& a, const unsigned long long* src, int K, uint32_t tag,
+                                   const float* gain, bool keep_raw, const XStage& x, float* xr, Cons& cs, CtlX& cx,
+                                   int64_t tok = 0) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    csync();
+    float ss = 0.f;
+    auto put = [&](int i, float v) {
+        ss += v * v;
+        if (keep_raw) xr[i] = v;
+        x.xs[i] = gain ? v * gain[i] : v;
+    };
+    if (src) {
+        if (!xw_read(src, K, tag, tid, NC, cs.stop, put)) {
+            if (cs.stop.seen()) cs.ctl.abort = 1;   // another CTA gave up
+            else cs.fail(1024u);
+        }
+    } else {
+        for (int i = tid; i < K; i += NC) put(i, dequant_one(a.emb, tok, i));
+    }
+    ss = warp_sum(ss);
+    if (lane == 0) cx.wsum[warp] = ss;
+    csync();
+    // blocks of 32: 8 lanes per block, 4 elements per lane
+    const int nblk = K >> 5;
+    for (int base = 4 * warp; base < nblk; base += 4 * NW) {
+        const int blk = base + (lane >> 3), j = lane & 7;
+        const bool on = blk < nblk;
+        const float4 v = on ? reinterpret_cast<const float4*>(x.xs)[blk * 8 + j] : make_float4(0.f, 0.f, 0.f, 0.f);
+        float am = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+        float sm = (v.x + v.y) + (v.z + v.w);
+        am = fmaxf(am, __shfl_xor_sync(0xFFFFFFFFu, am, 1));
+        am = fmaxf(am, __shfl_xor_sync(0xFFFFFFFFu, am, 2));
+        am = fmaxf(am, __shfl_xor_sync(0xFFFFFFFFu, am, 4));
+        sm += __shfl_xor_sync(0xFFFFFFFFu, sm, 1);
+        sm += __shfl_xor_sync(0xFFFFFFFFu, sm, 2);
+        sm += __shfl_xor_sync(0xFFFFFFFFu, sm, 4);
+        if (!on) continue;
+        const float inv = am > 0.f ? 32767.f / am : 0.f;
+        const float e[4] = {v.x, v.y, v.z, v.w};
+        uint32_t hw = 0, lw = 0;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int q = max(-32767, min(32767, __float2int_rn(e[k] * inv)));
+            hw |= (uint32_t)(q >> 8 & 0xFF) << (8 * k);
+            lw |= (uint32_t)(q & 0xFF) << (8 * k);
+        }
+        const int at = xq_index<FMT>(blk * 32 + 4 * j, K);
+        *reinterpret_cast<uint32_t*>(x.hi + at) = hw;
+        *reinterpret_cast<uint32_t*>(x.lo + at) = lw;
+        if (j == 0) {
+            x.sc[blk] = am / 32767.f;
+            if (FMT == FMT_Q4_K) x.sum32[blk] = sm;
+        }
+    }
+    float tot = 0.f;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) tot += cx.wsum[w];
+    csync();
+    return gain ? rsqrtf(tot / (float)K + a.eps) : 1.f;
+}
+
+FQ_DEV uint32_t tag_of(uint32_t seq, int layer) { return (seq << 8) | (uint32_t)(layer + 1); }
+
+// Attention of this CTA's unit plus the merge of its kv head's chunks (8 dims per slice).
+template <int G>
+FQ_DEV void attention_phase(const StreamArgs& a, const StreamLayer& lw, int layer, const SeqState& ss, uint32_t tag,
+                            Cons& cs, AttSmem<G>& as, const AttnUnit& u) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int S = a.S;
+    csync();
+    if (u.active && warp < G + 2) {
+        // q heads of the group, then k and v of the kv head, from the QKV exchange words
+        const int row = warp < G ? (u.g * G + warp) : warp == G ? (a.Hq + u.g) : (a.Hq + a.Hkv + u.g);
+        float v[4];
+        const unsigned long long* src = a.qkv + (size_t)row * HEAD_DIM + 4 * lane;
+        const unsigned long long* const pp[2] = {src, src + 2};
+        if (!xw_read_pairs<2>(pp, tag, cs.stop, v)) {
+            if (cs.stop.seen()) cs.ctl.abort = 1;
+            else cs.fail(2048u);
+        }
+        const float2* rope_row = a.rope + (size_t)ss.pos * (HEAD_DIM / 2);
+        if (warp < G) {
+            norm_rope4(v, lw.q_norm, rope_row, a.eps, lane);
+            const float qscale = 1.4426950408889634f * rsqrtf((float)HEAD_DIM);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) as.qs[warp][4 * lane + j] = v[j] * qscale;
+        } else {
+            if (warp == G) norm_rope4(v, lw.k_norm, rope_row, a.eps, lane);
+            const int which = warp - G;   // 0: k, 1: v
+            uint16_t* dst = reinterpret_cast<uint16_t*>(warp == G ? ss.k : ss.v) +
+                            (((size_t)layer * a.Hkv + u.g) * (size_t)ss.cap + ss.pos) * HEAD_DIM;
+            const bool owner = u.c == S - 1;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const uint16_t b = __bfloat16_as_ushort(__float2bfloat16_rn(v[j]));
+                as.kv_new[which][4 * lane + j] = b;
+                if (owner) dst[4 * lane + j] = b;
+            }
+        }
+    }
+    csync();
+    if (cs.ctl.abort || !u.active) {
+        // an inactive CTA carries no attention items
+        return;
+    }
+    WarpAtt<G> w;
+    {
+        const int i = lane & 7;
+        if constexpr (G <= QREG_MAX_G) {
+#pragma unroll
+            for (int h = 0; h < G; ++h)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    w.q[h][e] = as.qs[h][8 * i + e];
+                    w.q[h][8 + e] = as.qs[h][64 + 8 * i + e];
+                }
+        }
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+            w.m[h] = -INFINITY;
+            w.l[h] = 0.f;
+#pragma unroll
+            for (int d = 0; d < 4; ++d) w.acc[h][d] = 0.f;
+        }
+    }
+    const int nt = u.nt;
+    const int e = u.e;
+    // quads (4 positions) of every tile go to the warps round-robin: global quad g to warp g % NW
+    // (tile nt, one row from shared memory: the new position of the unit that owns it)
+    constexpr int QPT = TP / 4;   // quads per tile
+    const int ntiles = nt + (u.c == S - 1 ? 1 : 0);
+    int owner = 0;                // warp of the next quad
+    for (int t = 0; t < ntiles; ++t) {
+        const bool ring_tile = t < nt;
+        if (ring_tile && !cs.wait_full(lane)) break;
+        const int n = ring_tile ? min(TP, e - (u.t0 + t * TP)) : 1;
+        const uint8_t* kb = ring_tile ? cs.slot() : reinterpret_cast<const uint8_t*>(as.kv_new[0]);
+        const uint8_t* vb = ring_tile ? kb + TP * HEAD_DIM * 2 : reinterpret_cast<const uint8_t*>(as.kv_new[1]);
+        for (int qd = 0; 4 * qd < n; ++qd) {
+            if (owner == warp) att_quad<G>(w, as.qs, kb, vb, n, qd, lane);
+            owner = owner + 1 == NW ? 0 : owner + 1;
+        }
+        if (ring_tile) cs.release(lane);
+    }
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+        if (lane == 0) {
+            as.mw[warp][h] = w.m[h];
+            as.lw[warp][h] = w.l[h];
+        }
+        *reinterpret_cast<float4*>(&as.ow[warp][h][4 * lane]) =
+            make_float4(w.acc[h][0], w.acc[h][1], w.acc[h][2], w.acc[h][3]);
+    }
+    csync();
+    if (cs.ctl.abort) return;
+    for (int t = tid; t < G * HEAD_DIM; t += NC) {
+        const int h = t / HEAD_DIM, d = t % HEAD_DIM;
+        float M = -INFINITY;
+#pragma unroll
+        for (int ww = 0; ww < NW; ++ww) M = fmaxf(M, as.mw[ww][h]);
+        float Lsum = 0.f, O = 0.f;
+        if (M != -INFINITY) {
+#pragma unroll
+            for (int ww = 0; ww < NW; ++ww) {
+                const float c = exp2f(as.mw[ww][h] - M);
+                Lsum = fmaf(as.lw[ww][h], c, Lsum);
+                O = fmaf(as.ow[ww][h][d], c, O);
+            }
+        }
+        unsigned long long* p = a.part + ((size_t)(u.g * G + h) * S + u.c) * (HEAD_DIM + 2);
+        if (d == 0) {
+            xw_store(p, M, tag);
+            xw_store(p + 1, Lsum, tag);
+        }
+        xw_store(p + 2 + d, O, tag);
+    }
+    // ---- merge: slice sl (dims 8 sl .. 8 sl + 7) of the group's heads, slices u.c, u.c + S, ...
+    for (int sl = u.c; sl < MSL; sl += S) {
+        csync();
+        if (cs.ctl.abort) return;
+        for (int t = tid; t < G * S; t += NC) {
+            const int h = t / S, c = t % S;
+            const unsigned long long* p = a.part + ((size_t)(u.g * G + h) * S + c) * (HEAD_DIM + 2);
+            float v[10];
+            const unsigned long long* o8 = p + 2 + 8 * sl;
+            const unsigned long long* const pp[5] = {p, o8, o8 + 2, o8 + 4, o8 + 6};
+            if (!xw_read_pairs<5>(pp, tag, cs.stop, v)) {
+                if (cs.stop.seen()) cs.ctl.abort = 1;
+                else cs.fail(4096u);
+            }
+            as.pm[h][c] = v[0];
+            as.pl[h][c] = v[1];
+            float* po = &as.po[(h * S + c) * 8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) po[k] = v[2 + k];
+        }
+        csync();
+        if (cs.ctl.abort) return;
+        if (tid < G * 8) {
+            const int h = tid / 8, k = tid % 8;
+            float M = -INFINITY;
+            for (int c = 0; c < S; ++c) M = fmaxf(M, as.pm[h][c]);
+            float Lsum = 0.f, O = 0.f;
+            for (int c = 0; c < S; ++c) {
+                const float m = as.pm[h][c];
+                if (m == -INFINITY) continue;
+                const float wgt = exp2f(m - M);
+                Lsum = fmaf(as.pl[h][c], wgt, Lsum);
+                O = fmaf(as.po[(h * S + c) * 8 + k], wgt, O);
+            }
+            xw_store(a.o + (size_t)(u.g * G + h) * HEAD_DIM + 8 * sl + k, O / Lsum, tag);
+        }
+    }
+}
+
+}  // namespace
+
+template <int FMT, int G>
+__global__ void __launch_bounds__(NTH) stream_step_kernel(const __grid_constant__ StreamArgs a) {
+    extern __shared__ __align__(1024) uint8_t smem[];
+    __shared__ Ctl ctl;
+    __shared__ CtlX cx;
+    __shared__ ProjPlan pp[NPROJ];
+    __shared__ AttnUnit au;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + a.lay_bars);
+    Ring ring{smem, bars, bars + MAXSLOT, a.nslot};
+    float* xs = reinterpret_cast<float*>(smem + a.lay_xs);
+    XStage xq;
+    xq.xs = xs;
+    xq.hi = reinterpret_cast<int8_t*>(smem + a.lay_xq);
+    xq.lo = reinterpret_cast<uint8_t*>(smem + a.lay_xq + a.kmax);
+    xq.sc = reinterpret_cast<float*>(smem + a.lay_xq + 2 * a.kmax);
+    xq.sum32 = xq.sc + a.kmax / 32;
+    float* xr = reinterpret_cast<float*>(smem + a.lay_xr);
+    float* red = reinterpret_cast<float*>(smem + a.lay_red);
+    if (tid == 0) {
+        for (int s = 0; s < a.nslot; ++s) {
+            mbar_init(&ring.full[s], 1);
+            mbar_init(&ring.empty[s], NW);
+        }
+        mbar_fence_init();
+        ctl.abort = 0;
+        ctl.best = 0ull;
+        ctl.last = 0;
+        au = attn_unit_of(a.Hkv, a.S, a.st->seq[0].pos);
+    }
+    if (tid < NPROJ) pp[tid] = a.plan[blockIdx.x * NPROJ + tid];
+    __syncthreads();
+    const uint32_t seq = ld_volatile(&a.ctl[1]) & 0xFFFFFFu;
+    const Stop stop{a.ctl + 2, seq + 1u};
+    if (warp == NW) {
+        if (lane == 0) produce(a, ring, &ctl.abort, stop, pp, au);
+        return;
+    }
+
+    const SeqState ss = a.st->seq[0];
+    const int64_t tok = (ss.token >= 0 && ss.token < a.emb.N) ? ss.token : 0;
+    Cons cs{ring, ctl, a.err, stop};
+    AttSmem<G>& as = *reinterpret_cast<AttSmem<G>*>(xs);
+
+    // The step as one loop over phases, so that every phase body exists once in the code:
+    // q = 5 L + {0: RMSNorm + QKV, 1: attention, 2: O + residual, 3: RMSNorm + gate_up +
+    // SwiGLU, 4: down + residual}; q = 5 n_layers: final RMSNorm + LM head.
+    const int nq = 5 * a.n_layers + (a.head ? 1 : 0);
+    float inv = 1.f;
+    for (int q = 0; q < nq && !ctl.abort; ++q) {
+        const int L = q / 5, ph = q - 5 * L;
+        const bool lm = L == a.n_layers;
+        const StreamLayer& lw = a.layers[lm ? 0 : L];
+        const uint32_t tag = tag_of(seq, L);
+        if (ph == 1) {
+            attention_phase<G>(a, lw, L, ss, tag, cs, as, au);
+            csync();
+            continue;
+        }
+        // ---- a projection phase: its matrix, input, gain and plan
+        const int j = lm ? P_LM : ph == 0 ? P_QKV : ph == 2 ? P_O : ph == 3 ? P_GU : P_DN;
+        const QMat& W = lm ? a.out : ph == 0 ? lw.qkv : ph == 2 ? lw.o : ph == 3 ? lw.gate_up : lw.down;
+        const unsigned long long* src = lm ? a.xf : ph == 0 ? (L == 0 ? nullptr : a.xf) : ph == 2 ? a.o
+                                                                                               : ph == 3 ? a.xa : a.h;
+        const uint32_t tag_in = (lm || ph == 0) ? tag_of(seq, L - 1) : tag;
+        const float* gain = lm ? a.out_norm : ph == 0 ? lw.attn_norm : ph == 3 ? lw.ffn_norm : nullptr;
+        const bool keep_raw = ph == 0 || ph == 3;   // the residual for the next add
+        const float inv_p = stage<FMT>(a, src, W.K, tag_in, gain, keep_raw, xq, xr, cs, cx, tok);
+        if (gain) inv = inv_p;
+        if (ctl.abort) break;
+        const ProjPlan& P = pp[j];
+        if (!proj_tasks<FMT>(cs, W, P, xq, red)) ctl.abort = 1;
+        csync();
+        if (ctl.abort) break;
+        // ---- epilogue over this CTA's rows
+        const int kparts = P.kparts;
+        const int step = ph == 3 && !lm ? 2 : 1;   // gate/up rows come in pairs
+        unsigned long long kb = 0ull;
+        for (int r = P.r0 + step * tid; r < P.r1; r += step * NC) {
+            float y = 0.f, y2 = 0.f;
+            for (int k = 0; k < kparts; ++k) y += red[(r - P.r0) * kparts + k];
+            if (step == 2)
+                for (int k = 0; k < kparts; ++k) y2 += red[(r + 1 - P.r0) * kparts + k];
+            if (lm) {
+                y *= inv;
+                if (a.logits) a.logits[r] = y;
+                const unsigned long long key = argmax_key(y, (uint32_t)r);
+                kb = key > kb ? key : kb;
+            } else if (ph == 0) {
+                xw_store(a.qkv + r, y * inv, tag);
+            } else if (ph == 2) {
+                xw_store(a.xa + r, xr[r] + y, tag);
+            } else if (ph == 3) {
+                xw_store(a.h + r / 2, silu(y * inv) * (y2 * inv), tag);
+            } else {
+                const float xn = xr[r] + y;
+                xw_store(a.xf + r, xn, tag);
+                if (a.trace_x) a.trace_x[(size_t)L * a.H + r] = xn;
+            }
+        }
+        if (lm && a.greedy) {
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const unsigned long long other = __shfl_xor_sync(0xFFFFFFFFu, kb, o);
+                kb = other > kb ? other : kb;
+            }
+            if (lane == 0 && kb) atomicMax(&ctl.best, kb);
+        }
+    }
+
+    // ---- finishing ticket: the last CTA hands the greedy token on and advances the launch
+    // sequence (every CTA takes it, also after a failure, so the sequence stays in step)
+    csync();
+    if (tid == 0) {
+        StepState* st = a.st;
+        if (a.greedy && ctl.best) atomicMax(&st->keys[0], ctl.best);
+        __threadfence();
+        const uint32_t t = atomicAdd(&a.ctl[0], 1u);
+        if (t == gridDim.x - 1) {
+            __threadfence();
+            a.ctl[0] = 0u;
+            if (a.greedy) {
+                const unsigned long long k = atomicExch(&st->keys[0], 0ull);
+                const uint32_t idx = argmax_key_index(k);
+                const int32_t tk = idx < (uint32_t)a.V ? (int32_t)idx : 0;
+                st->seq[0].token = tk;
+                st->seq[0].pos += 1;
+                if (st->tokens_out) st->tokens_out[st->step] = tk;
+                st->step += 1;
+            }
+            __threadfence();
+            atomicAdd(&a.ctl[1], 1u);
+        }
+    }
+}
+
+namespace {
+
+int g_sms_s = 0;
+int g_optin_s = 0;
+
+template <int FMT, int G>
+bool launch_fg(const StreamArgs& a, cudaStream_t s) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(g_sms_s);
+    cfg.blockDim = dim3(NTH);
+    cfg.dynamicSmemBytes = a.smem_bytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, stream_step_kernel<FMT, G>, a) == cudaSuccess;
+}
+
+template <int FMT, int G>
+void prepare_fg() {
+    cudaFuncAttributes fa;
+    cudaFuncGetAttributes(&fa, stream_step_kernel<FMT, G>);
+    cudaFuncSetAttribute(stream_step_kernel<FMT, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         g_optin_s - (int)fa.sharedSizeBytes);
+}
+
+}  // namespace
+
+void stream_prepare() {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&g_sms_s, cudaDevAttrMultiProcessorCount, dev);
+    cudaDeviceGetAttribute(&g_optin_s, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    prepare_fg<FMT_Q8_0, 1>();
+    prepare_fg<FMT_Q8_0, 2>();
+    prepare_fg<FMT_Q8_0, 4>();
+    prepare_fg<FMT_Q4_K, 1>();
+    prepare_fg<FMT_Q4_K, 2>();
+    prepare_fg<FMT_Q4_K, 4>();
+}
+
+int stream_ctas() { return g_sms_s; }
+
+int stream_chunks(int Hkv) { return g_sms_s > 0 && Hkv > 0 ? g_sms_s / Hkv : 0; }
+
+bool stream_plan(StreamArgs& a, const StreamLayer& l0, int fmt, int G, std::vector<ProjPlan>& plans) {
+    if (g_sms_s == 0 || a.S < 1 || a.S > MAXS) return false;
+    {
+        const int R = fmt == FMT_Q8_0 ? PCfg<FMT_Q8_0>::R : PCfg<FMT_Q4_K>::R;
+        const int UE = fmt == FMT_Q8_0 ? PCfg<FMT_Q8_0>::UE : PCfg<FMT_Q4_K>::UE;
+        const QMat* mats[NPROJ] = {&l0.qkv, &l0.o, &l0.gate_up, &l0.down, &a.out};
+        plans.assign((size_t)g_sms_s * NPROJ, ProjPlan{});
+        for (int c = 0; c < g_sms_s; ++c)
+            for (int j = 0; j < NPROJ; ++j) {
+                const QMat& W = *mats[j];
+                ProjPlan& q = plans[(size_t)c * NPROJ + j];
+                row_range(W.N, j == P_GU, c, g_sms_s, q.r0, q.r1);
+                q.rs = rows_per_item(W);
+                q.U = W.K / UE;
+                const Split sp = choose_split(q.r0, q.r1, q.rs, R, q.U);
+                q.kparts = sp.kparts;
+                q.up = sp.up;
+            }
+    }
+    const int kmax = std::max({a.H, a.F, a.Hq * HEAD_DIM});
+    int red = 0;   // floats of per-(row, K part) partial sums: the largest share of a CTA
+    for (const ProjPlan& q : plans)
+        if (q.r1 > q.r0) red = std::max(red, (q.r1 - q.r0) * q.kparts);
+    size_t att = 0;
+    switch (G) {
+        case 1: att = sizeof(AttSmem<1>); break;
+        case 2: att = sizeof(AttSmem<2>); break;
+        case 4: att = sizeof(AttSmem<4>); break;
+        default: return false;
+    }
+    const int xs_bytes = std::max(kmax * 4, (int)att);               // float staging / attention scratch
+    const int xq_bytes = 2 * kmax + 2 * (kmax / 32) * 4;              // hi, lo planes; block scales and sums
+    const int fixed = align_up(xs_bytes, 16) + align_up(xq_bytes, 16) + align_up(a.H * 4, 16) +
+                      align_up(red * 4, 16) + 2 * MAXSLOT * 8;
+    const int avail = g_optin_s - 1024 - fixed;   // static shared memory of the kernel
+    const int nslot = std::min(MAXSLOT, avail / SLOT);
+    if (nslot < 4) return false;
+    a.nslot = nslot;
+    a.kmax = kmax;
+    a.lay_xs = nslot * SLOT;
+    a.lay_xq = a.lay_xs + align_up(xs_bytes, 16);
+    a.lay_xr = a.lay_xq + align_up(xq_bytes, 16);
+    a.lay_red = a.lay_xr + align_up(a.H * 4, 16);
+    a.lay_bars = a.lay_red + align_up(red * 4, 16);
+    a.smem_bytes = a.lay_bars + 2 * MAXSLOT * 8;
+    return true;
+}
+
+bool launch_stream(const StreamArgs& a, int fmt, int G, cudaStream_t s) {
+    if (g_sms_s == 0) return false;
+    if (fmt == FMT_Q8_0) {
+        switch (G) {
+            case 1: return launch_fg<FMT_Q8_0, 1>(a, s);
+            case 2: return launch_fg<FMT_Q8_0, 2>(a, s);
+            case 4: return launch_fg<FMT_Q8_0, 4>(a, s);
+        }
+    } else if (fmt == FMT_Q4_K) {
+        switch (G) {
+            case 1: return launch_fg<FMT_Q4_K, 1>(a, s);
+            case 2: return launch_fg<FMT_Q4_K, 2>(a, s);
+            case 4: return launch_fg<FMT_Q4_K, 4>(a, s);
+        }
+    }
+    return false;
+}
+
+}  // namespace fq

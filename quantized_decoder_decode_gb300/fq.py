@@ -92,6 +92,9 @@ def lib():
                 "fq_layer_step_trace": [vp, u32, vp, u32, vp, vp, vp, vp, vp],
                 "fq_gemv": [vp, u32, ctypes.c_int, u32, vp, vp, vp],
                 "fq_check_device": [vp, vp],
+                "fq_debug_wait_timeout": [vp, vp],
+                "fq_set_option": [vp, ctypes.c_int, ctypes.c_int],
+                "fq_step_path": [vp, u32, ctypes.c_int, ctypes.POINTER(ctypes.c_int)],
                 "fq_step_kernels": [vp, vp, ctypes.POINTER(ctypes.c_uint32)],
                 "fq_layer_step_noalloc": [vp, u32, vp, u32, vp, vp],
             }
@@ -118,7 +121,7 @@ def lib():
 EXPORTED = ("fq_desc_init", "fq_load_weights", "fq_model_free", "fq_kv_init", "fq_kv_free", "fq_kv_len",
             "fq_kv_capacity", "fq_kv_append", "fq_kv_commit", "fq_kv_rewind", "fq_kv_read", "fq_layer_step", "fq_decode_step",
             "fq_decode_step_batch", "fq_decode_step_all_logits", "fq_forward_step", "fq_decode_greedy", "fq_decode_step_trace", "fq_dequant_rows", "fq_quantize_q8_0", "fq_layer_step_trace",
-            "fq_gemv", "fq_step_kernels", "fq_check_device", "fq_layer_step_noalloc", "fq_last_error",
+            "fq_gemv", "fq_step_kernels", "fq_check_device", "fq_debug_wait_timeout", "fq_set_option", "fq_step_path", "fq_layer_step_noalloc", "fq_last_error",
             "fq_status_str")
 
 
@@ -303,6 +306,26 @@ def fq_step_kernels(model: int, stream: int = 0) -> int:
 
 def fq_check_device(model: int, stream: int = 0) -> None:
     _check(lib().fq_check_device(model, stream), "fq_check_device")
+
+
+OPT_STEP_PATH, OPT_DEPENDENT_LAUNCH, OPT_GRAPHS, OPT_TENSOR_CORES = range(4)
+PATH_AUTO, PATH_KERNELS = 0, 1
+
+
+def fq_set_option(model: int, opt: int, value: int) -> None:
+    _check(lib().fq_set_option(model, opt, int(value)), "fq_set_option")
+
+
+def fq_step_path(model: int, n: int, kv_dtype: str) -> bool:
+    """True when a step of n sequences with a kv_dtype cache runs as the streamed kernel."""
+    out = ctypes.c_int(0)
+    _check(lib().fq_step_path(model, n, DTYPES[kv_dtype], ctypes.byref(out)), "fq_step_path")
+    return bool(out.value)
+
+
+def fq_debug_wait_timeout(model: int, stream: int = 0) -> None:
+    """Test hook: make every bounded wait of one LM-head GEMV launch run out."""
+    _check(lib().fq_debug_wait_timeout(model, stream), "fq_debug_wait_timeout")
 
 
 def fq_layer_step_noalloc(model: int, layer: int, kv: int, pos: int, x_ptr: int, stream: int = 0) -> None:

@@ -208,7 +208,9 @@ def test_all_logits_step_contract(pair_factory):
 
 
 def test_graph_replay_equals_direct_launches(pair_factory):
+    # the kernel sequence captured once and replayed, against the same kernels launched directly
     p = pair_factory(workload(SMALL_G4, "q8_0", "bf16"), max_positions=512, with_oracle=False)
+    fq.fq_set_option(p.model, fq.OPT_STEP_PATH, fq.PATH_KERNELS)
     a, _ = p.new_seq(capacity=256, ctx=150, seq=0, oracle_cache=False)
     b, _ = p.new_seq(capacity=256, ctx=150, seq=0, oracle_cache=False)
     la = torch.empty(SMALL_G4.vocab_size, dtype=torch.float32, device=DEV)
