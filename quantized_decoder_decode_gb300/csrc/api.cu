@@ -830,6 +830,7 @@ fq_status fq_load_weights(const fq_desc* d, const fq_weight_src* src, void* stre
             sp.out_norm = m->output_norm;
             sp.head = 1;
             sp.S = stream_chunks((int)Hkv);
+            sp.max_pos = (int)p.max_positions;
             std::vector<ProjPlan> plans;
             if (ok && stream_plan(sp, sl[0], fmt, (int)G, plans)) {
                 StreamLayer* dsl;

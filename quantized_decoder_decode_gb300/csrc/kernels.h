@@ -190,6 +190,8 @@ struct StreamArgs {
     uint32_t* ctl = nullptr;      // [0] finishing ticket (zero between launches), [1] launch sequence
     uint32_t* err = nullptr;
     int S = 0;                    // attention chunks per kv head
+    int max_pos = 0;              // cache capacity the plan covers (positions)
+    int score_cap = 0;            // attention scores per head the shared memory holds
     const ProjPlan* plan = nullptr;   // device [CTAs][NPROJ]
     // shared-memory plan (stream_plan)
     int nslot = 0, kmax = 0, lay_xs = 0, lay_xq = 0, lay_xr = 0, lay_red = 0, lay_bars = 0, smem_bytes = 0;

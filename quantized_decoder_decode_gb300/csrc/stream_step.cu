@@ -41,12 +41,12 @@ namespace fq {
 
 namespace {
 
-constexpr int NW = 15;                // consumer warps (16 warps per CTA: 4 per scheduler, 128 registers)
+constexpr int NW = 8;                 // consumer warps (a power of two)
 constexpr int NC = NW * 32;           // consumer threads
 constexpr int NTH = NC + 32;          // + the producer warp
 constexpr int SLOT = 16384;           // bytes per ring slot
 constexpr int MAXSLOT = 16;
-constexpr int TP = 32;                // cached positions per attention tile (bf16 K and V rows: 8 KB each)
+constexpr int TP = 64;                // cached positions per attention item (64 bf16 rows of K or of V: 16 KB)
 constexpr int MSL = 16;               // merge slices per kv head (8 dimensions each)
 constexpr int MAXS = 160;             // attention chunks per kv head at most
 constexpr long long BUDGET = 1ll << 29;
@@ -84,21 +84,25 @@ struct Ctl {
 };
 
 // Poll n exchange words (n even; src 16-byte aligned) until all carry `tag`, handing each
-// value to put(i, v).  Threads take pairs tid, tid + nthr, ... in batches of four; every
-// round re-issues the loads of all pairs of the batch that are not ready yet, so a batch
-// costs one round trip after its last pair was written.
+// pair to put(i, v_i, v_i+1, g_i, g_i+1) with the matching pair of `gain` (1 without one).
+// Threads take pairs tid, tid + nthr, ... in batches of eight; the gains of a batch are loaded
+// with its first round, and every round re-issues the loads of the pairs that are not ready
+// yet, so a batch costs one round trip after its last pair was written.
 template <class Put>
 FQ_DEV bool xw_read(const unsigned long long* src, int n, uint32_t tag, int tid, int nthr, const Stop& stop,
-                    Put put) {
-    constexpr int B = 4;
+                    const float* gain, Put put) {
+    constexpr int B = 8;
     for (int base = 2 * tid; base < n; base += 2 * nthr * B) {
         unsigned long long a[B], b[B];
+        float2 g[B];
         uint32_t pending = 0;
 #pragma unroll
         for (int j = 0; j < B; ++j) {
             const int i = base + 2 * nthr * j;
+            g[j] = make_float2(1.f, 1.f);
             if (i < n) {
                 xw_load2(src + i, a[j], b[j]);
+                if (gain) g[j] = *reinterpret_cast<const float2*>(gain + i);
                 pending |= 1u << j;
             }
         }
@@ -108,9 +112,7 @@ FQ_DEV bool xw_read(const unsigned long long* src, int n, uint32_t tag, int tid,
 #pragma unroll
             for (int j = 0; j < B; ++j)
                 if ((pending >> j & 1u) && tag_ok(a[j], b[j], tag)) {
-                    const int i = base + 2 * nthr * j;
-                    put(i, __uint_as_float((uint32_t)a[j]));
-                    put(i + 1, __uint_as_float((uint32_t)b[j]));
+                    put(base + 2 * nthr * j, __uint_as_float((uint32_t)a[j]), __uint_as_float((uint32_t)b[j]), g[j]);
                     pending &= ~(1u << j);
                 }
             if (!pending) break;
@@ -191,7 +193,7 @@ FQ_HD inline Split choose_split(int r0, int r1, int rs, int R, int U) {
         const int up = ((U + kp - 1) / kp + 31) / 32 * 32;
         const int kpe = (U + up - 1) / up;
         const long long cost = (long long)((groups * kpe + NW - 1) / NW) * up;
-        if (best_cost < 0 || cost < best_cost) {
+        if (best_cost < 0 || cost * 10 < best_cost * 9) {
             best_cost = cost;
             best = Split{kpe, up};
         }
@@ -217,7 +219,7 @@ FQ_DEV AttnUnit attn_unit_of(int Hkv, int S, int pos) {
     u.t1 = (int)(T * (u.c + 1) / S);
     if (!u.active) u.t0 = u.t1 = 0;
     u.e = min(u.t1, pos);
-    u.nt = u.e > u.t0 ? (u.e - u.t0 + TP - 1) / TP : 0;
+    u.nt = u.e > u.t0 ? (u.e - u.t0 + TP - 1) / TP : 0;   // K items, then as many V items
     return u;
 }
 // ---------------------------------------------------------------- producer
@@ -285,11 +287,10 @@ struct Producer {
         const size_t head = ((size_t)layer * a.Hkv + u.g) * (size_t)ss.cap * HEAD_DIM;
         const uint16_t* K = reinterpret_cast<const uint16_t*>(ss.k) + head;
         const uint16_t* V = reinterpret_cast<const uint16_t*>(ss.v) + head;
-        for (int t = 0; t < nt; ++t) {
-            const int tb = u.t0 + t * TP, n = min(TP, e - tb);
-            if (!item(K + (size_t)tb * HEAD_DIM, (uint32_t)n * HEAD_DIM * 2, V + (size_t)tb * HEAD_DIM,
-                      (uint32_t)n * HEAD_DIM * 2, TP * HEAD_DIM * 2))
-                return false;
+        for (int t = 0; t < 2 * nt; ++t) {   // the chunk's K rows, then its V rows
+            const int tb = u.t0 + (t % nt) * TP, n = min(TP, e - tb);
+            const uint16_t* src = (t < nt ? K : V) + (size_t)tb * HEAD_DIM;
+            if (!item(src, (uint32_t)n * HEAD_DIM * 2, nullptr, 0, 0)) return false;
         }
         return true;
     }
@@ -444,7 +445,7 @@ FQ_DEV int dp4a_uu(uint32_t a, uint32_t b, int c) {
 template <int FMT> struct PCfg;
 // rows per task R; elements per unit (one lane's share of a row per pass)
 template <> struct PCfg<FMT_Q8_0> { static constexpr int R = 4, UE = 16; };
-template <> struct PCfg<FMT_Q4_K> { static constexpr int R = 2, UE = 64; };
+template <> struct PCfg<FMT_Q4_K> { static constexpr int R = 4, UE = 64; };
 
 // R rows of an item (rows row0.. of its nr rows), units [ua, ub) of each row: lane takes units
 // ua + lane, ua + lane + 32, ...  Returns per-row partial sums before the warp reduction.
@@ -457,6 +458,7 @@ FQ_DEV void task_dot(const uint8_t* slot, int nr, int K, int row0, int ua, int u
     if constexpr (FMT == FMT_Q8_0) {
         const uint16_t* sc = reinterpret_cast<const uint16_t*>(slot + (size_t)nr * K);
         const int K32 = K >> 5;
+#pragma unroll 2
         for (int u = ua + lane; u < ub; u += 32) {
             const uint4 h = *reinterpret_cast<const uint4*>(x.hi + 16 * u);
             const uint4 l = *reinterpret_cast<const uint4*>(x.lo + 16 * u);
@@ -482,6 +484,7 @@ FQ_DEV void task_dot(const uint8_t* slot, int nr, int K, int row0, int ua, int u
     } else {
         const int rb = K / 256 * 144;
         const int P = K >> 2;   // bytes per piece plane
+#pragma unroll 2
         for (int u = ua + lane; u < ub; u += 32) {   // 64-element unit: nibble chunk c of super-block u / 4
             const int c = u & 3;
             const int e0 = (u >> 2) * 256 + 64 * c;
@@ -547,26 +550,25 @@ FQ_DEV int proj_tasks(Cons& cs, const QMat& W, const ProjPlan& pp, const XStage&
     constexpr int R = PCfg<FMT>::R;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int r0 = pp.r0, r1 = pp.r1, rs = pp.rs, U = pp.U;
-    const Split sp{pp.kparts, pp.up};
-    int owner = 0;   // warp of the next task
+    const int kparts = pp.kparts, up = pp.up;
+    int first = warp;   // this warp's first task of the current item (tasks go round-robin)
     for (int r = r0; r < r1; r += rs) {
         const int nr = min(rs, r1 - r);
+        const int ntask = (nr + R - 1) / R * kparts;
         if (!cs.wait_full(lane)) return 0;
         const uint8_t* slot = cs.slot();
-        for (int g = 0; g < nr; g += R)
-            for (int kp = 0; kp < sp.kparts; ++kp) {
-                if (owner == warp) {
-                    float acc[R];
-                    task_dot<FMT>(slot, nr, W.K, g, kp * sp.up, min(U, (kp + 1) * sp.up), lane, x, acc);
-                    const float s = reduce_rows<R>(acc, lane);
-                    const int rr = lane / (32 / R);
-                    if ((lane & (32 / R - 1)) == 0 && g + rr < nr) red[(size_t)(r - r0 + g + rr) * sp.kparts + kp] = s;
-                }
-                owner = owner + 1 == NW ? 0 : owner + 1;
-            }
+        for (int t = first; t < ntask; t += NW) {
+            const int g = t / kparts * R, kp = t - t / kparts * kparts;
+            float acc[R];
+            task_dot<FMT>(slot, nr, W.K, g, kp * up, min(U, (kp + 1) * up), lane, x, acc);
+            const float s = reduce_rows<R>(acc, lane);
+            const int rr = lane / (32 / R);
+            if ((lane & (32 / R - 1)) == 0 && g + rr < nr) red[(size_t)(r - r0 + g + rr) * kparts + kp] = s;
+        }
+        first = (first - ntask) & (NW - 1);
         cs.release(lane);
     }
-    return sp.kparts;
+    return kparts;
 }
 
 // ---------------------------------------------------------------- consumers: attention
@@ -587,105 +589,76 @@ FQ_DEV void norm_rope4(float v[4], const float* gain, const float2* rope_row, fl
     }
 }
 
-// Shared memory of the attention phase (inside the staging area).  The arrays read or
-// written with 16-byte vector accesses come first, each a multiple of 16 bytes long.
+// Shared memory of the attention phase (inside the staging area); the scores of the chunk's
+// positions follow the struct, [G][score capacity].
 template <int G>
 struct alignas(16) AttSmem {
     float qs[G][HEAD_DIM];            // normalised, rotated, scaled by log2(e)/sqrt(D)
-    float ow[NW][G][HEAD_DIM];        // per-warp accumulators for the cross-warp merge
+    float ow[NW][G][HEAD_DIM];        // per-warp V sums for the cross-warp reduction
     uint16_t kv_new[2][HEAD_DIM];     // the new position's k and v as stored (bf16)
-    float mw[NW][G], lw[NW][G];
+    float hm[G], hl[G];               // per head: max score, sum of exp2(score - max)
     float pm[G][MAXS], pl[G][MAXS];   // merge: (m, l) of every chunk of the kv head
     float po[G * MAXS * 8];           //        and its 8 dimensions of the slice
+    float sc[1];                      // scores / weights [G][cap], cap = the plan's score capacity
 };
 static_assert(sizeof(float) * HEAD_DIM % 16 == 0, "vector-accessed attention arrays stay 16-byte aligned");
+static_assert((NW & (NW - 1)) == 0 && NW >= 4, "task rotation uses NW - 1 as a mask; the prologue needs G + 2 warps");
 
-// One warp's online-softmax state over the positions it has seen.  q lives in registers for
-// up to two heads per kv head (lane (j, i): dims 8i..8i+7 and 64+8i..64+8i+7 of every head),
-// else it is read from shared memory as it is used.
-constexpr int QREG_MAX_G = 2;
+// Scores of K rows row = 32 step + 4 warp + (lane >> 3) of an item of n rows (8 lanes per row,
+// 16 dims each: 8i..8i+7 and 64+8i..64+8i+7); lane i == h of the row's group writes head h's
+// score to sc[h][base + row].
 template <int G>
-struct WarpAtt {
-    float q[G <= QREG_MAX_G ? G : 1][16];
-    float m[G], l[G], acc[G][4];      // acc: dims 4 lane .. 4 lane + 3
-};
-
-// Positions 4 quad + (lane >> 3) of a tile of n valid rows: K rows at kb, V rows at vb, both
-// bf16 rows of 128 dims (256 bytes).  8 lanes share a position, 16 dims each.
-template <int G>
-FQ_DEV void att_quad(WarpAtt<G>& w, const float (*qs)[HEAD_DIM], const uint8_t* kb, const uint8_t* vb, int n, int quad,
-                     int lane) {
+FQ_DEV void att_scores(const float (&q)[G][16], const uint8_t* kb, int n, int base, float* sc, int cap, int warp,
+                       int lane) {
     const int j = lane >> 3, i = lane & 7;
-    const int row = 4 * quad + j;
-    const bool valid = row < n;
-    float s[G];
 #pragma unroll
-    for (int h = 0; h < G; ++h) s[h] = 0.f;
-    if (valid) {
-        const uint4 a = *reinterpret_cast<const uint4*>(kb + (size_t)row * 256 + 16 * i);
-        const uint4 b = *reinterpret_cast<const uint4*>(kb + (size_t)row * 256 + 128 + 16 * i);
-        const float k[16] = {bf_lo(a.x), bf_hi(a.x), bf_lo(a.y), bf_hi(a.y), bf_lo(a.z), bf_hi(a.z),
-                             bf_lo(a.w), bf_hi(a.w), bf_lo(b.x), bf_hi(b.x), bf_lo(b.y), bf_hi(b.y),
-                             bf_lo(b.z), bf_hi(b.z), bf_lo(b.w), bf_hi(b.w)};
+    for (int step = 0; step < TP / (4 * NW); ++step) {
+        const int row = 32 * step + 4 * warp + j;
+        if (32 * step + 4 * warp >= n) break;   // the whole group of four rows is past the end
+        const bool valid = row < n;
+        float s[G];
+#pragma unroll
+        for (int h = 0; h < G; ++h) s[h] = 0.f;
+        if (valid) {
+            const uint4 a = *reinterpret_cast<const uint4*>(kb + (size_t)row * 256 + 16 * i);
+            const uint4 b = *reinterpret_cast<const uint4*>(kb + (size_t)row * 256 + 128 + 16 * i);
+            const float k[16] = {bf_lo(a.x), bf_hi(a.x), bf_lo(a.y), bf_hi(a.y), bf_lo(a.z), bf_hi(a.z),
+                                 bf_lo(a.w), bf_hi(a.w), bf_lo(b.x), bf_hi(b.x), bf_lo(b.y), bf_hi(b.y),
+                                 bf_lo(b.z), bf_hi(b.z), bf_lo(b.w), bf_hi(b.w)};
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+                float t0 = 0.f, t1 = 0.f;
+#pragma unroll
+                for (int e = 0; e < 16; e += 2) {
+                    t0 = fmaf(q[h][e], k[e], t0);
+                    t1 = fmaf(q[h][e + 1], k[e + 1], t1);
+                }
+                s[h] = t0 + t1;
+            }
+        }
 #pragma unroll
         for (int h = 0; h < G; ++h) {
-            float q[16];
-            if constexpr (G <= QREG_MAX_G) {
-#pragma unroll
-                for (int e = 0; e < 16; ++e) q[e] = w.q[h][e];
-            } else {
-                const float4* q0 = reinterpret_cast<const float4*>(&qs[h][8 * i]);
-                const float4* q1 = reinterpret_cast<const float4*>(&qs[h][64 + 8 * i]);
-                const float4 x0 = q0[0], x1 = q0[1], x2 = q1[0], x3 = q1[1];
-                q[0] = x0.x; q[1] = x0.y; q[2] = x0.z; q[3] = x0.w; q[4] = x1.x; q[5] = x1.y; q[6] = x1.z; q[7] = x1.w;
-                q[8] = x2.x; q[9] = x2.y; q[10] = x2.z; q[11] = x2.w; q[12] = x3.x; q[13] = x3.y; q[14] = x3.z;
-                q[15] = x3.w;
-            }
-            float t0 = 0.f, t1 = 0.f;
-#pragma unroll
-            for (int e = 0; e < 16; e += 2) {
-                t0 = fmaf(q[e], k[e], t0);
-                t1 = fmaf(q[e + 1], k[e + 1], t1);
-            }
-            s[h] = t0 + t1;
+            s[h] += __shfl_xor_sync(0xFFFFFFFFu, s[h], 4);
+            s[h] += __shfl_xor_sync(0xFFFFFFFFu, s[h], 2);
+            s[h] += __shfl_xor_sync(0xFFFFFFFFu, s[h], 1);
+            if (valid && i == h) sc[h * cap + base + row] = s[h];
         }
     }
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-        s[h] += __shfl_xor_sync(0xFFFFFFFFu, s[h], 4);
-        s[h] += __shfl_xor_sync(0xFFFFFFFFu, s[h], 2);
-        s[h] += __shfl_xor_sync(0xFFFFFFFFu, s[h], 1);
-        if (!valid) s[h] = -INFINITY;
-    }
-    float p[G];
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-        float mt = fmaxf(s[h], __shfl_xor_sync(0xFFFFFFFFu, s[h], 8));
-        mt = fmaxf(mt, __shfl_xor_sync(0xFFFFFFFFu, mt, 16));
-        const float mn = fmaxf(w.m[h], mt);
-        if (mn == -INFINITY) {             // nothing seen yet and no valid row here
-            p[h] = 0.f;
-            continue;
-        }
-        const float corr = exp2f(w.m[h] - mn);
-        p[h] = valid ? exp2f(s[h] - mn) : 0.f;
-        float ps = p[h] + __shfl_xor_sync(0xFFFFFFFFu, p[h], 8);
-        ps += __shfl_xor_sync(0xFFFFFFFFu, ps, 16);
-        w.l[h] = w.l[h] * corr + ps;
-        w.m[h] = mn;
-#pragma unroll
-        for (int d = 0; d < 4; ++d) w.acc[h][d] *= corr;
-    }
-#pragma unroll
-    for (int jj = 0; jj < 4; ++jj) {
-        if (4 * quad + jj >= n) break;
-        const uint2 v = *reinterpret_cast<const uint2*>(vb + (size_t)(4 * quad + jj) * 256 + 8 * lane);
+}
+
+// V rows warp, warp + NW, ... of an item of n rows weighted by p = sc[h][base + row]: lane
+// takes dims 4 lane .. 4 lane + 3 of every head.
+template <int G>
+FQ_DEV void att_values(float (&acc)[G][4], const uint8_t* vb, int n, int base, const float* sc, int cap, int warp,
+                       int lane) {
+    for (int row = warp; row < n; row += NW) {
+        const uint2 v = *reinterpret_cast<const uint2*>(vb + (size_t)row * 256 + 8 * lane);
         const float vf[4] = {bf_lo(v.x), bf_hi(v.x), bf_lo(v.y), bf_hi(v.y)};
 #pragma unroll
         for (int h = 0; h < G; ++h) {
-            const float pj = __shfl_sync(0xFFFFFFFFu, p[h], 8 * jj);
+            const float p = sc[h * cap + base + row];
 #pragma unroll
-            for (int d = 0; d < 4; ++d) w.acc[h][d] = fmaf(pj, vf[d], w.acc[h][d]);
+            for (int d = 0; d < 4; ++d) acc[h][d] = fmaf(p, vf[d], acc[h][d]);
         }
     }
 }
@@ -707,18 +680,20 @@ FQ_DEV float stage(const StreamArgs& a, const unsigned long long* src, int K, ui
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     csync();
     float ss = 0.f;
-    auto put = [&](int i, float v) {
-        ss += v * v;
-        if (keep_raw) xr[i] = v;
-        x.xs[i] = gain ? v * gain[i] : v;
+    auto put = [&](int i, float v0, float v1, float2 g) {
+        ss += v0 * v0 + v1 * v1;
+        if (keep_raw) *reinterpret_cast<float2*>(xr + i) = make_float2(v0, v1);
+        *reinterpret_cast<float2*>(x.xs + i) = make_float2(v0 * g.x, v1 * g.y);
     };
     if (src) {
-        if (!xw_read(src, K, tag, tid, NC, cs.stop, put)) {
+        if (!xw_read(src, K, tag, tid, NC, cs.stop, gain, put)) {
             if (cs.stop.seen()) cs.ctl.abort = 1;   // another CTA gave up
             else cs.fail(1024u);
         }
     } else {
-        for (int i = tid; i < K; i += NC) put(i, dequant_one(a.emb, tok, i));
+        for (int i = 2 * tid; i < K; i += 2 * NC)
+            put(i, dequant_one(a.emb, tok, i), dequant_one(a.emb, tok, i + 1),
+                gain ? *reinterpret_cast<const float2*>(gain + i) : make_float2(1.f, 1.f));
     }
     ss = warp_sum(ss);
     if (lane == 0) cx.wsum[warp] = ss;
@@ -806,74 +781,79 @@ FQ_DEV void attention_phase(const StreamArgs& a, const StreamLayer& lw, int laye
         // an inactive CTA carries no attention items
         return;
     }
-    WarpAtt<G> w;
-    {
-        const int i = lane & 7;
-        if constexpr (G <= QREG_MAX_G) {
-#pragma unroll
-            for (int h = 0; h < G; ++h)
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    w.q[h][e] = as.qs[h][8 * i + e];
-                    w.q[h][8 + e] = as.qs[h][64 + 8 * i + e];
-                }
-        }
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-            w.m[h] = -INFINITY;
-            w.l[h] = 0.f;
-#pragma unroll
-            for (int d = 0; d < 4; ++d) w.acc[h][d] = 0.f;
-        }
-    }
     const int nt = u.nt;
-    const int e = u.e;
-    // quads (4 positions) of every tile go to the warps round-robin: global quad g to warp g % NW
-    // (tile nt, one row from shared memory: the new position of the unit that owns it)
-    constexpr int QPT = TP / 4;   // quads per tile
-    const int ntiles = nt + (u.c == S - 1 ? 1 : 0);
-    int owner = 0;                // warp of the next quad
-    for (int t = 0; t < ntiles; ++t) {
-        const bool ring_tile = t < nt;
-        if (ring_tile && !cs.wait_full(lane)) break;
-        const int n = ring_tile ? min(TP, e - (u.t0 + t * TP)) : 1;
-        const uint8_t* kb = ring_tile ? cs.slot() : reinterpret_cast<const uint8_t*>(as.kv_new[0]);
-        const uint8_t* vb = ring_tile ? kb + TP * HEAD_DIM * 2 : reinterpret_cast<const uint8_t*>(as.kv_new[1]);
-        for (int qd = 0; 4 * qd < n; ++qd) {
-            if (owner == warp) att_quad<G>(w, as.qs, kb, vb, n, qd, lane);
-            owner = owner + 1 == NW ? 0 : owner + 1;
-        }
-        if (ring_tile) cs.release(lane);
-    }
+    const int n = u.e - u.t0 > 0 ? u.e - u.t0 : 0;          // cached positions of the chunk
+    const bool owns_new = u.c == S - 1;
+    const int cap = a.score_cap;
+    float* sc = as.sc;
+    // ---- pass 1: scores of every position (K items), the new position last
+    {
+        float q[G][16];
+        const int i = lane & 7;
 #pragma unroll
-    for (int h = 0; h < G; ++h) {
-        if (lane == 0) {
-            as.mw[warp][h] = w.m[h];
-            as.lw[warp][h] = w.l[h];
+        for (int h = 0; h < G; ++h)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                q[h][e] = as.qs[h][8 * i + e];
+                q[h][8 + e] = as.qs[h][64 + 8 * i + e];
+            }
+        for (int t = 0; t < nt; ++t) {
+            if (!cs.wait_full(lane)) break;
+            att_scores<G>(q, cs.slot(), min(TP, n - t * TP), t * TP, sc, cap, warp, lane);
+            cs.release(lane);
         }
-        *reinterpret_cast<float4*>(&as.ow[warp][h][4 * lane]) =
-            make_float4(w.acc[h][0], w.acc[h][1], w.acc[h][2], w.acc[h][3]);
+        if (owns_new && warp == 0)
+            att_scores<G>(q, reinterpret_cast<const uint8_t*>(as.kv_new[0]), 1, n, sc, cap, 0, lane);
     }
+    csync();
+    if (cs.ctl.abort) return;
+    // ---- softmax over the chunk: warp h takes head h (base 2; q carries log2(e)/sqrt(D))
+    const int npos = n + (owns_new ? 1 : 0);
+    for (int h = warp; h < G; h += NW) {
+        float* sh = sc + h * cap;
+        float m = -INFINITY;
+        for (int t = lane; t < npos; t += 32) m = fmaxf(m, sh[t]);
+        m = warp_max(m);
+        float l = 0.f;
+        for (int t = lane; t < npos; t += 32) {
+            const float p = exp2f(sh[t] - m);
+            sh[t] = p;
+            l += p;
+        }
+        l = warp_sum(l);
+        if (lane == 0) {
+            as.hm[h] = npos ? m : -INFINITY;
+            as.hl[h] = l;
+        }
+    }
+    csync();
+    // ---- pass 2: weighted V rows (V items), the new position last
+    float acc[G][4];
+#pragma unroll
+    for (int h = 0; h < G; ++h)
+#pragma unroll
+        for (int d = 0; d < 4; ++d) acc[h][d] = 0.f;
+    for (int t = 0; t < nt; ++t) {
+        if (!cs.wait_full(lane)) break;
+        att_values<G>(acc, cs.slot(), min(TP, n - t * TP), t * TP, sc, cap, warp, lane);
+        cs.release(lane);
+    }
+    if (owns_new && warp == 0)
+        att_values<G>(acc, reinterpret_cast<const uint8_t*>(as.kv_new[1]), 1, n, sc, cap, 0, lane);
+#pragma unroll
+    for (int h = 0; h < G; ++h)
+        *reinterpret_cast<float4*>(&as.ow[warp][h][4 * lane]) = make_float4(acc[h][0], acc[h][1], acc[h][2], acc[h][3]);
     csync();
     if (cs.ctl.abort) return;
     for (int t = tid; t < G * HEAD_DIM; t += NC) {
         const int h = t / HEAD_DIM, d = t % HEAD_DIM;
-        float M = -INFINITY;
+        float O = 0.f;
 #pragma unroll
-        for (int ww = 0; ww < NW; ++ww) M = fmaxf(M, as.mw[ww][h]);
-        float Lsum = 0.f, O = 0.f;
-        if (M != -INFINITY) {
-#pragma unroll
-            for (int ww = 0; ww < NW; ++ww) {
-                const float c = exp2f(as.mw[ww][h] - M);
-                Lsum = fmaf(as.lw[ww][h], c, Lsum);
-                O = fmaf(as.ow[ww][h][d], c, O);
-            }
-        }
+        for (int ww = 0; ww < NW; ++ww) O += as.ow[ww][h][d];
         unsigned long long* p = a.part + ((size_t)(u.g * G + h) * S + u.c) * (HEAD_DIM + 2);
         if (d == 0) {
-            xw_store(p, M, tag);
-            xw_store(p + 1, Lsum, tag);
+            xw_store(p, as.hm[h], tag);
+            xw_store(p + 1, as.hl[h], tag);
         }
         xw_store(p + 2 + d, O, tag);
     }
@@ -919,7 +899,7 @@ FQ_DEV void attention_phase(const StreamArgs& a, const StreamLayer& lw, int laye
 }  // namespace
 
 template <int FMT, int G>
-__global__ void __launch_bounds__(NTH) stream_step_kernel(const __grid_constant__ StreamArgs a) {
+__global__ void __launch_bounds__(NTH, 1) stream_step_kernel(const __grid_constant__ StreamArgs a) {
     extern __shared__ __align__(1024) uint8_t smem[];
     __shared__ Ctl ctl;
     __shared__ CtlX cx;
@@ -1124,6 +1104,8 @@ bool stream_plan(StreamArgs& a, const StreamLayer& l0, int fmt, int G, std::vect
     int red = 0;   // floats of per-(row, K part) partial sums: the largest share of a CTA
     for (const ProjPlan& q : plans)
         if (q.r1 > q.r0) red = std::max(red, (q.r1 - q.r0) * q.kparts);
+    // scores of one chunk: its cached positions (at most ceil(max_pos / S)) and the new one
+    a.score_cap = (a.max_pos + a.S - 1) / a.S + 2;
     size_t att = 0;
     switch (G) {
         case 1: att = sizeof(AttSmem<1>); break;
@@ -1131,6 +1113,7 @@ bool stream_plan(StreamArgs& a, const StreamLayer& l0, int fmt, int G, std::vect
         case 4: att = sizeof(AttSmem<4>); break;
         default: return false;
     }
+    att += (size_t)G * a.score_cap * sizeof(float);
     const int xs_bytes = std::max(kmax * 4, (int)att);               // float staging / attention scratch
     const int xq_bytes = 2 * kmax + 2 * (kmax / 32) * 4;              // hi, lo planes; block scales and sums
     const int fixed = align_up(xs_bytes, 16) + align_up(xq_bytes, 16) + align_up(a.H * 4, 16) +
