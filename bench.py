@@ -6,7 +6,14 @@ by running the model on seeded random token ids; then greedy decode chains of 64
 batch 1, each chain starting from those 2048 cached positions (the cache is rewound
 between chains, so every timed step is the same workload).  One "step" = one decode token
 through the whole hot path (embedding, 28 x [norm+QKV, QK-norm+rope+append+attention,
-O-proj, norm+gate_up+SwiGLU, down], output norm, LM head, argmax).
+O-proj, norm+gate_up+SwiGLU, down], output norm, LM head, argmax).  At batch 1 the step is
+one streamed persistent kernel, so the roofline kernel is the step itself.
+
+The same line carries the other halves of the metric, measured the same way:
+  q4k_batch1  the 36-layer Qwen3-8B shape with Q4_K weights, batch 1 at context 8192;
+  batch32     the 8B shape with Q8_0 weights, 32 lockstep sequences at contexts U[512, 4096];
+  layer_step  one 0.6B-shaped layer (f32 KV, 128 positions), hot and cold (16 rotated
+              weight + cache copies, more than L2 holds).
 
 Timing: W warm-up steps, then exactly K steps bracketed by a barrier and synchronisation,
 CUDA events on the launching stream, max over ranks.  Every step streams ~0.87 GB
@@ -36,26 +43,27 @@ WORKLOAD = "qwen3-0.6b"
 CHAIN = 64
 CONTEXT = 2048
 
-# DRAM bytes (read + write) of one LM-head GEMV launch, from the ncu capture summarised in
-# profiles/gemv_tma_q8_0_lm_head_qwen3-0.6b.md (its metrics-only recapture).  Reported only while the kernel's sources
-# hash to the value they had when the counters were taken.
-LM_HEAD_TRAFFIC = {"qwen3-0.6b": (168251392, "ae06facd60aae183")}
-GEMV_SOURCES = ["gemv_tma.cu", "quant.cuh", "tma.cuh", "common.cuh"]
+# DRAM bytes (read + write) of one streamed-step launch per workload, from a metrics-only ncu
+# capture of that kernel (the profiles/ summary of the streamed step gives the command).
+# Reported only while the kernel's sources hash to the value they had when the counters were
+# taken: a changed kernel has unmeasured traffic.
+STEP_TRAFFIC = {}
+STEP_SOURCES = ["stream_step.cu", "kernels.h", "quant.cuh", "tma.cuh", "common.cuh"]
 
 
-def gemv_source_hash() -> str:
+def step_source_hash() -> str:
     import hashlib
     h = hashlib.sha256()
     base = os.path.join(os.path.dirname(os.path.abspath(__file__)), "quantized_decoder_decode_gb300", "csrc")
-    for f in GEMV_SOURCES:
+    for f in STEP_SOURCES:
         with open(os.path.join(base, f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-def lm_head_traffic(workload: str):
-    t = LM_HEAD_TRAFFIC.get(workload)
-    return t[0] if t and t[1] == gemv_source_hash() else None
+def step_traffic(workload: str):
+    t = STEP_TRAFFIC.get(workload)
+    return t[0] if t and t[1] == step_source_hash() else None
 
 
 def measured_peaks():
@@ -319,16 +327,12 @@ def weight_bytes(w, experts_per_layer=None) -> dict:
     return {"layers": L * (attn + norms) + ffn, "lm_head": head, "embedding_rows": w.batch * H * bpw}
 
 
-def run_fq(args):
+def load_workload(w, max_ctx_extra: int, dev, stream):
+    """The workload's model on the device and one KV cache per sequence holding its context
+    (filled by the model for the default workload, else the seeded N(0, 1) prior)."""
     import torch
     import synth.workloads as wl
     from quantized_decoder_decode_gb300 import fq
-
-    rank, world, local = dist_setup(args.gpus)
-    dev = torch.device("cuda", torch.cuda.current_device())
-    st = torch.cuda.current_stream(dev)
-    stream = st.cuda_stream
-    w = workload_of(args)
     d = w.dims
     n = w.batch
     chain = w.steps
@@ -340,7 +344,7 @@ def run_fq(args):
                            num_key_value_heads=d.num_key_value_heads, head_dim=d.head_dim,
                            rms_norm_eps=d.rms_norm_eps, rope_theta=d.rope_theta, num_experts=d.num_experts,
                            num_experts_used=d.num_experts_used, moe_intermediate_size=d.moe_intermediate_size,
-                           max_positions=cap_max + 64)
+                           max_positions=cap_max + max_ctx_extra)
     src, keep = fq.weight_src(desc, W, w.weight_dtype)
     model = fq.fq_load_weights(desc, src, stream)
     del src, keep
@@ -364,6 +368,35 @@ def run_fq(args):
             fq.fq_kv_commit(kv, c)
         torch.cuda.synchronize()
         first = [int(t) for t in wl.first_ids(w)]
+    return W, model, kvs, ctxs, first, toks, logits
+
+
+def free_workload(model, kvs):
+    from quantized_decoder_decode_gb300 import fq
+    for kv in kvs:
+        fq.fq_kv_free(kv)
+    fq.fq_model_free(model)
+
+
+def step_bytes_of(w, ctxs, experts=None) -> dict:
+    """Algorithmic bytes of one step (weights touched + KV read + KV written) averaged over a
+    chain of w.steps steps from the contexts ctxs."""
+    d = w.dims
+    wb = weight_bytes(w, experts)
+    eb = KV_ELEM_BYTES[w.kv_dtype]
+    kv_read = sum(2 * d.num_layers * d.kv_dim * (c + (w.steps - 1) / 2) * eb for c in ctxs)
+    kv_write = w.batch * 2 * d.num_layers * d.kv_dim * eb
+    total = wb["layers"] + wb["lm_head"] + wb["embedding_rows"] + kv_read + kv_write
+    return {"total": total, "weights_layers": wb["layers"], "lm_head": wb["lm_head"],
+            "embedding_rows": wb["embedding_rows"], "kv_read": kv_read, "kv_write": kv_write}
+
+
+def time_chains(model, kvs, ctxs, first, toks, logits, chain, steps, warmup, world, local, stream, st):
+    """Greedy chains of `chain` steps from the cached contexts (rewound between chains):
+    `warmup` untimed steps, then exactly `steps` steps between CUDA events on the launching
+    stream, bracketed by a barrier and synchronisation; clocks sampled meanwhile."""
+    import torch
+    from quantized_decoder_decode_gb300 import fq
 
     def rewind():
         for kv, c in zip(kvs, ctxs):
@@ -378,24 +411,125 @@ def run_fq(args):
             done += s_
         rewind()
 
-    chains(max(args.warmup, 3))
+    chains(max(warmup, 3))
     torch.cuda.synchronize()
     barrier(world)
-
-    # ---- timed region: exactly K steps (each step = one token for each of the n sequences)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clk:
         torch.cuda.synchronize()
         barrier(world)
-        torch.cuda.nvtx.range_push("timed")
         ev0.record(st)
-        chains(args.steps)
+        chains(steps)
         ev1.record(st)
-        torch.cuda.nvtx.range_pop()
         torch.cuda.synchronize()
         barrier(world)
-    value, dt = aggregate(n * args.steps, ev0.elapsed_time(ev1) / 1e3, world)
-    kernels_per_step = fq.fq_step_kernels(model, stream)
+    return ev0.elapsed_time(ev1) / 1e3, clk.summary(), fq.fq_step_kernels(model, stream), rewind
+
+
+def sub_record(name: str, steps: int, warmup: int, dev, stream, st, peak, peak_kind) -> dict:
+    """One more workload measured the same way as the main line (batch-1 8B Q4_K, or the
+    batch-32 8B lockstep), for the same JSON line."""
+    import synth.workloads as wl
+    w = wl.WORKLOADS[name]
+    W, model, kvs, ctxs, first, toks, logits = load_workload(w, 64, dev, stream)
+    del W
+    dt, clocks, kps, _ = time_chains(model, kvs, ctxs, first, toks, logits, w.steps, steps, warmup, 1, 0, stream, st)
+    free_workload(model, kvs)
+    sb = step_bytes_of(w, ctxs)
+    gbs = sb["total"] / (dt / steps) / 1e9
+    return {"workload": config_dict(w)["workload"], "batch": w.batch, "value": w.batch * steps / dt,
+            "unit": "tokens/s", "steps": steps, "ms_per_step": dt / steps * 1e3, "kernels_per_step": kps,
+            "step_roofline": {"bytes_per_step": sb["total"], "achieved_gbs": gbs, "peak": peak,
+                              "frac": gbs / peak, "peak_kind": peak_kind},
+            "clocks": clocks}
+
+
+def layer_step_record(dev, stream, st, peak, peak_kind, copies: int = 16, reps: int = 6) -> dict:
+    """The single 0.6B-shaped layer (one token, f32 KV with 128 prior positions): its 17.8 MB
+    working set fits in L2, so it is timed hot (the same weights and cache every call) and
+    cold (rotating over `copies` independent weight + cache copies, more than L2 holds)."""
+    import torch
+    import synth.workloads as wl
+    from quantized_decoder_decode_gb300 import fq
+    w = wl.WORKLOADS["qwen3-0.6b-layer"]
+    d = w.dims
+    side = torch.cuda.Stream(dev)
+    ss = side.cuda_stream
+    models, kvs, xs = [], [], []
+    for i in range(copies):
+        wi = wl.dataclasses.replace(w, seed=w.seed + 1000 * i)
+        W = wl.make_weights(wi)
+        desc = fq.fq_desc_init(vocab_size=d.vocab_size, hidden_size=d.hidden_size,
+                               intermediate_size=d.intermediate_size, num_layers=1,
+                               num_attention_heads=d.num_attention_heads, num_key_value_heads=d.num_key_value_heads,
+                               head_dim=d.head_dim, max_positions=w.context + 8)
+        src, keep = fq.weight_src(desc, W, w.weight_dtype)
+        m = fq.fq_load_weights(desc, src, stream)
+        kv = fq.fq_kv_init(m, w.context + 8, w.kv_dtype)
+        k, v = wl.make_kv_prior(wi, 0, 0, w.context)
+        kt, vt = kv_tensor(k, dev), kv_tensor(v, dev)
+        fq.fq_kv_append(kv, 0, 0, w.context, kt.data_ptr(), vt.data_ptr(), stream)
+        fq.fq_kv_commit(kv, w.context)
+        models.append(m)
+        kvs.append(kv)
+        xs.append(torch.from_numpy(wl.layer_input(wi)).to(dev))
+    torch.cuda.synchronize()
+
+    def calls(order):
+        for i in order:
+            fq.fq_layer_step(models[i], 0, kvs[i], w.context, xs[i].data_ptr(), ss)
+            fq.fq_kv_rewind(kvs[i], w.context)
+
+    results = {}
+    for kind, order in (("hot", [0] * copies), ("cold", list(range(copies)))):
+        with torch.cuda.stream(side):
+            calls(order)                       # per-stream workspaces exist before timing
+        torch.cuda.synchronize()
+        # every timed call is queued behind a short sleep kernel before the GPU reaches it,
+        # so the events see the GPU time of the calls, not the host's launch rate
+        n_calls = reps * copies
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(side):
+            torch.cuda._sleep(50_000_000)
+            e0.record(side)
+            for _ in range(reps):
+                calls(order)
+            e1.record(side)
+        torch.cuda.synchronize()
+        results[kind] = {"us_per_layer_step": e0.elapsed_time(e1) * 1e3 / n_calls}
+    wb = weight_bytes(w)
+    nbytes = wb["layers"] + 2 * d.kv_dim * w.context * 4 + 2 * d.kv_dim * 4
+    for kind in results:
+        if "us_per_layer_step" in results[kind]:
+            gbs = nbytes / (results[kind]["us_per_layer_step"] * 1e-6) / 1e9
+            results[kind].update({"achieved_gbs": gbs, "frac": gbs / peak})
+    for kv, m in zip(kvs, models):
+        fq.fq_kv_free(kv)
+        fq.fq_model_free(m)
+    return {"workload": config_dict(w)["workload"].split(";")[0] + "; one token, f32 KV with 128 prior positions",
+            "bytes_per_layer_step": nbytes, "copies_cold": copies, "peak": peak, "peak_kind": peak_kind, **results}
+
+
+def run_fq(args):
+    import torch
+    import synth.workloads as wl
+    from quantized_decoder_decode_gb300 import fq
+
+    rank, world, local = dist_setup(args.gpus)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    st = torch.cuda.current_stream(dev)
+    stream = st.cuda_stream
+    w = workload_of(args)
+    d = w.dims
+    n = w.batch
+    chain = w.steps
+    W, model, kvs, ctxs, first, toks, logits = load_workload(w, 64, dev, stream)
+
+    # ---- timed region: exactly K steps (each step = one token for each of the n sequences)
+    dt_dev, clocks, kernels_per_step, rewind = time_chains(model, kvs, ctxs, first, toks, logits, chain, args.steps,
+                                                           args.warmup, world, local, stream, st)
+    value, dt = aggregate(n * args.steps, dt_dev, world)
+    streamed = fq.fq_step_path(model, n, w.kv_dtype)
 
     # ---- end to end through the public API with host buffers: per step the tokens go in
     # from pinned host memory (by value through the call) and the chosen tokens come back
@@ -429,40 +563,34 @@ def run_fq(args):
         rewind()
         experts = [len(set(ri[L].flatten().tolist())) for L in range(d.num_layers)]
 
-    # ---- roofline of the dominant kernel: the dequant GEMV, timed live on the LM head (the
-    # largest single launch of the step) with CUDA events on its stream
     peak, peak_kind = measured_peaks()
-    x = torch.randn(d.hidden_size, device=dev)
-    y = torch.empty(d.vocab_size, device=dev)
-    reps = 20
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
-    for _ in range(3):
-        fq.fq_gemv(model, 0, fq.W_OUTPUT, 1, x.data_ptr(), y.data_ptr(), stream)
-    torch.cuda.synchronize()
-    for a_, b_ in evs:
-        a_.record(st)
-        fq.fq_gemv(model, 0, fq.W_OUTPUT, 1, x.data_ptr(), y.data_ptr(), stream)
-        b_.record(st)
-    torch.cuda.synchronize()
-    kt = sum(a_.elapsed_time(b_) for a_, b_ in evs) / reps / 1e3
-    bpw = 34 / 32 if w.weight_dtype == "q8_0" else 144 / 256
-    kbytes = d.vocab_size * d.hidden_size * bpw + d.hidden_size * 4 + d.vocab_size * 4
-    achieved = kbytes / kt / 1e9
-
-    wb = weight_bytes(w, experts)
-    eb = KV_ELEM_BYTES[w.kv_dtype]
-    kv_read = sum(2 * d.num_layers * d.kv_dim * (c + (chain - 1) / 2) * eb for c in ctxs)
-    kv_write = n * 2 * d.num_layers * d.kv_dim * eb
-    total = wb["layers"] + wb["lm_head"] + wb["embedding_rows"] + kv_read + kv_write
-    step_gbs = total / (dt / args.steps) / 1e9
-    # kernels inside the timed region: each step replays one captured graph; each chain adds
-    # the one state-setup launch made before its replays
+    sb = step_bytes_of(w, ctxs, experts)
+    step_gbs = sb["total"] / (dt / args.steps) / 1e9
+    # kernels inside the timed region: one launch per step (streamed) or one graph per step,
+    # plus the state set-up launch of every chain
     n_chains = (args.steps + chain - 1) // chain
+    if streamed:
+        # the dominant kernel is the whole step: one launch per token, timed above
+        kt = dt_dev / args.steps
+        roof = {"bound": "hbm", "kernel": "streamed decode step (one persistent kernel per token)",
+                "achieved": sb["total"] / kt / 1e9, "peak": peak, "unit": "GB/s",
+                "frac": sb["total"] / kt / 1e9 / peak, "peak_kind": peak_kind, "bytes_per_launch": sb["total"],
+                "us_per_launch": kt * 1e6, "traffic": step_traffic(w.name)}
+    else:
+        roof = None
+    free_workload(model, kvs)
+    del W
+
+    subs = {}
+    if rank == 0 and world == 1 and not args.no_subrecords and args.workload == WORKLOAD:
+        subs["q4k_batch1"] = sub_record("qwen3-8b-q4k", 64, 8, dev, stream, st, peak, peak_kind)
+        subs["batch32"] = sub_record("qwen3-8b-batch32", 32, 8, dev, stream, st, peak, peak_kind)
+        subs["layer_step"] = layer_step_record(dev, stream, st, peak, peak_kind)
 
     if rank == 0:
         cb = None
         if world == 1 and not args.no_cpu_baseline and w.prefill_from_model:
-            cb = cpu_baseline(w, W, budget_s=args.cpu_budget)
+            cb = cpu_baseline(w, wl.make_weights(w), budget_s=args.cpu_budget)
         line = {
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": max(args.warmup, 3), "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
@@ -472,24 +600,17 @@ def run_fq(args):
                     "d2h_bytes_per_step": 4 * n, "steps": e2e_steps},
             "gpu_launches": args.steps * kernels_per_step + n_chains,
             "kernels_per_step": kernels_per_step,
-            "roofline": {"bound": "hbm", "kernel": f"dequant GEMV ({w.weight_dtype}), LM head launch "
-                                                   f"{d.vocab_size}x{d.hidden_size}",
-                         "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                         "peak_kind": peak_kind, "bytes_per_launch": kbytes, "us_per_launch": kt * 1e6,
-                         "traffic": lm_head_traffic(w.name)},
-            "step_roofline": {"bytes_per_step": total, "achieved_gbs": step_gbs, "peak": peak,
+            "step_path": "streamed" if streamed else "kernel sequence",
+            "roofline": roof,
+            "step_roofline": {"bytes_per_step": sb["total"], "achieved_gbs": step_gbs, "peak": peak,
                               "frac": step_gbs / peak, "peak_kind": peak_kind,
-                              "breakdown": {"weights_layers": wb["layers"], "lm_head": wb["lm_head"],
-                                            "embedding_rows": wb["embedding_rows"], "kv_read": kv_read,
-                                            "kv_write": kv_write},
+                              "breakdown": {k: v for k, v in sb.items() if k != "total"},
                               "experts_per_layer": (sum(experts) / len(experts)) if experts else None},
-            "clocks": clk.summary(),
+            "clocks": clocks,
             "cpu_baseline": cb,
+            **subs,
         }
         print(json.dumps(line))
-    for kv in kvs:
-        fq.fq_kv_free(kv)
-    fq.fq_model_free(model)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
@@ -710,6 +831,8 @@ def main():
     ap.add_argument("--impl", default="fq", choices=["fq", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-subrecords", action="store_true",
+                    help="skip the 8B batch-1 / batch-32 and single-layer records of the default line")
     ap.add_argument("--kv", default=None, choices=["bf16", "q8_0"],
                     help="cache dtype in place of the workload's own (q8_0: the integer-score cache)")
     ap.add_argument("--verify", action="store_true",

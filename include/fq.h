@@ -212,10 +212,11 @@ fq_status fq_decode_greedy(const fq_model* m, fq_kv* const* caches, uint32_t n, 
 /* Same as fq_decode_step_batch, also writing the residual stream after every layer to
  * layer_out (device f32 [layers][n][hidden]) and, for MoE models, the router choice to
  * route_idx (device int32 [layers][n][num_experts_used]) and route_w (device f32, same
- * shape); any of the three may be NULL. */
+ * shape) and the router logits before the softmax to route_logits (device f32
+ * [layers][n][num_experts]); any of the four may be NULL. */
 fq_status fq_decode_step_trace(const fq_model* m, fq_kv* const* caches, uint32_t n, const int32_t* tokens,
                                float* logits, float* layer_out, int32_t* route_idx, float* route_w,
-                               void* stream);
+                               float* route_logits, void* stream);
 
 /* fq_layer_step that also copies the layer's intermediates out (device f32, any may be
  * NULL): qkv [(Hq + 2 Hkv) * head_dim] raw projections before QK-norm/rope (rows q | k | v),

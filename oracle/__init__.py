@@ -76,6 +76,7 @@ def lib():
                 "or_cache_read": ([vp, i32, i32, i32, vp, vp], i32),
                 "or_layer_step": ([vp, i32, vp, i32, vp, vp, vp], i32),
                 "or_qkv_project": ([vp, i32, vp, i32, vp, vp, vp], i32),
+                "or_layer_step_route": ([vp, i32, vp, i32, vp, vp, vp, vp], i32),
                 "or_decode_step": ([vp, vp, i32, i32, vp, vp, vp, vp], i32),
                 "or_decode_step_batch": ([vp, vp, i32, vp, vp], i32),
                 "or_forward_last_logits": ([vp, vp, i32, vp], i32),
@@ -290,15 +291,17 @@ class Model:
     def new_cache(self, capacity: int) -> "Cache":
         return Cache(self, capacity)
 
-    def layer_step(self, layer: int, cache: "Cache", pos: int, x: np.ndarray):
+    def layer_step(self, layer: int, cache: "Cache", pos: int, x: np.ndarray, router_logits: bool = False):
+        """(x after the layer, expert ids, expert weights[, router logits when asked])."""
         x = np.array(x, dtype=np.float64, copy=True)
         n_used = max(self.dims.num_experts_used, 1)
         idx = np.zeros(n_used, dtype=np.int32)
         w = np.zeros(n_used, dtype=np.float64)
-        rc = lib().or_layer_step(self._h, layer, cache._h, pos, _p(x), _p(idx), _p(w))
+        rl = np.zeros(max(self.dims.num_experts, 1), dtype=np.float64) if router_logits else None
+        rc = lib().or_layer_step_route(self._h, layer, cache._h, pos, _p(x), _p(idx), _p(w), _p(rl))
         if rc:
             raise OracleError(rc, "or_layer_step")
-        return x, idx, w
+        return (x, idx, w, rl) if router_logits else (x, idx, w)
 
     def qkv_project(self, layer: int, xn: np.ndarray, pos: int):
         """q, k, v of one token from the normalised input xn (q, k after QK-norm and RoPE)."""

@@ -444,7 +444,7 @@ void qkv_project(const or_model* m, const or_layer_w& w, const double* xn, int p
 
 // FFN block on one token (dense SwiGLU or routed mixture), returns the residual update
 void ffn(const or_model* m, const or_layer_w& w, const double* x, double* dx, int* route_idx,
-         double* route_w, bool serial) {
+         double* route_w, bool serial, double* route_logits = nullptr) {
     const or_dims& d = m->d;
     auto gv = serial ? gemv_serial : gemv_parallel;
     std::vector<double> xn(d.hidden);
@@ -459,6 +459,7 @@ void ffn(const or_model* m, const or_layer_w& w, const double* x, double* dx, in
     }
     std::vector<double> r(d.n_exp);
     gv(OR_F32, w.router, d.n_exp, d.hidden, xn.data(), r.data());
+    if (route_logits) std::copy(r.begin(), r.end(), route_logits);
     std::vector<int> idx(d.n_used);
     std::vector<double> wt(d.n_used);
     or_router(r.data(), d.n_exp, d.n_used, d.norm_topk, idx.data(), wt.data());
@@ -601,6 +602,11 @@ int or_qkv_project(const or_model* m, int layer, const double* xn, int pos, doub
 
 int or_layer_step(const or_model* m, int layer, or_cache* c, int pos, double* x, int* route_idx,
                   double* route_w) {
+    return or_layer_step_route(m, layer, c, pos, x, route_idx, route_w, nullptr);
+}
+
+int or_layer_step_route(const or_model* m, int layer, or_cache* c, int pos, double* x, int* route_idx,
+                        double* route_w, double* route_logits) {
     const or_dims& d = m->d;
     if (layer < 0 || layer >= d.layers || !x) return OR_INVALID_ARGUMENT;
     if (c->m != m) return OR_MISMATCHED_KV_CACHES;
@@ -627,7 +633,7 @@ int or_layer_step(const or_model* m, int layer, or_cache* c, int pos, double* x,
     for (int i = 0; i < d.hidden; ++i) x[i] += dx[i];
 
     // FFN block
-    ffn(m, w, x, dx.data(), route_idx, route_w, false);
+    ffn(m, w, x, dx.data(), route_idx, route_w, false, route_logits);
     for (int i = 0; i < d.hidden; ++i) x[i] += dx[i];
     return OR_OK;
 }

@@ -107,6 +107,11 @@ enum { OR_OK = 0, OR_INVALID_CONFIG = 1, OR_INVALID_SEQUENCE_LENGTH = 2, OR_KV_C
 int or_layer_step(const or_model* m, int layer, or_cache* c, int pos, double* x, int* route_idx,
                   double* route_w);
 
+/* or_layer_step that also writes the MoE router logits (n_exp values, before the softmax) to
+ * route_logits (may be NULL). */
+int or_layer_step_route(const or_model* m, int layer, or_cache* c, int pos, double* x, int* route_idx,
+                        double* route_w, double* route_logits);
+
 /* The attention block's projections for one token of layer `layer` at position pos, from the
  * already normalised input xn (length hidden): q [n_q][head_dim], k and v [n_kv][head_dim],
  * q and k after the per-head RMSNorm with q_norm / k_norm and then RoPE, v as projected. */

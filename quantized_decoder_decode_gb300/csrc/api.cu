@@ -269,6 +269,7 @@ struct Body {
     float* layer_out = nullptr;
     int32_t* route_idx = nullptr;
     float* route_w = nullptr;
+    float* route_logits = nullptr;
     // rows are consecutive positions of one sequence (the all-logits step): every row's new
     // k/v is appended before any row attends
     bool block = false;
@@ -280,8 +281,8 @@ struct Body {
 // (stream_step.cu) unless the caller asked for the kernel sequence.
 bool stream_eligible(const Body& b, int kv_type) {
     const fq_model* m = b.m;
-    return m->slayers && m->opt_path != FQ_PATH_KERNELS && b.n == 1 && !b.route_idx && !b.block && b.head_row < 0 &&
-           kv_type == KV_BF16;
+    return m->slayers && m->opt_path != FQ_PATH_KERNELS && b.n == 1 && !b.route_idx && !b.route_logits && !b.block &&
+           b.head_row < 0 && kv_type == KV_BF16;
 }
 
 // The kernels of one decode step, in order.  The first launch follows the set-up kernel
@@ -407,6 +408,11 @@ fq_status enqueue_step(const Body& b, cudaStream_t s, int kv_type, float* x_over
                                    cudaMemcpyDeviceToDevice, s));
                 first = true;
             }
+            if (b.route_logits) {
+                CK(cudaMemcpyAsync(b.route_logits + (size_t)L * n * E, w->rlogits, sizeof(float) * n * E,
+                                   cudaMemcpyDeviceToDevice, s));
+                first = true;
+            }
         }
         if (b.layer_out) {
             CK(cudaMemcpyAsync(b.layer_out + (size_t)L * n * H, x, sizeof(float) * n * H, cudaMemcpyDeviceToDevice, s));
@@ -455,7 +461,7 @@ fq_status run_body(const Body& b, cudaStream_t s, int kv_type, int reps) {
     Workspace* w = b.w;
     const int mode = b.greedy ? MODE_GREEDY : MODE_DECODE;
     // one streamed kernel per step needs no graph
-    if (!b.m->opt_graphs || b.layer_out || b.route_idx || stream_eligible(b, kv_type)) {
+    if (!b.m->opt_graphs || b.layer_out || b.route_idx || b.route_logits || stream_eligible(b, kv_type)) {
         for (int r = 0; r < reps; ++r) TRY(enqueue_step(b, s, kv_type, nullptr, -1));
         w->last_kernels = stream_eligible(b, kv_type) ? 1u : 0u;
         return FQ_OK;
@@ -1095,17 +1101,19 @@ fq_status fq_decode_greedy(const fq_model* m, fq_kv* const* caches, uint32_t n, 
 }
 
 fq_status fq_decode_step_trace(const fq_model* m, fq_kv* const* caches, uint32_t n, const int32_t* tokens,
-                               float* logits, float* layer_out, int32_t* route_idx, float* route_w, void* stream) {
+                               float* logits, float* layer_out, int32_t* route_idx, float* route_w,
+                               float* route_logits, void* stream) {
     TRY(check_caches(m, caches, n, 1));
     TRY(check_tokens(m, tokens, n));
-    if ((route_idx || route_w) && !m->moe()) return fail(FQ_ERR_INVALID_ARGUMENT, "route trace on a dense model");
+    if ((route_idx || route_w || route_logits) && !m->moe())
+        return fail(FQ_ERR_INVALID_ARGUMENT, "route trace on a dense model");
     if ((route_idx == nullptr) != (route_w == nullptr)) return fail(FQ_ERR_INVALID_ARGUMENT, "route_idx and route_w go together");
     cudaStream_t s = (cudaStream_t)stream;
     uint32_t cap = max_cap(caches, n);
     Workspace* w;
     TRY(ensure_ws(m, s, (int)n, cap, &w));
     TRY(setup_state(w, caches, tokens, (int)n, false, nullptr, logits, s));
-    Body b{m, w, (int)n, 0, 0, logits, false, layer_out, route_idx, route_w};
+    Body b{m, w, (int)n, 0, 0, logits, false, layer_out, route_idx, route_w, route_logits};
     attn_split((int)n, m->d.p.num_key_value_heads, cap, b.chunk, b.splits);
     TRY(enqueue_step(b, s, caches[0]->type, nullptr, -1));
     for (uint32_t i = 0; i < n; ++i) caches[i]->len += 1;

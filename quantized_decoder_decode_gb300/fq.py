@@ -86,7 +86,7 @@ def lib():
                 "fq_decode_step_all_logits": [vp, vp, vp, u32, u32, vp, vp],
                 "fq_forward_step": [vp, vp, vp, u32, u32, vp, vp],
                 "fq_decode_greedy": [vp, vp, u32, vp, u32, vp, vp, vp],
-                "fq_decode_step_trace": [vp, vp, u32, vp, vp, vp, vp, vp, vp],
+                "fq_decode_step_trace": [vp, vp, u32, vp, vp, vp, vp, vp, vp, vp],
                 "fq_dequant_rows": [vp, u32, ctypes.c_int, u64, u64, vp, vp],
                 "fq_quantize_q8_0": [vp, u64, vp, vp],
                 "fq_layer_step_trace": [vp, u32, vp, u32, vp, vp, vp, vp, vp],
@@ -273,10 +273,11 @@ def fq_decode_greedy(model: int, kvs, first_tokens, n_steps: int, tokens_out_ptr
 
 
 def fq_decode_step_trace(model: int, kvs, tokens, logits_ptr: int, layer_out_ptr: int = 0, route_idx_ptr: int = 0,
-                         route_w_ptr: int = 0, stream: int = 0) -> None:
+                         route_w_ptr: int = 0, stream: int = 0, route_logits_ptr: int = 0) -> None:
     toks, tp = _i32(tokens)
     _check(lib().fq_decode_step_trace(model, _caches(kvs), len(kvs), tp, logits_ptr or None, layer_out_ptr or None,
-                                      route_idx_ptr or None, route_w_ptr or None, stream), "fq_decode_step_trace")
+                                      route_idx_ptr or None, route_w_ptr or None, route_logits_ptr or None, stream),
+           "fq_decode_step_trace")
 
 
 def fq_dequant_rows(model: int, layer: int, which: int, row0: int, n_rows: int, out_ptr: int, stream: int = 0) -> None:

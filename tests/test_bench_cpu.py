@@ -50,3 +50,17 @@ def test_kv_tensor_keeps_the_bytes():
     assert t.dtype == torch.int16 and t.numpy().view(np.uint16).tolist() == [0x3F80, 0xBF80]
     blocks = np.arange(34, dtype=np.uint8)
     assert bench.kv_tensor(blocks, torch.device("cpu")).dtype == torch.uint8
+
+
+def test_step_bytes_of_a_chain_counts_the_growing_context():
+    # a chain of 64 steps from 2048 cached positions reads 2048 + 31.5 positions per step on
+    # average; the weights are the same every step
+    w = wl.WORKLOADS["qwen3-0.6b"]
+    sb = bench.step_bytes_of(w, [2048])
+    per_pos = 2 * 28 * 8 * 128 * 2
+    assert sb["kv_read"] == pytest.approx(per_pos * (2048 + 31.5))
+    assert sb["kv_write"] == per_pos
+    assert sb["total"] == pytest.approx(sb["weights_layers"] + sb["lm_head"] + sb["embedding_rows"] + sb["kv_read"]
+                                        + sb["kv_write"])
+    b32 = bench.step_bytes_of(wl.WORKLOADS["qwen3-8b-batch32"], [512, 4096])
+    assert b32["kv_write"] == 32 * 2 * 36 * 8 * 128 * 2

@@ -11,7 +11,7 @@ import oracle
 import synth
 import synth.workloads as wl
 from quantized_decoder_decode_gb300 import fq
-from tests.gpu_util import DEV, Pair, assert_layer_close, assert_logits_close, max_err, stream
+from tests.gpu_util import DEV, Pair, assert_layer_close, assert_logits_close, check_routing, max_err, stream, topk_ids
 
 pytestmark = pytest.mark.gpu
 
@@ -95,30 +95,57 @@ def test_layer_step_qwen3_0p6b_layer(pair_factory):
 # ---------------------------------------------------------------- decode steps
 
 def _compare_step(p, kvs, ocs, tokens, what):
+    """One traced step against the oracle's step from the same caches: every layer's residual
+    stream under the per-layer tolerance, the logits under 2e-2.  MoE: the expert ids are the
+    exact top-k of the GPU's own router logits and equal the oracle's unless the oracle's
+    k-th / (k+1)-th router-logit gap is within the measured router error (a near-tie: the
+    trajectories then part, and the rest of that sequence's step is not compared)."""
     d = p.dims
     n = len(kvs)
     logits = torch.empty((n, d.vocab_size), dtype=torch.float32, device=DEV)
     lo = torch.empty((d.num_layers, n, d.hidden_size), dtype=torch.float32, device=DEV)
-    ri = rw = None
+    ri = rw = rl = None
     if d.is_moe:
         ri = torch.empty((d.num_layers, n, d.num_experts_used), dtype=torch.int32, device=DEV)
         rw = torch.empty((d.num_layers, n, d.num_experts_used), dtype=torch.float32, device=DEV)
+        rl = torch.empty((d.num_layers, n, d.num_experts), dtype=torch.float32, device=DEV)
     fq.fq_decode_step_trace(p.model, kvs, tokens, logits.data_ptr(), lo.data_ptr(),
-                            ri.data_ptr() if ri is not None else 0, rw.data_ptr() if rw is not None else 0, stream())
+                            ri.data_ptr() if ri is not None else 0, rw.data_ptr() if rw is not None else 0, stream(),
+                            route_logits_ptr=rl.data_ptr() if rl is not None else 0)
     torch.cuda.synchronize()
     got_lg, got_lo = logits.cpu().numpy(), lo.cpu().numpy()
     refs = []
     for s in range(n):
-        lg, lo_ref, rix, rwx = p.om.decode_step(ocs[s], int(tokens[s]), ocs[s].len, trace=True)
+        pos = ocs[s].len
+        lg, lo_ref, rix, rwx = p.om.decode_step(ocs[s], int(tokens[s]), pos, trace=True)
         refs.append(lg)
+        parted = False
         for L in range(d.num_layers):
+            if d.is_moe:
+                gi = ri[L, s].cpu().tolist()
+                if sorted(gi) != sorted(rix[L].tolist()):
+                    # the oracle's router logits on the GPU's own input to this layer decide
+                    # whether this is a near-tie
+                    oc2 = p.om.new_cache(ocs[s].capacity)
+                    for LL in range(d.num_layers):
+                        k, v = ocs[s].read(LL, 0, pos)
+                        oc2.write(LL, 0, k, v)
+                    oc2.set_len(pos)
+                    x_in = got_lo[L - 1, s] if L else oracle.dequant(p.w.weight_dtype, p.W["tok_embd"][int(tokens[s])],
+                                                                     d.hidden_size)
+                    _, idx, _, rlog = p.om.layer_step(L, oc2, pos, np.asarray(x_in, np.float64), router_logits=True)
+                    assert check_routing(gi, rl[L, s].cpu().numpy(), idx, rlog, d.num_experts_used,
+                                         f"{what} seq {s} layer {L}") or sorted(gi) == sorted(idx.tolist()), \
+                        f"{what} seq {s} layer {L}: routing"
+                    parted = True
+                    break
+                assert sorted(gi) == topk_ids(rl[L, s].cpu().numpy(), d.num_experts_used), (what, s, L)
             assert_layer_close(got_lo[L, s], lo_ref[L], f"{what} seq {s} layer {L}")
             if d.is_moe:
-                # expert indices exact; routing weights under the per-layer tolerance
-                assert sorted(ri[L, s].cpu().tolist()) == sorted(rix[L].tolist()), (what, s, L)
                 gw = dict(zip(ri[L, s].cpu().tolist(), rw[L, s].cpu().tolist()))
                 assert_layer_close([gw[e] for e in rix[L].tolist()], rwx[L], f"{what} seq {s} layer {L} weights")
-        assert_logits_close(got_lg[s], lg, f"{what} seq {s} logits")
+        if not parted:
+            assert_logits_close(got_lg[s], lg, f"{what} seq {s} logits")
     return got_lg, np.stack(refs)
 
 
