@@ -176,10 +176,12 @@ FQ_HD inline void row_range(int N, bool pairs, int c, int G, int& r0, int& r1) {
 
 // bytes of one row in a slot: Q8_0 codes + fp16 scales, or Q4_K super-blocks
 FQ_HD int slot_row_bytes(const QMat& W) { return W.fmt == FMT_Q8_0 ? W.K + W.K / 16 : W.K / 256 * 144; }
+// rows per ring item: as many as a slot holds
 FQ_HD int rows_per_item(const QMat& W) { return SLOT / slot_row_bytes(W); }
 
 // How a phase's rows x K are cut into tasks (R rows x `up` units): the K split that gives the
-// busiest warp the least work, with whole 32-lane passes.
+// busiest warp the least work, with whole 32-lane passes; a split must save a tenth of that
+// work to be taken, since it adds a barrier and the partial-sum epilogue.
 struct Split {
     int kparts, up;
 };
@@ -449,7 +451,9 @@ template <> struct PCfg<FMT_Q4_K> { static constexpr int R = 4, UE = 64; };
 
 // R rows of an item (rows row0.. of its nr rows), units [ua, ub) of each row: lane takes units
 // ua + lane, ua + lane + 32, ...  Returns per-row partial sums before the warp reduction.
-template <int FMT>
+// FULL: all R rows exist, and their work has no branches and interleaves; otherwise rows past
+// the item's end are skipped one by one.
+template <int FMT, bool FULL>
 FQ_DEV void task_dot(const uint8_t* slot, int nr, int K, int row0, int ua, int ub, int lane, const XStage& x,
                      float (&acc)[PCfg<FMT>::R]) {
     constexpr int R = PCfg<FMT>::R;
@@ -466,19 +470,18 @@ FQ_DEV void task_dot(const uint8_t* slot, int nr, int K, int row0, int ua, int u
 #pragma unroll
             for (int r = 0; r < R; ++r) {
                 const int row = row0 + r;
-                if (row < nr) {
-                    const uint4 c = *reinterpret_cast<const uint4*>(slot + (size_t)row * K + 16 * u);
-                    const float d = h2f(sc[row * K32 + (u >> 1)]);
-                    int A = dp4a_ss(c.x, h.x, 0);
-                    A = dp4a_ss(c.y, h.y, A);
-                    A = dp4a_ss(c.z, h.z, A);
-                    A = dp4a_ss(c.w, h.w, A);
-                    int B = dp4a_su(c.x, l.x, 0);
-                    B = dp4a_su(c.y, l.y, B);
-                    B = dp4a_su(c.z, l.z, B);
-                    B = dp4a_su(c.w, l.w, B);
-                    acc[r] = fmaf(d * s, (float)(A * 256 + B), acc[r]);
-                }
+                if (!FULL && row >= nr) break;
+                const uint4 c = *reinterpret_cast<const uint4*>(slot + (size_t)row * K + 16 * u);
+                const float d = h2f(sc[row * K32 + (u >> 1)]);
+                int A = dp4a_ss(c.x, h.x, 0);
+                A = dp4a_ss(c.y, h.y, A);
+                A = dp4a_ss(c.z, h.z, A);
+                A = dp4a_ss(c.w, h.w, A);
+                int B = dp4a_su(c.x, l.x, 0);
+                B = dp4a_su(c.y, l.y, B);
+                B = dp4a_su(c.z, l.z, B);
+                B = dp4a_su(c.w, l.w, B);
+                acc[r] = fmaf(d * s, (float)(A * 256 + B), acc[r]);
             }
         }
     } else {
@@ -500,7 +503,7 @@ FQ_DEV void task_dot(const uint8_t* slot, int nr, int K, int row0, int ua, int u
 #pragma unroll
             for (int r = 0; r < R; ++r) {
                 const int row = row0 + r;
-                if (row >= nr) break;
+                if (!FULL && row >= nr) break;
                 const uint8_t* blk = slot + (size_t)row * rb + (u >> 2) * 144;
                 const uint4 hdr = *reinterpret_cast<const uint4*>(blk);
                 const uint4 q0 = *reinterpret_cast<const uint4*>(blk + 16 + 32 * c);
@@ -543,10 +546,13 @@ FQ_DEV void task_dot(const uint8_t* slot, int nr, int K, int row0, int ua, int u
 
 // Rows [r0, r1) of W times the staged input: every item of the phase is waited for and
 // released by every consumer warp in order; the phase's tasks (R rows of one item x one K
-// part) go to the warps round-robin.  Partial sums land in red[row - r0][kpart]; returns the
-// number of K parts (0 when a wait gave up).
-template <int FMT>
-FQ_DEV int proj_tasks(Cons& cs, const QMat& W, const ProjPlan& pp, const XStage& x, float* red) {
+// part) go to the warps round-robin.  `direct` (one K part, and gate/up pairs never split
+// between items): the task's warp finishes its rows at once, emit(row, y, y2) (y2: the up row
+// after a gate row when `pairs`); otherwise partial sums land in red[row - r0][kpart].
+// Returns false when a wait gave up.
+template <int FMT, class Emit>
+FQ_DEV bool proj_tasks(Cons& cs, const QMat& W, const ProjPlan& pp, const XStage& x, float* red, bool direct,
+                       bool pairs, Emit&& emit) {
     constexpr int R = PCfg<FMT>::R;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int r0 = pp.r0, r1 = pp.r1, rs = pp.rs, U = pp.U;
@@ -560,15 +566,24 @@ FQ_DEV int proj_tasks(Cons& cs, const QMat& W, const ProjPlan& pp, const XStage&
         for (int t = first; t < ntask; t += NW) {
             const int g = t / kparts * R, kp = t - t / kparts * kparts;
             float acc[R];
-            task_dot<FMT>(slot, nr, W.K, g, kp * up, min(U, (kp + 1) * up), lane, x, acc);
+            // (the branch-free form pays for Q8_0 rows; Q4_K's larger body runs slower interleaved)
+            if (FMT == FMT_Q8_0 && g + R <= nr)
+                task_dot<FMT, true>(slot, nr, W.K, g, kp * up, min(U, (kp + 1) * up), lane, x, acc);
+            else task_dot<FMT, false>(slot, nr, W.K, g, kp * up, min(U, (kp + 1) * up), lane, x, acc);
             const float s = reduce_rows<R>(acc, lane);
             const int rr = lane / (32 / R);
-            if ((lane & (32 / R - 1)) == 0 && g + rr < nr) red[(size_t)(r - r0 + g + rr) * kparts + kp] = s;
+            const bool owner = (lane & (32 / R - 1)) == 0 && g + rr < nr;
+            if (direct) {
+                const float s2 = __shfl_down_sync(0xFFFFFFFFu, s, 32 / R);   // the next row's sum
+                if (owner && !(pairs && (rr & 1))) emit(r + g + rr, s, s2);
+            } else if (owner) {
+                red[(size_t)(r - r0 + g + rr) * kparts + kp] = s;
+            }
         }
         first = (first - ntask) & (NW - 1);
         cs.release(lane);
     }
-    return kparts;
+    return true;
 }
 
 // ---------------------------------------------------------------- consumers: attention
@@ -945,9 +960,11 @@ __global__ void __launch_bounds__(NTH, 1) stream_step_kernel(const __grid_consta
     // The step as one loop over phases, so that every phase body exists once in the code:
     // q = 5 L + {0: RMSNorm + QKV, 1: attention, 2: O + residual, 3: RMSNorm + gate_up +
     // SwiGLU, 4: down + residual}; q = 5 n_layers: final RMSNorm + LM head.
+    // A flag set by one warp is read only after a barrier that every warp passes, so that all
+    // warps leave the loop at the same phase.
     const int nq = 5 * a.n_layers + (a.head ? 1 : 0);
     float inv = 1.f;
-    for (int q = 0; q < nq && !ctl.abort; ++q) {
+    for (int q = 0; q < nq; ++q) {
         const int L = q / 5, ph = q - 5 * L;
         const bool lm = L == a.n_layers;
         const StreamLayer& lw = a.layers[lm ? 0 : L];
@@ -955,6 +972,7 @@ __global__ void __launch_bounds__(NTH, 1) stream_step_kernel(const __grid_consta
         if (ph == 1) {
             attention_phase<G>(a, lw, L, ss, tag, cs, as, au);
             csync();
+            if (ctl.abort) break;
             continue;
         }
         // ---- a projection phase: its matrix, input, gain and plan
@@ -969,18 +987,9 @@ __global__ void __launch_bounds__(NTH, 1) stream_step_kernel(const __grid_consta
         if (gain) inv = inv_p;
         if (ctl.abort) break;
         const ProjPlan& P = pp[j];
-        if (!proj_tasks<FMT>(cs, W, P, xq, red)) ctl.abort = 1;
-        csync();
-        if (ctl.abort) break;
-        // ---- epilogue over this CTA's rows
-        const int kparts = P.kparts;
-        const int step = ph == 3 && !lm ? 2 : 1;   // gate/up rows come in pairs
+        const bool pairs = ph == 3 && !lm;   // gate/up rows come in pairs
         unsigned long long kb = 0ull;
-        for (int r = P.r0 + step * tid; r < P.r1; r += step * NC) {
-            float y = 0.f, y2 = 0.f;
-            for (int k = 0; k < kparts; ++k) y += red[(r - P.r0) * kparts + k];
-            if (step == 2)
-                for (int k = 0; k < kparts; ++k) y2 += red[(r + 1 - P.r0) * kparts + k];
+        auto emit = [&](int r, float y, float y2) {
             if (lm) {
                 y *= inv;
                 if (a.logits) a.logits[r] = y;
@@ -997,7 +1006,25 @@ __global__ void __launch_bounds__(NTH, 1) stream_step_kernel(const __grid_consta
                 xw_store(a.xf + r, xn, tag);
                 if (a.trace_x) a.trace_x[(size_t)L * a.H + r] = xn;
             }
+        };
+        const bool direct = P.kparts == 1 && !(pairs && (P.rs & 1));
+        if (!proj_tasks<FMT>(cs, W, P, xq, red, direct, pairs, emit)) ctl.abort = 1;
+        const int kparts = P.kparts;
+        if (!direct) {
+            // ---- the epilogue over this CTA's rows after the partial sums
+            csync();
+            if (ctl.abort) break;
+            const int step = pairs ? 2 : 1;
+            for (int r = P.r0 + step * tid; r < P.r1; r += step * NC) {
+                float y = 0.f, y2 = 0.f;
+                for (int k = 0; k < kparts; ++k) y += red[(r - P.r0) * kparts + k];
+                if (pairs)
+                    for (int k = 0; k < kparts; ++k) y2 += red[(r + 1 - P.r0) * kparts + k];
+                emit(r, y, y2);
+            }
         }
+        // direct: the rows were finished in the tasks; the next phase's first barrier
+        // orders them before its writes to shared memory, and reads the flag after it
         if (lm && a.greedy) {
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) {
@@ -1094,6 +1121,7 @@ bool stream_plan(StreamArgs& a, const StreamLayer& l0, int fmt, int G, std::vect
                 ProjPlan& q = plans[(size_t)c * NPROJ + j];
                 row_range(W.N, j == P_GU, c, g_sms_s, q.r0, q.r1);
                 q.rs = rows_per_item(W);
+                if (q.rs < 1) return false;   // a row must fit one slot
                 q.U = W.K / UE;
                 const Split sp = choose_split(q.r0, q.r1, q.rs, R, q.U);
                 q.kparts = sp.kparts;
