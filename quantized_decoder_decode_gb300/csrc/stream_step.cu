@@ -525,18 +525,17 @@ FQ_DEV void task_dot(const uint8_t* slot, int nr, int K, int row0, int ua, int u
                 }
                 const float d = h2f((unsigned short)(hdr.x & 0xFFFFu));
                 const float dmin = h2f((unsigned short)(hdr.x >> 16));
-                const uint32_t W0 = hdr.y, W1 = hdr.z, W2 = hdr.w;
-                uint32_t sc0, mn0, sc1, mn1;
-                if (c < 2) {
-                    const uint32_t sh = 16u * c;
-                    sc0 = (W0 >> sh) & 63u; sc1 = (W0 >> (sh + 8)) & 63u;
-                    mn0 = (W1 >> sh) & 63u; mn1 = (W1 >> (sh + 8)) & 63u;
-                } else {
-                    const uint32_t sh = 16u * (c - 2);
-                    const uint32_t a0 = W2 >> sh, b0 = W0 >> sh, b1 = W1 >> sh;
-                    sc0 = (a0 & 15u) | ((b0 >> 2) & 48u); sc1 = ((a0 >> 8) & 15u) | ((b0 >> 10) & 48u);
-                    mn0 = ((a0 >> 4) & 15u) | ((b1 >> 2) & 48u); mn1 = ((a0 >> 12) & 15u) | ((b1 >> 10) & 48u);
-                }
+                // 6-bit scale and min of sub-blocks 2c and 2c + 1 (the low pair, c < 2: byte j of
+                // words 0 and 1; the high pair: low / high nibble of byte j - 4 of word 2, top
+                // bits from bytes j - 4 of words 0 / 1), one form for both with selects, since c
+                // differs between neighbouring lanes
+                const uint32_t sh = 16u * (c & 1);
+                const uint32_t a0 = hdr.w >> sh, b0 = hdr.y >> sh, b1 = hdr.z >> sh;
+                const bool hp = c >= 2;
+                const uint32_t X0 = hp ? a0 : b0, Y0 = hp ? b0 >> 2 : b0;
+                const uint32_t X1 = hp ? a0 >> 4 : b1, Y1 = hp ? b1 >> 2 : b1;
+                const uint32_t sc0 = (X0 & 15u) | (Y0 & 48u), sc1 = ((X0 >> 8) & 15u) | ((Y0 >> 8) & 48u);
+                const uint32_t mn0 = (X1 & 15u) | (Y1 & 48u), mn1 = ((X1 >> 8) & 15u) | ((Y1 >> 8) & 48u);
                 acc[r] += d * (float)sc0 * s_lo * (float)(Alo * 256 + Blo) - dmin * (float)mn0 * m_lo +
                           d * (float)sc1 * s_hi * (float)(Ahi * 256 + Bhi) - dmin * (float)mn1 * m_hi;
             }
