@@ -41,7 +41,7 @@ namespace fq {
 
 namespace {
 
-constexpr int NW = 8;                 // consumer warps (a power of two)
+constexpr int NW = 11;                // consumer warps (with the producer, 3 per SM sub-partition)
 constexpr int NC = NW * 32;           // consumer threads
 constexpr int NTH = NC + 32;          // + the producer warp
 constexpr int SLOT = 16384;           // bytes per ring slot
@@ -498,7 +498,8 @@ FQ_DEV void task_dot(const uint8_t* slot, int nr, int K, int row0, int ua, int u
                 h[p] = *reinterpret_cast<const uint4*>(x.hi + p * P + 16 * u);
                 l[p] = *reinterpret_cast<const uint4*>(x.lo + p * P + 16 * u);
             }
-            const float s_lo = x.sc[e0 >> 5], s_hi = x.sc[(e0 >> 5) + 1];
+            // the high nibbles are used in place (16 x their value): 1/16 goes with their block scale
+            const float s_lo = x.sc[e0 >> 5], s_hi = x.sc[(e0 >> 5) + 1] * 0.0625f;
             const float m_lo = x.sum32[e0 >> 5], m_hi = x.sum32[(e0 >> 5) + 1];
 #pragma unroll
             for (int r = 0; r < R; ++r) {
@@ -512,7 +513,7 @@ FQ_DEV void task_dot(const uint8_t* slot, int nr, int K, int row0, int ua, int u
                 int Alo = 0, Blo = 0, Ahi = 0, Bhi = 0;
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
-                    const uint32_t qlo = w[i] & 0x0F0F0F0Fu, qhi = (w[i] >> 4) & 0x0F0F0F0Fu;
+                    const uint32_t qlo = w[i] & 0x0F0F0F0Fu, qhi = w[i] & 0xF0F0F0F0u;
                     const uint4& hl = h[i >> 2];
                     const uint4& ll = l[i >> 2];
                     const uint4& hh = h[2 + (i >> 2)];
@@ -579,7 +580,7 @@ FQ_DEV bool proj_tasks(Cons& cs, const QMat& W, const ProjPlan& pp, const XStage
                 red[(size_t)(r - r0 + g + rr) * kparts + kp] = s;
             }
         }
-        first = (first - ntask) & (NW - 1);
+        first = ((first - ntask) % NW + NW) % NW;
         cs.release(lane);
     }
     return true;
@@ -616,9 +617,9 @@ struct alignas(16) AttSmem {
     float sc[1];                      // scores / weights [G][cap], cap = the plan's score capacity
 };
 static_assert(sizeof(float) * HEAD_DIM % 16 == 0, "vector-accessed attention arrays stay 16-byte aligned");
-static_assert((NW & (NW - 1)) == 0 && NW >= 4, "task rotation uses NW - 1 as a mask; the prologue needs G + 2 warps");
+static_assert(NW >= 6, "the prologue needs G + 2 warps");
 
-// Scores of K rows row = 32 step + 4 warp + (lane >> 3) of an item of n rows (8 lanes per row,
+// Scores of K rows row = 4 NW step + 4 warp + (lane >> 3) of an item of n rows (8 lanes per row,
 // 16 dims each: 8i..8i+7 and 64+8i..64+8i+7); lane i == h of the row's group writes head h's
 // score to sc[h][base + row].
 template <int G>
@@ -626,9 +627,9 @@ FQ_DEV void att_scores(const float (&q)[G][16], const uint8_t* kb, int n, int ba
                        int lane) {
     const int j = lane >> 3, i = lane & 7;
 #pragma unroll
-    for (int step = 0; step < TP / (4 * NW); ++step) {
-        const int row = 32 * step + 4 * warp + j;
-        if (32 * step + 4 * warp >= n) break;   // the whole group of four rows is past the end
+    for (int step = 0; step < (TP + 4 * NW - 1) / (4 * NW); ++step) {
+        const int row = 4 * NW * step + 4 * warp + j;
+        if (4 * NW * step + 4 * warp >= n) break;   // the whole group of four rows is past the end
         const bool valid = row < n;
         float s[G];
 #pragma unroll
