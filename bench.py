@@ -43,11 +43,14 @@ WORKLOAD = "qwen3-0.6b"
 CHAIN = 64
 CONTEXT = 2048
 
-# DRAM bytes (read + write) of one streamed-step launch per workload, from a metrics-only ncu
-# capture of that kernel (the profiles/ summary of the streamed step gives the command).
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one streamed-step launch per
+# workload, from a metrics-only ncu capture of that kernel inside the timed NVTX range.
 # Reported only while the kernel's sources hash to the value they had when the counters were
 # taken: a changed kernel has unmeasured traffic.
-STEP_TRAFFIC = {}
+STEP_TRAFFIC = {
+    "qwen3-0.6b": (869624576, "b5e9451c775157b2"),     # mean of 2 launches: 868.79 MB read + 0.83 MB written
+    "qwen3-8b-q4k": (5500999936, "b5e9451c775157b2"),  # 5468.92 MB read + 32.08 MB written (exchange words)
+}
 STEP_SOURCES = ["stream_step.cu", "kernels.h", "quant.cuh", "tma.cuh", "common.cuh"]
 
 
@@ -419,7 +422,9 @@ def time_chains(model, kvs, ctxs, first, toks, logits, chain, steps, warmup, wor
         torch.cuda.synchronize()
         barrier(world)
         ev0.record(st)
+        torch.cuda.nvtx.range_push("timed")   # the region a profiler's NVTX filter selects
         chains(steps)
+        torch.cuda.nvtx.range_pop()
         ev1.record(st)
         torch.cuda.synchronize()
         barrier(world)
@@ -440,7 +445,8 @@ def sub_record(name: str, steps: int, warmup: int, dev, stream, st, peak, peak_k
     return {"workload": config_dict(w)["workload"], "batch": w.batch, "value": w.batch * steps / dt,
             "unit": "tokens/s", "steps": steps, "ms_per_step": dt / steps * 1e3, "kernels_per_step": kps,
             "step_roofline": {"bytes_per_step": sb["total"], "achieved_gbs": gbs, "peak": peak,
-                              "frac": gbs / peak, "peak_kind": peak_kind},
+                              "frac": gbs / peak, "peak_kind": peak_kind,
+                              "traffic": step_traffic(name) if kps == 1 else None},
             "clocks": clocks}
 
 
