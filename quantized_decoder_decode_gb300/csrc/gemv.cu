@@ -375,7 +375,7 @@ void gemv_prepare() {
 }
 
 void launch_gemv(const GemvArgs& a, cudaStream_t s, bool pdl) {
-    if (!getenv("FQ_NO_TMA") && launch_gemv_tma(a, s, pdl)) return;
+    if (launch_gemv_tma(a, s, pdl)) return;
     // expert mode: an expert's tokens are only known on the device; the four-row variant reads
     // and converts each weight once for up to four of them
     const bool one = a.B == 1 && !(a.route && a.W.fmt == FMT_Q8_0);
