@@ -617,6 +617,7 @@ struct alignas(16) AttSmem {
     float sc[1];                      // scores / weights [G][cap], cap = the plan's score capacity
 };
 static_assert(sizeof(float) * HEAD_DIM % 16 == 0, "vector-accessed attention arrays stay 16-byte aligned");
+static_assert(NC % 32 == 0, "a warp stages whole blocks of 32 values");
 static_assert(NW >= 6, "the prologue needs G + 2 warps");
 
 // Scores of K rows row = 4 NW step + 4 warp + (lane >> 3) of an item of n rows (8 lanes per row,
@@ -710,13 +711,15 @@ FQ_DEV float stage(const StreamArgs& a, const unsigned long long* src, int K, ui
             put(i, dequant_one(a.emb, tok, i), dequant_one(a.emb, tok, i + 1),
                 gain ? *reinterpret_cast<const float2*>(gain + i) : make_float2(1.f, 1.f));
     }
-    ss = warp_sum(ss);
-    if (lane == 0) cx.wsum[warp] = ss;
-    csync();
-    // blocks of 32: 8 lanes per block, 4 elements per lane
+    // Blocks of 32 values, quantised by the warp that staged them: a warp's threads take 64
+    // consecutive values per round (2 NC values apart), so warp w holds blocks 2w, 2w + 1,
+    // then 2w + NC / 16, ... and needs no CTA barrier before quantising them.  8 lanes per
+    // block, 4 values per lane; lanes 16-31 take the warp's next pair of blocks.
+    __syncwarp();
     const int nblk = K >> 5;
-    for (int base = 4 * warp; base < nblk; base += 4 * NW) {
-        const int blk = base + (lane >> 3), j = lane & 7;
+    constexpr int BSTRIDE = NC / 16;   // blocks between a warp's rounds
+    for (int base = 2 * warp; base < nblk; base += 2 * BSTRIDE) {
+        const int blk = base + (lane >> 4) * BSTRIDE + ((lane >> 3) & 1), j = lane & 7;
         const bool on = blk < nblk;
         const float4 v = on ? reinterpret_cast<const float4*>(x.xs)[blk * 8 + j] : make_float4(0.f, 0.f, 0.f, 0.f);
         float am = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
@@ -745,10 +748,12 @@ FQ_DEV float stage(const StreamArgs& a, const unsigned long long* src, int K, ui
             if (FMT == FMT_Q4_K) x.sum32[blk] = sm;
         }
     }
+    ss = warp_sum(ss);
+    if (lane == 0) cx.wsum[warp] = ss;
+    csync();   // every block quantised, every warp's sum of squares in
     float tot = 0.f;
 #pragma unroll
     for (int w = 0; w < NW; ++w) tot += cx.wsum[w];
-    csync();
     return gain ? rsqrtf(tot / (float)K + a.eps) : 1.f;
 }
 
