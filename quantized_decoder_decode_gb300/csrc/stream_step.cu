@@ -239,10 +239,11 @@ struct Producer {
     uint32_t* err;
     Stop stop;
     uint32_t it = 0;
+    int s = 0;              // it % nslot and the parity of it / nslot, kept as counters
+    uint32_t par = 0;
 
     FQ_DEV bool wait_free() {
-        const int s = it % r.nslot;
-        const uint32_t ph = ((it / r.nslot) & 1u) ^ 1u;
+        const uint32_t ph = par ^ 1u;
         if (mbar_try_wait(&r.empty[s], ph)) return true;
         const long long t0 = clock64();
         while (!mbar_try_wait(&r.empty[s], ph)) {
@@ -260,12 +261,15 @@ struct Producer {
     // one item of up to two contiguous byte ranges (sizes multiples of 16) into the next slot
     FQ_DEV bool item(const void* a, uint32_t an, const void* b, uint32_t bn, uint32_t b_off) {
         if (!wait_free()) return false;
-        const int s = it % r.nslot;
         uint8_t* dst = r.buf + (size_t)s * SLOT;
         mbar_arrive_expect_tx(&r.full[s], an + bn);
         if (an) bulk_g2s(dst, a, an, &r.full[s]);
         if (bn) bulk_g2s(dst + b_off, b, bn, &r.full[s]);
         ++it;
+        if (++s == r.nslot) {
+            s = 0;
+            par ^= 1u;
+        }
         return true;
     }
     FQ_DEV bool rows(const QMat& W, const ProjPlan& pp) {
@@ -338,6 +342,8 @@ struct Cons {
     uint32_t* err;
     Stop stop;
     uint32_t it = 0;           // items consumed so far (same sequence as the producer's)
+    int s = 0;                 // it % nslot and the parity of it / nslot, kept as counters
+    uint32_t par = 0;
 
     // this CTA gives up: record `code`, stop the launch, leave at the next barrier
     FQ_DEV void fail(uint32_t code) {
@@ -347,11 +353,9 @@ struct Cons {
     }
 
     FQ_DEV bool wait_full(int lane) {
-        const int s = it % ring.nslot;
-        const uint32_t ph = (it / ring.nslot) & 1u;
-        if (mbar_try_wait(&ring.full[s], ph)) return true;
+        if (mbar_try_wait(&ring.full[s], par)) return true;
         const long long t0 = clock64();
-        while (!mbar_try_wait(&ring.full[s], ph)) {
+        while (!mbar_try_wait(&ring.full[s], par)) {
             if (ctl.abort) return false;
             if (clock64() - t0 > BUDGET) {
                 fail(512u);
@@ -360,11 +364,15 @@ struct Cons {
         }
         return true;
     }
-    FQ_DEV const uint8_t* slot() const { return ring.buf + (size_t)(it % ring.nslot) * SLOT; }
+    FQ_DEV const uint8_t* slot() const { return ring.buf + (size_t)s * SLOT; }
     FQ_DEV void release(int lane) {
         __syncwarp();
-        if (lane == 0) mbar_arrive(&ring.empty[it % ring.nslot]);
+        if (lane == 0) mbar_arrive(&ring.empty[s]);
         ++it;
+        if (++s == ring.nslot) {
+            s = 0;
+            par ^= 1u;
+        }
     }
 };
 
