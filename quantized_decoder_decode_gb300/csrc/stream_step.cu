@@ -768,12 +768,23 @@ FQ_DEV float stage(const StreamArgs& a, const unsigned long long* src, int K, ui
 FQ_DEV uint32_t tag_of(uint32_t seq, int layer) { return (seq << 8) | (uint32_t)(layer + 1); }
 
 // Attention of this CTA's unit plus the merge of its kv head's chunks (8 dims per slice).
+// A StreamLayer copied word by word (by one warp) into shared memory.
+FQ_DEV void copy_layer(StreamLayer& dst, const StreamLayer& src, int lane) {
+    static_assert(sizeof(StreamLayer) % 4 == 0, "copied as 32-bit words");
+    constexpr int NWD = (int)(sizeof(StreamLayer) / 4);
+    for (int i = lane; i < NWD; i += 32)
+        reinterpret_cast<uint32_t*>(&dst)[i] = reinterpret_cast<const uint32_t*>(&src)[i];
+}
+
+// `next`: the next layer's table entry, copied into shared memory by the last warp while
+// the others wait for q, k and v (null after the last layer).
 template <int G>
 FQ_DEV void attention_phase(const StreamArgs& a, const StreamLayer& lw, int layer, const SeqState& ss, uint32_t tag,
-                            Cons& cs, AttSmem<G>& as, const AttnUnit& u) {
+                            Cons& cs, AttSmem<G>& as, const AttnUnit& u, const StreamLayer* next, StreamLayer* next_dst) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int S = a.S;
     csync();
+    if (next && warp == NW - 1) copy_layer(*next_dst, *next, lane);
     if (u.active && warp < G + 2) {
         // q heads of the group, then k and v of the kv head, from the QKV exchange words
         const int row = warp < G ? (u.g * G + warp) : warp == G ? (a.Hq + u.g) : (a.Hq + a.Hkv + u.g);
@@ -933,6 +944,7 @@ __global__ void __launch_bounds__(NTH, 1) stream_step_kernel(const __grid_consta
     __shared__ CtlX cx;
     __shared__ ProjPlan pp[NPROJ];
     __shared__ AttnUnit au;
+    __shared__ StreamLayer sl[2];   // this layer's and the next layer's table entries
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + a.lay_bars);
     Ring ring{smem, bars, bars + MAXSLOT, a.nslot};
@@ -957,6 +969,7 @@ __global__ void __launch_bounds__(NTH, 1) stream_step_kernel(const __grid_consta
         au = attn_unit_of(a.Hkv, a.S, a.st->seq[0].pos);
     }
     if (tid < NPROJ) pp[tid] = a.plan[blockIdx.x * NPROJ + tid];
+    if (warp == NW - 1) copy_layer(sl[0], a.layers[0], lane);
     __syncthreads();
     const uint32_t seq = ld_volatile(&a.ctl[1]) & 0xFFFFFFu;
     const Stop stop{a.ctl + 2, seq + 1u};
@@ -980,10 +993,11 @@ __global__ void __launch_bounds__(NTH, 1) stream_step_kernel(const __grid_consta
     for (int q = 0; q < nq; ++q) {
         const int L = q / 5, ph = q - 5 * L;
         const bool lm = L == a.n_layers;
-        const StreamLayer& lw = a.layers[lm ? 0 : L];
+        const StreamLayer& lw = sl[lm ? 0 : (L & 1)];   // the layer's table entry, in shared memory
         const uint32_t tag = tag_of(seq, L);
         if (ph == 1) {
-            attention_phase<G>(a, lw, L, ss, tag, cs, as, au);
+            const bool more = L + 1 < a.n_layers;
+            attention_phase<G>(a, lw, L, ss, tag, cs, as, au, more ? &a.layers[L + 1] : nullptr, &sl[(L + 1) & 1]);
             csync();
             if (ctl.abort) break;
             continue;
