@@ -598,16 +598,18 @@ FQ_DEV bool proj_tasks(Cons& cs, const QMat& W, const ProjPlan& pp, const XStage
 
 // q / k head held as 4 dims per lane (dims 4l..4l+3) by one warp: RMSNorm with the gain,
 // then the rotate-half RoPE (pairs (i, i + 64): lane l < 16 holds i, lane l + 16 holds i + 64)
-FQ_DEV void norm_rope4(float v[4], const float* gain, const float2* rope_row, float eps, int lane) {
+// (gain: the lane's 4 gains; rot: cos/sin of its 4 dims at the position, both loaded by the
+// caller ahead of the values)
+FQ_DEV void norm_rope4(float v[4], const float (&gain)[4], const float2 (&rot)[4], float eps, int lane) {
     float ss = v[0] * v[0] + v[1] * v[1] + v[2] * v[2] + v[3] * v[3];
     ss = warp_sum(ss);
     const float inv = rsqrtf(ss / (float)HEAD_DIM + eps);
 #pragma unroll
-    for (int j = 0; j < 4; ++j) v[j] = v[j] * inv * gain[4 * lane + j];
+    for (int j = 0; j < 4; ++j) v[j] = v[j] * inv * gain[j];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
         const float partner = __shfl_xor_sync(0xFFFFFFFFu, v[j], 16);
-        const float2 cs = rope_row[(4 * lane + j) & 63];
+        const float2 cs = rot[j];
         v[j] = lane < 16 ? v[j] * cs.x - partner * cs.y : partner * cs.y + v[j] * cs.x;
     }
 }
@@ -788,6 +790,17 @@ FQ_DEV void attention_phase(const StreamArgs& a, const StreamLayer& lw, int laye
     if (u.active && warp < G + 2) {
         // q heads of the group, then k and v of the kv head, from the QKV exchange words
         const int row = warp < G ? (u.g * G + warp) : warp == G ? (a.Hq + u.g) : (a.Hq + a.Hkv + u.g);
+        // the gains and rotations of this lane's dims first: their loads overlap the wait
+        float gn[4] = {1.f, 1.f, 1.f, 1.f};
+        float2 rot[4] = {};
+        if (warp <= G) {
+            const float* g = warp < G ? lw.q_norm : lw.k_norm;
+            const float2* rope_row = a.rope + (size_t)ss.pos * (HEAD_DIM / 2);
+            const float4 g4 = *reinterpret_cast<const float4*>(g + 4 * lane);
+            gn[0] = g4.x; gn[1] = g4.y; gn[2] = g4.z; gn[3] = g4.w;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) rot[j] = rope_row[(4 * lane + j) & 63];
+        }
         float v[4];
         const unsigned long long* src = a.qkv + (size_t)row * HEAD_DIM + 4 * lane;
         const unsigned long long* const pp[2] = {src, src + 2};
@@ -795,14 +808,13 @@ FQ_DEV void attention_phase(const StreamArgs& a, const StreamLayer& lw, int laye
             if (cs.stop.seen()) cs.ctl.abort = 1;
             else cs.fail(2048u);
         }
-        const float2* rope_row = a.rope + (size_t)ss.pos * (HEAD_DIM / 2);
         if (warp < G) {
-            norm_rope4(v, lw.q_norm, rope_row, a.eps, lane);
+            norm_rope4(v, gn, rot, a.eps, lane);
             const float qscale = 1.4426950408889634f * rsqrtf((float)HEAD_DIM);
 #pragma unroll
             for (int j = 0; j < 4; ++j) as.qs[warp][4 * lane + j] = v[j] * qscale;
         } else {
-            if (warp == G) norm_rope4(v, lw.k_norm, rope_row, a.eps, lane);
+            if (warp == G) norm_rope4(v, gn, rot, a.eps, lane);
             const int which = warp - G;   // 0: k, 1: v
             uint16_t* dst = reinterpret_cast<uint16_t*>(warp == G ? ss.k : ss.v) +
                             (((size_t)layer * a.Hkv + u.g) * (size_t)ss.cap + ss.pos) * HEAD_DIM;
