@@ -618,14 +618,18 @@ FQ_DEV void norm_rope4(float v[4], const float (&gain)[4], const float2 (&rot)[4
 // positions follow the struct, [G][score capacity].
 template <int G>
 struct alignas(16) AttSmem {
+    // (the arrays read as float4 come first, at offsets that are multiples of 16)
     float qs[G][HEAD_DIM];            // normalised, rotated, scaled by log2(e)/sqrt(D)
     float ow[NW][G][HEAD_DIM];        // per-warp V sums for the cross-warp reduction
+    float po[G * MAXS * 8];           // merge: 8 dimensions of the slice of every chunk
     uint16_t kv_new[2][HEAD_DIM];     // the new position's k and v as stored (bf16)
     float hm[G], hl[G];               // per head: max score, sum of exp2(score - max)
-    float pm[G][MAXS], pl[G][MAXS];   // merge: (m, l) of every chunk of the kv head
-    float po[G * MAXS * 8];           //        and its 8 dimensions of the slice
+    float pm[G][MAXS], pl[G][MAXS];   //        and (m, l) of every chunk of the kv head
     float sc[1];                      // scores / weights [G][cap], cap = the plan's score capacity
 };
+static_assert(offsetof(AttSmem<1>, po) % 16 == 0 && offsetof(AttSmem<2>, po) % 16 == 0 &&
+                  offsetof(AttSmem<4>, po) % 16 == 0 && offsetof(AttSmem<1>, ow) % 16 == 0,
+              "float4 merge reads stay aligned");
 static_assert(sizeof(float) * HEAD_DIM % 16 == 0, "vector-accessed attention arrays stay 16-byte aligned");
 static_assert(NC % 32 == 0, "a warp stages whole blocks of 32 values");
 static_assert(NW >= 6, "the prologue needs G + 2 warps");
@@ -930,19 +934,38 @@ FQ_DEV void attention_phase(const StreamArgs& a, const StreamLayer& lw, int laye
         }
         csync();
         if (cs.ctl.abort) return;
-        if (tid < G * 8) {
-            const int h = tid / 8, k = tid % 8;
+        // warp h merges head h: lanes take chunks c = lane, lane + 32, ...; the maximum, the
+        // weight of every chunk and the 9 weighted sums are warp reductions
+        if (warp < G) {
+            const int h = warp;
             float M = -INFINITY;
-            for (int c = 0; c < S; ++c) M = fmaxf(M, as.pm[h][c]);
-            float Lsum = 0.f, O = 0.f;
-            for (int c = 0; c < S; ++c) {
+            for (int c = lane; c < S; c += 32) M = fmaxf(M, as.pm[h][c]);
+            M = warp_max(M);
+            float Lsum = 0.f, O[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            for (int c = lane; c < S; c += 32) {
                 const float m = as.pm[h][c];
                 if (m == -INFINITY) continue;
                 const float wgt = exp2f(m - M);
                 Lsum = fmaf(as.pl[h][c], wgt, Lsum);
-                O = fmaf(as.po[(h * S + c) * 8 + k], wgt, O);
+                const float4 p0 = *reinterpret_cast<const float4*>(&as.po[(h * S + c) * 8]);
+                const float4 p1 = *reinterpret_cast<const float4*>(&as.po[(h * S + c) * 8 + 4]);
+                O[0] = fmaf(p0.x, wgt, O[0]); O[1] = fmaf(p0.y, wgt, O[1]);
+                O[2] = fmaf(p0.z, wgt, O[2]); O[3] = fmaf(p0.w, wgt, O[3]);
+                O[4] = fmaf(p1.x, wgt, O[4]); O[5] = fmaf(p1.y, wgt, O[5]);
+                O[6] = fmaf(p1.z, wgt, O[6]); O[7] = fmaf(p1.w, wgt, O[7]);
             }
-            xw_store(a.o + (size_t)(u.g * G + h) * HEAD_DIM + 8 * sl + k, O / Lsum, tag);
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) {
+                Lsum += __shfl_xor_sync(0xFFFFFFFFu, Lsum, off);
+#pragma unroll
+                for (int k = 0; k < 8; ++k) O[k] += __shfl_xor_sync(0xFFFFFFFFu, O[k], off);
+            }
+            if (lane < 8) {
+                float o = O[0];
+#pragma unroll
+                for (int k = 1; k < 8; ++k) o = lane == k ? O[k] : o;
+                xw_store(a.o + (size_t)(u.g * G + h) * HEAD_DIM + 8 * sl + lane, o / Lsum, tag);
+            }
         }
     }
 }
