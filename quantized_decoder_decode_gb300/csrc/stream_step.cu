@@ -634,6 +634,19 @@ static_assert(sizeof(float) * HEAD_DIM % 16 == 0, "vector-accessed attention arr
 static_assert(NC % 32 == 0, "a warp stages whole blocks of 32 values");
 static_assert(NW >= 6, "the prologue needs G + 2 warps");
 
+// Two independent fused multiply-adds in one instruction (the packed f32x2 form): each half is
+// exactly fmaf(a, b, c) of that half.
+FQ_DEV void ffma2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
+    asm("{\n\t.reg .b64 a, b, d;\n\t"
+        "mov.b64 a, {%2, %3};\n\t"
+        "mov.b64 b, {%4, %5};\n\t"
+        "mov.b64 d, {%0, %1};\n\t"
+        "fma.rn.f32x2 d, a, b, d;\n\t"
+        "mov.b64 {%0, %1}, d;\n\t}"
+        : "+f"(d0), "+f"(d1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
 // Scores of K rows row = 4 NW step + 4 warp + (lane >> 3) of an item of n rows (8 lanes per row,
 // 16 dims each: 8i..8i+7 and 64+8i..64+8i+7); lane i == h of the row's group writes head h's
 // score to sc[h][base + row].
@@ -659,10 +672,7 @@ FQ_DEV void att_scores(const float (&q)[G][16], const uint8_t* kb, int n, int ba
             for (int h = 0; h < G; ++h) {
                 float t0 = 0.f, t1 = 0.f;
 #pragma unroll
-                for (int e = 0; e < 16; e += 2) {
-                    t0 = fmaf(q[h][e], k[e], t0);
-                    t1 = fmaf(q[h][e + 1], k[e + 1], t1);
-                }
+                for (int e = 0; e < 16; e += 2) ffma2(t0, t1, q[h][e], q[h][e + 1], k[e], k[e + 1]);
                 s[h] = t0 + t1;
             }
         }
@@ -687,8 +697,8 @@ FQ_DEV void att_values(float (&acc)[G][4], const uint8_t* vb, int n, int base, c
 #pragma unroll
         for (int h = 0; h < G; ++h) {
             const float p = sc[h * cap + base + row];
-#pragma unroll
-            for (int d = 0; d < 4; ++d) acc[h][d] = fmaf(p, vf[d], acc[h][d]);
+            ffma2(acc[h][0], acc[h][1], p, p, vf[0], vf[1]);
+            ffma2(acc[h][2], acc[h][3], p, p, vf[2], vf[3]);
         }
     }
 }
