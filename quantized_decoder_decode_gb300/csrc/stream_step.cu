@@ -452,6 +452,30 @@ FQ_DEV int dp4a_uu(uint32_t a, uint32_t b, int c) {
     return d;
 }
 
+// Two independent fused multiply-adds in one instruction (the packed f32x2 form): each half is
+// exactly fmaf(a, b, c) of that half.
+FQ_DEV void ffma2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
+    asm("{\n\t.reg .b64 a, b, d;\n\t"
+        "mov.b64 a, {%2, %3};\n\t"
+        "mov.b64 b, {%4, %5};\n\t"
+        "mov.b64 d, {%0, %1};\n\t"
+        "fma.rn.f32x2 d, a, b, d;\n\t"
+        "mov.b64 {%0, %1}, d;\n\t}"
+        : "+f"(d0), "+f"(d1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
+// Two independent multiplies in one instruction (packed f32x2): (d0, d1) = (a0 b0, a1 b1).
+FQ_DEV void fmul2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
+    asm("{\n\t.reg .b64 a, b, d;\n\t"
+        "mov.b64 a, {%2, %3};\n\t"
+        "mov.b64 b, {%4, %5};\n\t"
+        "mul.rn.f32x2 d, a, b;\n\t"
+        "mov.b64 {%0, %1}, d;\n\t}"
+        : "=f"(d0), "=f"(d1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
 template <int FMT> struct PCfg;
 // rows per task R; elements per unit (one lane's share of a row per pass)
 template <> struct PCfg<FMT_Q8_0> { static constexpr int R = 4, UE = 16; };
@@ -545,8 +569,14 @@ FQ_DEV void task_dot(const uint8_t* slot, int nr, int K, int row0, int ua, int u
                 const uint32_t X1 = hp ? a0 >> 4 : b1, Y1 = hp ? b1 >> 2 : b1;
                 const uint32_t sc0 = (X0 & 15u) | (Y0 & 48u), sc1 = ((X0 >> 8) & 15u) | ((Y0 >> 8) & 48u);
                 const uint32_t mn0 = (X1 & 15u) | (Y1 & 48u), mn1 = ((X1 >> 8) & 15u) | ((Y1 >> 8) & 48u);
-                acc[r] += d * (float)sc0 * s_lo * (float)(Alo * 256 + Blo) - dmin * (float)mn0 * m_lo +
-                          d * (float)sc1 * s_hi * (float)(Ahi * 256 + Bhi) - dmin * (float)mn1 * m_hi;
+                // both sub-blocks at once (packed pairs): d sc s (A 256 + B) - dmin mn m
+                float t0, t1, u0, u1;
+                fmul2(t0, t1, d, d, (float)sc0, (float)sc1);
+                fmul2(t0, t1, t0, t1, s_lo, s_hi);
+                fmul2(u0, u1, -dmin, -dmin, (float)mn0, (float)mn1);
+                fmul2(u0, u1, u0, u1, m_lo, m_hi);
+                ffma2(u0, u1, t0, t1, (float)(Alo * 256 + Blo), (float)(Ahi * 256 + Bhi));
+                acc[r] += u0 + u1;
             }
         }
     }
@@ -633,19 +663,6 @@ static_assert(offsetof(AttSmem<1>, po) % 16 == 0 && offsetof(AttSmem<2>, po) % 1
 static_assert(sizeof(float) * HEAD_DIM % 16 == 0, "vector-accessed attention arrays stay 16-byte aligned");
 static_assert(NC % 32 == 0, "a warp stages whole blocks of 32 values");
 static_assert(NW >= 6, "the prologue needs G + 2 warps");
-
-// Two independent fused multiply-adds in one instruction (the packed f32x2 form): each half is
-// exactly fmaf(a, b, c) of that half.
-FQ_DEV void ffma2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
-    asm("{\n\t.reg .b64 a, b, d;\n\t"
-        "mov.b64 a, {%2, %3};\n\t"
-        "mov.b64 b, {%4, %5};\n\t"
-        "mov.b64 d, {%0, %1};\n\t"
-        "fma.rn.f32x2 d, a, b, d;\n\t"
-        "mov.b64 {%0, %1}, d;\n\t}"
-        : "+f"(d0), "+f"(d1)
-        : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
-}
 
 // Scores of K rows row = 4 NW step + 4 warp + (lane >> 3) of an item of n rows (8 lanes per row,
 // 16 dims each: 8i..8i+7 and 64+8i..64+8i+7); lane i == h of the row's group writes head h's
