@@ -499,12 +499,9 @@ FQ_DEV void task_dot(const uint8_t* slot, int nr, int K, int row0, int ua, int u
             const uint4 h = *reinterpret_cast<const uint4*>(x.hi + 16 * u);
             const uint4 l = *reinterpret_cast<const uint4*>(x.lo + 16 * u);
             const float s = x.sc[u >> 1];
-#pragma unroll
-            for (int r = 0; r < R; ++r) {
-                const int row = row0 + r;
-                if (!FULL && row >= nr) break;
+            auto dot = [&](int row, float& d, float& f) {   // one row's block: fp16 scale, integer sum
                 const uint4 c = *reinterpret_cast<const uint4*>(slot + (size_t)row * K + 16 * u);
-                const float d = h2f(sc[row * K32 + (u >> 1)]);
+                d = h2f(sc[row * K32 + (u >> 1)]);
                 int A = dp4a_ss(c.x, h.x, 0);
                 A = dp4a_ss(c.y, h.y, A);
                 A = dp4a_ss(c.z, h.z, A);
@@ -513,7 +510,28 @@ FQ_DEV void task_dot(const uint8_t* slot, int nr, int K, int row0, int ua, int u
                 B = dp4a_su(c.y, l.y, B);
                 B = dp4a_su(c.z, l.z, B);
                 B = dp4a_su(c.w, l.w, B);
-                acc[r] = fmaf(d * s, (float)(A * 256 + B), acc[r]);
+                f = (float)(A * 256 + B);
+            };
+            if constexpr (FULL) {
+                // rows in pairs: d s and the accumulation as packed f32x2 (the same two
+                // roundings per row as the scalar form)
+#pragma unroll
+                for (int r = 0; r < R; r += 2) {
+                    float d0, f0, d1, f1;
+                    dot(row0 + r, d0, f0);
+                    dot(row0 + r + 1, d1, f1);
+                    fmul2(d0, d1, d0, d1, s, s);
+                    ffma2(acc[r], acc[r + 1], d0, d1, f0, f1);
+                }
+            } else {
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    const int row = row0 + r;
+                    if (row >= nr) break;
+                    float d, f;
+                    dot(row, d, f);
+                    acc[r] = fmaf(d * s, f, acc[r]);
+                }
             }
         }
     } else {
