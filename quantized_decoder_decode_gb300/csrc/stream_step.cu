@@ -682,17 +682,16 @@ static_assert(sizeof(float) * HEAD_DIM % 16 == 0, "vector-accessed attention arr
 static_assert(NC % 32 == 0, "a warp stages whole blocks of 32 values");
 static_assert(NW >= 6, "the prologue needs G + 2 warps");
 
-// Scores of K rows row = 4 NW step + 4 warp + (lane >> 3) of an item of n rows (8 lanes per row,
-// 16 dims each: 8i..8i+7 and 64+8i..64+8i+7); lane i == h of the row's group writes head h's
-// score to sc[h][base + row].
+// Scores of the K rows of groups first, first + NW, ... of an item of n rows (group g: rows
+// 4g + (lane >> 3); 8 lanes per row, 16 dims each: 8i..8i+7 and 64+8i..64+8i+7); lane i == h
+// of the row's group writes head h's score to sc[h][base + row].  The caller rotates `first`
+// from item to item, so that the groups of the whole chunk go round the warps evenly.
 template <int G>
-FQ_DEV void att_scores(const float (&q)[G][16], const uint8_t* kb, int n, int base, float* sc, int cap, int warp,
+FQ_DEV void att_scores(const float (&q)[G][16], const uint8_t* kb, int n, int base, float* sc, int cap, int first,
                        int lane) {
     const int j = lane >> 3, i = lane & 7;
-#pragma unroll
-    for (int step = 0; step < (TP + 4 * NW - 1) / (4 * NW); ++step) {
-        const int row = 4 * NW * step + 4 * warp + j;
-        if (4 * NW * step + 4 * warp >= n) break;   // the whole group of four rows is past the end
+    for (int grp = first; 4 * grp < n; grp += NW) {
+        const int row = 4 * grp + j;
         const bool valid = row < n;
         float s[G];
 #pragma unroll
@@ -721,12 +720,12 @@ FQ_DEV void att_scores(const float (&q)[G][16], const uint8_t* kb, int n, int ba
     }
 }
 
-// V rows warp, warp + NW, ... of an item of n rows weighted by p = sc[h][base + row]: lane
-// takes dims 4 lane .. 4 lane + 3 of every head.
+// V rows first, first + NW, ... of an item of n rows weighted by p = sc[h][base + row]: lane
+// takes dims 4 lane .. 4 lane + 3 of every head (`first` rotates from item to item).
 template <int G>
-FQ_DEV void att_values(float (&acc)[G][4], const uint8_t* vb, int n, int base, const float* sc, int cap, int warp,
+FQ_DEV void att_values(float (&acc)[G][4], const uint8_t* vb, int n, int base, const float* sc, int cap, int first,
                        int lane) {
-    for (int row = warp; row < n; row += NW) {
+    for (int row = first; row < n; row += NW) {
         const uint2 v = *reinterpret_cast<const uint2*>(vb + (size_t)row * 256 + 8 * lane);
         const float vf[4] = {bf_lo(v.x), bf_hi(v.x), bf_lo(v.y), bf_hi(v.y)};
 #pragma unroll
@@ -899,7 +898,8 @@ FQ_DEV void attention_phase(const StreamArgs& a, const StreamLayer& lw, int laye
             }
         for (int t = 0; t < nt; ++t) {
             if (!cs.wait_full(lane)) break;
-            att_scores<G>(q, cs.slot(), min(TP, n - t * TP), t * TP, sc, cap, warp, lane);
+            const int rot = (warp - (t * (TP / 4)) % NW + NW) % NW;   // this warp's first group of item t
+            att_scores<G>(q, cs.slot(), min(TP, n - t * TP), t * TP, sc, cap, rot, lane);
             cs.release(lane);
         }
         if (owns_new && warp == 0)
@@ -935,7 +935,8 @@ FQ_DEV void attention_phase(const StreamArgs& a, const StreamLayer& lw, int laye
         for (int d = 0; d < 4; ++d) acc[h][d] = 0.f;
     for (int t = 0; t < nt; ++t) {
         if (!cs.wait_full(lane)) break;
-        att_values<G>(acc, cs.slot(), min(TP, n - t * TP), t * TP, sc, cap, warp, lane);
+        const int rot = (warp - (t * TP) % NW + NW) % NW;   // this warp's first row of item t
+        att_values<G>(acc, cs.slot(), min(TP, n - t * TP), t * TP, sc, cap, rot, lane);
         cs.release(lane);
     }
     if (owns_new && warp == 0)
