@@ -82,12 +82,15 @@ KV_ELEM_BYTES = {"f32": 4.0, "bf16": 2.0, "q8_0": 34 / 32}   # per cached value 
 
 
 def workload_of(args):
-    """The named workload, with its cache dtype replaced when --kv asks for another."""
+    """The named workload, with its cache dtype replaced when --kv asks for another, and its
+    layer count when --layers asks for fewer (a small case of the same shapes for profilers)."""
     import dataclasses
     import synth.workloads as wl
     w = wl.WORKLOADS[args.workload]
     if getattr(args, "kv", None) and args.kv != w.kv_dtype:
         w = dataclasses.replace(w, kv_dtype=args.kv)
+    if getattr(args, "layers", None):
+        w = dataclasses.replace(w, dims=dataclasses.replace(w.dims, num_layers=args.layers))
     return w
 
 
@@ -839,6 +842,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-subrecords", action="store_true",
                     help="skip the 8B batch-1 / batch-32 and single-layer records of the default line")
+    ap.add_argument("--layers", type=int, default=None,
+                    help="fewer layers of the workload's shapes: a small case for profilers, not a bench line")
     ap.add_argument("--kv", default=None, choices=["bf16", "q8_0"],
                     help="cache dtype in place of the workload's own (q8_0: the integer-score cache)")
     ap.add_argument("--verify", action="store_true",
