@@ -64,3 +64,14 @@ def test_step_bytes_of_a_chain_counts_the_growing_context():
                                         + sb["kv_write"])
     b32 = bench.step_bytes_of(wl.WORKLOADS["qwen3-8b-batch32"], [512, 4096])
     assert b32["kv_write"] == 32 * 2 * 36 * 8 * 128 * 2
+
+
+def test_layers_switch_keeps_the_shapes_and_names_the_reduced_model():
+    # a small profiling case: only the layer count changes, and the workload string says so
+    args = argparse.Namespace(workload="qwen3-8b-q4k", kv=None, layers=4)
+    w = bench.workload_of(args)
+    full = bench.workload_of(argparse.Namespace(workload="qwen3-8b-q4k", kv=None, layers=None))
+    assert w.dims.num_layers == 4 and full.dims.num_layers == 36
+    assert w.dims.hidden_size == full.dims.hidden_size and w.weight_dtype == full.weight_dtype
+    assert w.context == full.context
+    assert "4 layers" in bench.config_dict(w)["workload"]
