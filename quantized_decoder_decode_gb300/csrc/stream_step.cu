@@ -12,7 +12,7 @@
 //     shared-memory slots with bulk asynchronous copies (cp.async.bulk + mbarrier), as fast
 //     as slots free up.  It never waits for an activation, so HBM keeps streaming while the
 //     consumers wait for the other CTAs;
-//   * eight consumer warps run the step's phases on what has landed.  Per layer:
+//   * eleven consumer warps run the step's phases on what has landed.  Per layer:
 //       QKV   RMSNorm(x) . W_qkv rows                        (x: the previous layer's output)
 //       ATT   per-head QK-RMSNorm, half-rope, KV append, attention over the CTA's chunk of
 //             one kv head's cached positions (split-K flash decode; partial m, l, o)
