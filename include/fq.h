@@ -270,9 +270,10 @@ fq_status fq_layer_step_noalloc(const fq_model* m, uint32_t layer, fq_kv* kv, ui
  * implementations of the same step).  Set them between steps, not while a step of the model
  * is in flight on another thread; a change drops the CUDA graphs captured so far.
  *   FQ_OPT_STEP_PATH          FQ_PATH_AUTO (default): a batch-1 step of a dense model with
- *                             a bf16 cache runs as one streamed persistent kernel whose
- *                             producer warps copy the step's weights and cached K/V into
- *                             shared memory ahead of the activations; FQ_PATH_KERNELS: the
+ *                             a bf16 cache runs as one streamed persistent kernel (one
+ *                             CTA per SM) whose producer warp copies the CTA's share of the
+ *                             step's weights and cached K/V into shared memory ahead of the
+ *                             activations; FQ_PATH_KERNELS: the
  *                             sequence of per-stage kernels (replayed from a CUDA graph).
  *   FQ_OPT_DEPENDENT_LAUNCH   0 (default) / 1: programmatic dependent launch between the
  *                             kernels of the sequence.
