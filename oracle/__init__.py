@@ -73,6 +73,7 @@ def lib():
                 "or_model_set_layer": ([vp, i32] + [vp] * 15, None),
                 "or_cache_new": ([vp, i32], vp), "or_cache_free": ([vp], None), "or_cache_len": ([vp], i32),
                 "or_cache_write": ([vp, i32, i32, i32, vp, vp], i32), "or_cache_set_len": ([vp, i32], i32),
+                "or_cache_keep_current": ([vp, i32], i32),
                 "or_cache_read": ([vp, i32, i32, i32, vp, vp], i32),
                 "or_layer_step": ([vp, i32, vp, i32, vp, vp, vp], i32),
                 "or_qkv_project": ([vp, i32, vp, i32, vp, vp, vp], i32),
@@ -368,6 +369,13 @@ class Cache:
         rc = lib().or_cache_set_len(self._h, n)
         if rc:
             raise OracleError(rc, "or_cache_set_len")
+
+    def keep_current(self, keep: bool) -> None:
+        """While set, steps attend over the rows already written at their position (see
+        `write`) instead of storing the rows they compute."""
+        rc = lib().or_cache_keep_current(self._h, int(bool(keep)))
+        if rc:
+            raise OracleError(rc, "or_cache_keep_current")
 
     def write(self, layer: int, pos0: int, k: np.ndarray, v: np.ndarray) -> None:
         """k, v: [n, Hkv, D] float32 values, uint16 bf16 bit patterns, or uint8 ggml Q8_0

@@ -400,6 +400,7 @@ struct or_model {
 struct or_cache {
     const or_model* m;
     int cap, len;
+    int keep = 0;              // layer steps attend over the rows already at `len` instead of writing theirs
     std::vector<float> k, v;   // [layer][n_kv][cap][head_dim], values in the cache dtype
     size_t idx(int layer, int h, int pos) const {
         const or_dims& d = m->d;
@@ -574,6 +575,12 @@ int or_cache_write(or_cache* c, int layer, int pos0, int n, const float* k, cons
     return OR_OK;
 }
 
+int or_cache_keep_current(or_cache* c, int keep) {
+    if (!c) return OR_INVALID_ARGUMENT;
+    c->keep = keep != 0;
+    return OR_OK;
+}
+
 int or_cache_set_len(or_cache* c, int len) {
     if (len < 0 || len > c->cap) return OR_INVALID_ARGUMENT;
     c->len = len;
@@ -619,10 +626,11 @@ int or_layer_step_route(const or_model* m, int layer, or_cache* c, int pos, doub
     std::vector<double> xn(d.hidden), q(qd), k(kvd), v(kvd), o(qd), dx(d.hidden);
     or_rmsnorm(x, d.hidden, w.attn_norm, d.eps, xn.data());
     qkv_project(m, w, xn.data(), pos, q.data(), k.data(), v.data(), false);
-    for (int h = 0; h < d.n_kv; ++h) {
-        to_cache(m, &k[(size_t)h * D], D, &c->k[c->idx(layer, h, pos)]);
-        to_cache(m, &v[(size_t)h * D], D, &c->v[c->idx(layer, h, pos)]);
-    }
+    if (!c->keep)
+        for (int h = 0; h < d.n_kv; ++h) {
+            to_cache(m, &k[(size_t)h * D], D, &c->k[c->idx(layer, h, pos)]);
+            to_cache(m, &v[(size_t)h * D], D, &c->v[c->idx(layer, h, pos)]);
+        }
 #pragma omp parallel for schedule(static)
     for (int h = 0; h < d.n_q; ++h) {   // heads are independent outputs
         int g = h / group;

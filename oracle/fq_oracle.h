@@ -94,6 +94,10 @@ int  or_cache_len(const or_cache* c);
  * dequantised Q8_0 rows); returns 0 or an error code */
 int  or_cache_write(or_cache* c, int layer, int pos0, int n, const float* k, const float* v);
 int  or_cache_set_len(or_cache* c, int len);
+/* keep != 0: later layer steps on this cache attend over the k/v rows already written at the
+ * step's position (or_cache_write) instead of storing their own; the step still computes q,
+ * k and v.  A test uses it to continue from another implementation's rounded rows. */
+int  or_cache_keep_current(or_cache* c, int keep);
 /* read back [n][n_kv][head_dim] of one layer */
 int  or_cache_read(const or_cache* c, int layer, int pos0, int n, float* k, float* v);
 

@@ -470,6 +470,33 @@ def test_cache_holds_bf16_values_after_step():
     assert np.any(k != 0)
 
 
+def test_keep_current_attends_over_the_rows_written_at_the_position():
+    m, _, d, _ = tiny_model()
+    a, b, c = m.new_cache(8), m.new_cache(8), m.new_cache(8)
+    for p, t in enumerate([3, 17, 40]):
+        for cache in (a, b, c):
+            m.decode_step(cache, t, p, logits=False)
+    ref, ref_lo, _, _ = m.decode_step(a, 5, 3, trace=True)
+    # the step's own rows, written beforehand and kept: the same step bit for bit
+    for L in range(d.num_layers):
+        k, v = a.read(L, 3, 1)
+        b.write(L, 3, k, v)
+        c.write(L, 3, k, 2 * v if L == 1 else v)
+    b.keep_current(True)
+    lg = m.decode_step(b, 5, 3)
+    b.keep_current(False)
+    assert np.array_equal(lg, ref) and b.len == 4
+    # other rows: layer 0 is untouched, layer 1 attends over the doubled v row, which stays
+    c.keep_current(True)
+    lg2, lo2, _, _ = m.decode_step(c, 5, 3, trace=True)
+    c.keep_current(False)
+    assert np.array_equal(lo2[0], ref_lo[0]) and not np.array_equal(lo2[1], ref_lo[1])
+    assert np.array_equal(c.read(1, 3, 1)[1], 2 * a.read(1, 3, 1)[1])
+    # without the flag the step stores its own rows again
+    c.set_len(3)
+    assert np.array_equal(m.decode_step(c, 5, 3), ref)
+
+
 def test_q8_cache_holds_quantised_rows_after_step():
     m, _, d, _ = tiny_model(TINY_Q8KV, kv="q8_0")
     mf, _, _, _ = tiny_model(TINY_Q8KV, kv="f32")
