@@ -328,7 +328,11 @@ void launch_t(const GemvArgs& a, cudaStream_t s, bool pdl) {
     // one wave of resident CTAs over (row tiles, activation-row groups)
     const int groups = a.route ? a.max_experts : (a.B + NBG - 1) / NBG;
     const int per_group = std::max(1, Occ<FMT, R, NBG>::ctas_per_sm * g_sms / groups);
-    dim3 grid(a.route ? tiles : std::min(tiles, per_group), groups);
+    // expert mode: up to eight waves of CTAs over the possible experts (measured best of 2, 4,
+    // 8, 16 and one CTA per tile), each looping over row tiles of its expert, so that an
+    // expert's token inputs are staged once per CTA rather than once per tile
+    const int per_expert = std::max(1, 8 * Occ<FMT, R, NBG>::ctas_per_sm * g_sms / std::max(1, groups));
+    dim3 grid(std::min(tiles, a.route ? per_expert : per_group), groups);
     size_t smem = (size_t)NBG * xpad_len<FMT>(a.W.K) * 4 + (FMT == FMT_Q4_K ? (size_t)NBG * (a.W.K / 16) * 4 : 0) +
                   (size_t)(WARPS * R * NBG + WARPS * NBG) * 4;
     auto kern = gemv_kernel<FMT, R, NBG>;
