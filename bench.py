@@ -54,13 +54,15 @@ STEP_TRAFFIC = {
 STEP_SOURCES = ["stream_step.cu", "kernels.h", "quant.cuh", "tma.cuh", "common.cuh"]
 
 
-def step_source_hash() -> str:
-    """Hash of the streamed step's sources with comments and blank lines removed, so that a
-    comment edit does not count as a changed kernel."""
+def step_source_hash(base: str = None) -> str:
+    """Hash of the streamed step's sources (in `base`, by default the package's csrc) with
+    comments and blank lines removed, so that a comment edit does not count as a changed
+    kernel."""
     import hashlib
     import re
     h = hashlib.sha256()
-    base = os.path.join(os.path.dirname(os.path.abspath(__file__)), "quantized_decoder_decode_gb300", "csrc")
+    if base is None:
+        base = os.path.join(os.path.dirname(os.path.abspath(__file__)), "quantized_decoder_decode_gb300", "csrc")
     for f in STEP_SOURCES:
         with open(os.path.join(base, f), encoding="utf-8") as fh:
             text = fh.read()

@@ -1,7 +1,11 @@
 """Host-side accounting of bench.py, without a GPU: the algorithmic bytes a step moves (the
 numerator of every roofline figure the bench reports) against the per-configuration totals
-derived from the Qwen3 shapes and the ggml block sizes, and the --kv workload switch."""
+derived from the Qwen3 shapes and the ggml block sizes, the --kv and --layers workload
+switches, and the source hash that keeps a DRAM-traffic record tied to the kernel it was
+taken on."""
 import argparse
+import os
+import shutil
 
 import numpy as np
 import pytest
@@ -75,3 +79,17 @@ def test_layers_switch_keeps_the_shapes_and_names_the_reduced_model():
     assert w.dims.hidden_size == full.dims.hidden_size and w.weight_dtype == full.weight_dtype
     assert w.context == full.context
     assert "4 layers" in bench.config_dict(w)["workload"]
+
+
+def test_step_source_hash_ignores_comments_but_not_code(tmp_path):
+    src = os.path.join(os.path.dirname(os.path.abspath(bench.__file__)), "quantized_decoder_decode_gb300", "csrc")
+    for f in bench.STEP_SOURCES:
+        shutil.copy(os.path.join(src, f), tmp_path / f)
+    h0 = bench.step_source_hash(str(tmp_path))
+    assert h0 == bench.step_source_hash()
+    k = tmp_path / "stream_step.cu"
+    text = k.read_text()
+    k.write_text("// a comment line\n/* a block\n   comment */\n\n" + text.replace("{", "{  // trailing", 1))
+    assert bench.step_source_hash(str(tmp_path)) == h0
+    k.write_text(text.replace("constexpr int SLOT = 16384;", "constexpr int SLOT = 32768;"))
+    assert bench.step_source_hash(str(tmp_path)) != h0
